@@ -1,0 +1,466 @@
+/*
+ * w12_oracle.c -- plain, slow CPU oracle for the W12 hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library calls, links or
+ * includes this file; only the test suite, the smoke check and the CPU-baseline
+ * leg of the benchmark load it (through ctypes).  It shares no source with the
+ * CUDA library: every constant, table and layout rule below is written out
+ * here on its own.
+ *
+ * What it computes, and where each piece comes from:
+ *
+ *  - The W12 format: a BF16 weight is split into three 4-bit planes and
+ *    rebuilt bit for bit ("SpecPilot" summary pages, p5 "Reasons", second
+ *    bullet; p4 "项目介绍", second paragraph: decoded bit-exactly inside the
+ *    GEMM).  The pages give no layout; the one coded here is the documented
+ *    W12 v1 layout: plane H = sign and the top 3 mantissa bits, plane L = the
+ *    low 4 mantissa bits, plane E = the exponent as a 4-bit offset from a base
+ *    shared by a group of 128 consecutive k of one output column, with code 15
+ *    meaning "escape: the true exponent is in a side list".
+ *  - The GEMM: y[m,n] = sum_k x[m,k] * w[k,n], accumulated in fp64 in k order
+ *    (products of two bf16 values are exact in fp64).
+ *  - Greedy verification (p5 "Risks", third bullet: under greedy decoding
+ *    every committed token is the target model's own choice; p4 "结果与验证":
+ *    token-by-token check): per position the lowest index of the row maximum,
+ *    then the longest prefix of draft tokens that agree, then the target's
+ *    token at the first disagreement.
+ *
+ * Build: gcc -O2 -std=c11 -shared -fPIC (oracle/build.py).  Single thread.
+ */
+#include <stdint.h>
+#include <stddef.h>
+#include <string.h>
+#include <stdlib.h>
+#include <math.h>
+
+/* Status codes.  The numbering is the one the W12 C interface documents, so a
+ * test can compare the two sides' rejections of the same bad input. */
+#define W12REF_OK 0
+#define W12REF_ERR_ARG 1
+#define W12REF_ERR_SHAPE 2
+#define W12REF_ERR_BLOB 5
+#define W12REF_ERR_TOO_MANY_ESCAPES 6
+
+/* Input orientation of the weight matrix handed to the encoder. */
+#define W12REF_LAYOUT_KN 0 /* w[k*N + n] : row-major [K][N]               */
+#define W12REF_LAYOUT_NK 1 /* w[n*K + k] : row-major [N][K] (out x in)    */
+
+#define W12REF_GROUP 128   /* weights per group, along k                  */
+#define W12REF_WINDOW 15   /* exponent offsets 0..14 are coded directly   */
+#define W12REF_ESC_CODE 15 /* code meaning "exponent is in the side list" */
+#define W12REF_MAX_BASE 241 /* largest base: 241 + 14 = 255                */
+#define W12REF_MAX_ESC (1u << 24)
+
+typedef struct {
+    uint32_t version;
+    uint32_t reserved;
+    int64_t K, N, G;
+    uint64_t off_h, off_l, off_e, off_meta, off_esc;
+    uint64_t n_esc;
+    uint64_t total_bytes;
+} w12ref_desc;
+
+/* ---------------------------------------------------------------------- */
+/* BF16 fields                                                             */
+/* ---------------------------------------------------------------------- */
+
+static unsigned bf16_sign(uint16_t v) { return (v >> 15) & 1u; }
+static unsigned bf16_exp(uint16_t v) { return (v >> 7) & 0xFFu; }
+static unsigned bf16_man(uint16_t v) { return v & 0x7Fu; }
+
+static double bf16_to_double(uint16_t v)
+{
+    uint32_t u = (uint32_t)v << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static uint16_t weight_at(const uint16_t *w, int64_t K, int64_t N, int layout, int64_t k, int64_t n)
+{
+    return layout == W12REF_LAYOUT_KN ? w[k * N + n] : w[n * K + k];
+}
+
+/* ---------------------------------------------------------------------- */
+/* Logical codec: base, codes, escapes                                      */
+/* ---------------------------------------------------------------------- */
+
+/* Base of one group of 128 exponents: the b in [0, 241] whose window
+ * [b, b+14] holds the most exponents; among equally good b, the largest. */
+int w12ref_group_base(const uint16_t *vals)
+{
+    int best_b = 0, best_cover = -1;
+    for (int b = 0; b <= W12REF_MAX_BASE; ++b) {
+        int cover = 0;
+        for (int i = 0; i < W12REF_GROUP; ++i) {
+            int e = (int)bf16_exp(vals[i]);
+            if (e >= b && e <= b + W12REF_WINDOW - 1)
+                ++cover;
+        }
+        if (cover >= best_cover) { /* ">=": a later (larger) b wins a tie */
+            best_cover = cover;
+            best_b = b;
+        }
+    }
+    return best_b;
+}
+
+/* Code of one exponent under base b: the offset, or 15 for an escape. */
+static unsigned exp_code(unsigned e, unsigned b)
+{
+    if (e >= b && e <= b + W12REF_WINDOW - 1)
+        return e - b;
+    return W12REF_ESC_CODE;
+}
+
+static void gather_group(const uint16_t *w, int64_t K, int64_t N, int layout, int64_t g,
+                         uint16_t *out)
+{
+    int64_t kg_per_col = K / W12REF_GROUP;
+    int64_t n = g / kg_per_col, kg = g % kg_per_col;
+    for (int p = 0; p < W12REF_GROUP; ++p)
+        out[p] = weight_at(w, K, N, layout, kg * W12REF_GROUP + p, n);
+}
+
+/* ---------------------------------------------------------------------- */
+/* Physical layout v1                                                      */
+/* ---------------------------------------------------------------------- */
+/*
+ * Each plane is column-major: column n owns K/2 contiguous bytes.  A
+ * little-endian 32-bit word of a plane covers the 8 weights k0..k0+7
+ * (k0 a multiple of 8); its nibble q (bits 4q..4q+3) holds the nibble of
+ * weight k0 + PERM[q], with one permutation per plane.
+ */
+static const int PERM_H[8] = {4, 0, 5, 1, 6, 2, 7, 3};
+static const int PERM_L[8] = {0, 5, 1, 6, 2, 7, 3, 4};
+static const int PERM_E[8] = {0, 2, 4, 6, 1, 3, 5, 7};
+
+static int slot_of(const int *perm, int r)
+{
+    for (int q = 0; q < 8; ++q)
+        if (perm[q] == r)
+            return q;
+    return -1; /* unreachable: each table is a permutation of 0..7 */
+}
+
+static uint64_t nibble_byte(int64_t K, int64_t k, int64_t n, const int *perm, int *shift)
+{
+    int64_t k0 = k - (k % 8);
+    int q = slot_of(perm, (int)(k - k0));
+    *shift = (q % 2) * 4; /* even slots are the low nibble of their byte */
+    return (uint64_t)n * (uint64_t)(K / 2) + (uint64_t)(k0 / 2) + (uint64_t)(q / 2);
+}
+
+static void put_nibble(uint8_t *plane, int64_t K, int64_t k, int64_t n, const int *perm,
+                       unsigned v)
+{
+    int sh;
+    uint64_t at = nibble_byte(K, k, n, perm, &sh);
+    plane[at] = (uint8_t)((plane[at] & ~(0xFu << sh)) | ((v & 0xFu) << sh));
+}
+
+static unsigned get_nibble(const uint8_t *plane, int64_t K, int64_t k, int64_t n,
+                           const int *perm)
+{
+    int sh;
+    uint64_t at = nibble_byte(K, k, n, perm, &sh);
+    return (plane[at] >> sh) & 0xFu;
+}
+
+static uint64_t round256(uint64_t x) { return (x + 255u) & ~(uint64_t)255u; }
+
+static void fill_offsets(w12ref_desc *d, int64_t K, int64_t N, uint64_t n_esc)
+{
+    uint64_t plane = (uint64_t)K * (uint64_t)N / 2u;
+    d->version = 1;
+    d->reserved = 0;
+    d->K = K;
+    d->N = N;
+    d->G = N * (K / W12REF_GROUP);
+    d->off_h = 0;
+    d->off_l = round256(d->off_h + plane);
+    d->off_e = round256(d->off_l + plane);
+    d->off_meta = round256(d->off_e + plane);
+    d->off_esc = round256(d->off_meta + 4u * (uint64_t)(d->G + 1));
+    d->n_esc = n_esc;
+    d->total_bytes = round256(d->off_esc + 2u * n_esc);
+}
+
+static int check_shape(int64_t K, int64_t N, int layout)
+{
+    if (layout != W12REF_LAYOUT_KN && layout != W12REF_LAYOUT_NK)
+        return W12REF_ERR_ARG;
+    if (K < 0 || N < 0 || K % W12REF_GROUP != 0)
+        return W12REF_ERR_SHAPE;
+    return W12REF_OK;
+}
+
+/* Size the blob: counts the escapes, fills every offset. */
+int w12ref_plan(const uint16_t *w, int64_t K, int64_t N, int layout, w12ref_desc *d)
+{
+    int st = check_shape(K, N, layout);
+    if (st != W12REF_OK)
+        return st;
+    if (!d || (!w && K * N > 0))
+        return W12REF_ERR_ARG;
+    int64_t G = N * (K / W12REF_GROUP);
+    uint64_t n_esc = 0;
+    uint16_t grp[W12REF_GROUP];
+    for (int64_t g = 0; g < G; ++g) {
+        gather_group(w, K, N, layout, g, grp);
+        unsigned b = (unsigned)w12ref_group_base(grp);
+        for (int p = 0; p < W12REF_GROUP; ++p)
+            if (exp_code(bf16_exp(grp[p]), b) == W12REF_ESC_CODE)
+                ++n_esc;
+    }
+    if (n_esc >= W12REF_MAX_ESC)
+        return W12REF_ERR_TOO_MANY_ESCAPES;
+    fill_offsets(d, K, N, n_esc);
+    return W12REF_OK;
+}
+
+/* Encode into a zero-initialised host blob of d->total_bytes. */
+int w12ref_encode(const uint16_t *w, int64_t K, int64_t N, int layout, const w12ref_desc *d,
+                  uint8_t *blob)
+{
+    int st = check_shape(K, N, layout);
+    if (st != W12REF_OK)
+        return st;
+    if (!d || !blob || d->K != K || d->N != N)
+        return W12REF_ERR_ARG;
+    memset(blob, 0, (size_t)d->total_bytes);
+    uint8_t *H = blob + d->off_h, *L = blob + d->off_l, *E = blob + d->off_e;
+    uint32_t *meta = (uint32_t *)(blob + d->off_meta);
+    uint16_t *esc = (uint16_t *)(blob + d->off_esc);
+    int64_t kg_per_col = K / W12REF_GROUP;
+    uint64_t next = 0;
+    uint16_t grp[W12REF_GROUP];
+    for (int64_t g = 0; g < d->G; ++g) {
+        int64_t n = g / kg_per_col, kg = g % kg_per_col;
+        gather_group(w, K, N, layout, g, grp);
+        unsigned b = (unsigned)w12ref_group_base(grp);
+        meta[g] = (uint32_t)b | (uint32_t)(next << 8);
+        for (int p = 0; p < W12REF_GROUP; ++p) {
+            uint16_t v = grp[p];
+            int64_t k = kg * W12REF_GROUP + p;
+            unsigned s = bf16_sign(v), e = bf16_exp(v), m = bf16_man(v);
+            unsigned c = exp_code(e, b);
+            put_nibble(H, K, k, n, PERM_H, (s << 3) | (m >> 4));
+            put_nibble(L, K, k, n, PERM_L, m & 0xFu);
+            put_nibble(E, K, k, n, PERM_E, c);
+            if (c == W12REF_ESC_CODE) {
+                if (next >= d->n_esc)
+                    return W12REF_ERR_ARG; /* desc does not belong to this w */
+                esc[next++] = (uint16_t)((unsigned)p | (e << 7));
+            }
+        }
+    }
+    if (next != d->n_esc)
+        return W12REF_ERR_ARG;
+    meta[d->G] = (uint32_t)(next << 8);
+    return W12REF_OK;
+}
+
+/* One weight back from the blob: the logical decode rule, element by element. */
+static int weight_from_blob(const w12ref_desc *d, const uint8_t *blob, int64_t k, int64_t n,
+                            uint16_t *out)
+{
+    int64_t K = d->K;
+    int64_t g = n * (K / W12REF_GROUP) + k / W12REF_GROUP;
+    unsigned pos = (unsigned)(k % W12REF_GROUP);
+    const uint32_t *meta = (const uint32_t *)(blob + d->off_meta);
+    const uint16_t *esc = (const uint16_t *)(blob + d->off_esc);
+    unsigned h = get_nibble(blob + d->off_h, K, k, n, PERM_H);
+    unsigned l = get_nibble(blob + d->off_l, K, k, n, PERM_L);
+    unsigned c = get_nibble(blob + d->off_e, K, k, n, PERM_E);
+    unsigned b = meta[g] & 0xFFu;
+    unsigned e;
+    if (c != W12REF_ESC_CODE) {
+        e = b + c;
+    } else {
+        uint64_t lo = meta[g] >> 8, hi = meta[g + 1] >> 8;
+        if (lo > hi || hi > d->n_esc)
+            return W12REF_ERR_BLOB;
+        int found = 0;
+        e = 0;
+        for (uint64_t i = lo; i < hi; ++i) {
+            if ((esc[i] & 0x7Fu) == pos) {
+                e = (esc[i] >> 7) & 0xFFu;
+                found = 1;
+                break;
+            }
+        }
+        if (!found)
+            return W12REF_ERR_BLOB;
+    }
+    if (e > 255u)
+        return W12REF_ERR_BLOB;
+    unsigned s = (h >> 3) & 1u, m = ((h & 7u) << 4) | l;
+    *out = (uint16_t)((s << 15) | (e << 7) | m);
+    return W12REF_OK;
+}
+
+static int check_desc(const w12ref_desc *d)
+{
+    if (!d || d->version != 1 || d->K < 0 || d->N < 0 || d->K % W12REF_GROUP != 0)
+        return W12REF_ERR_ARG;
+    if (d->G != d->N * (d->K / W12REF_GROUP))
+        return W12REF_ERR_BLOB;
+    return W12REF_OK;
+}
+
+/* Decode the whole matrix into w (layout KN or NK). */
+int w12ref_decode(const w12ref_desc *d, const uint8_t *blob, uint16_t *w, int layout)
+{
+    int st = check_desc(d);
+    if (st != W12REF_OK)
+        return st;
+    if (layout != W12REF_LAYOUT_KN && layout != W12REF_LAYOUT_NK)
+        return W12REF_ERR_ARG;
+    for (int64_t n = 0; n < d->N; ++n)
+        for (int64_t k = 0; k < d->K; ++k) {
+            uint16_t v;
+            st = weight_from_blob(d, blob, k, n, &v);
+            if (st != W12REF_OK)
+                return st;
+            if (layout == W12REF_LAYOUT_KN)
+                w[k * d->N + n] = v;
+            else
+                w[n * d->K + k] = v;
+        }
+    return W12REF_OK;
+}
+
+/* ---------------------------------------------------------------------- */
+/* GEMM in fp64                                                            */
+/* ---------------------------------------------------------------------- */
+
+/* One output: y = sum_k x[m,k] * w[k,n] in k order, and s = sum_k |x w|. */
+static int dot_one(const w12ref_desc *d, const uint8_t *blob, const uint16_t *x, int64_t m,
+                   int64_t n, double *y, double *s)
+{
+    double acc = 0.0, mag = 0.0;
+    for (int64_t k = 0; k < d->K; ++k) {
+        uint16_t wv;
+        int st = weight_from_blob(d, blob, k, n, &wv);
+        if (st != W12REF_OK)
+            return st;
+        double p = bf16_to_double(x[m * d->K + k]) * bf16_to_double(wv);
+        acc += p;
+        mag += fabs(p);
+    }
+    *y = acc;
+    *s = mag;
+    return W12REF_OK;
+}
+
+/* Full product: x is [M][K] bf16, y and s are [M][N] fp64 (s may be NULL). */
+int w12ref_gemm(const w12ref_desc *d, const uint8_t *blob, const uint16_t *x, int64_t M,
+                double *y, double *s)
+{
+    int st = check_desc(d);
+    if (st != W12REF_OK)
+        return st;
+    if (M < 0 || !y)
+        return W12REF_ERR_ARG;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < d->N; ++n) {
+            double yy, ss;
+            st = dot_one(d, blob, x, m, n, &yy, &ss);
+            if (st != W12REF_OK)
+                return st;
+            y[m * d->N + n] = yy;
+            if (s)
+                s[m * d->N + n] = ss;
+        }
+    return W12REF_OK;
+}
+
+/* Selected outputs (ms[i], ns[i]) only, for full-size shapes. */
+int w12ref_gemm_at(const w12ref_desc *d, const uint8_t *blob, const uint16_t *x, int64_t M,
+                   int64_t count, const int64_t *ms, const int64_t *ns, double *y, double *s)
+{
+    int st = check_desc(d);
+    if (st != W12REF_OK)
+        return st;
+    for (int64_t i = 0; i < count; ++i) {
+        if (ms[i] < 0 || ms[i] >= M || ns[i] < 0 || ns[i] >= d->N)
+            return W12REF_ERR_ARG;
+        double ss;
+        st = dot_one(d, blob, x, ms[i], ns[i], &y[i], &ss);
+        if (st != W12REF_OK)
+            return st;
+        if (s)
+            s[i] = ss;
+    }
+    return W12REF_OK;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Greedy verification                                                     */
+/* ---------------------------------------------------------------------- */
+
+#define W12REF_F32 0
+#define W12REF_BF16 1
+
+static double logit_at(const void *logits, int dtype, int64_t i)
+{
+    if (dtype == W12REF_F32)
+        return (double)((const float *)logits)[i];
+    return bf16_to_double(((const uint16_t *)logits)[i]);
+}
+
+/* Lowest index of the maximum of one row.  NaN ranks above every number and
+ * the first NaN wins; -0 and +0 are equal (an ordinary comparison says so). */
+static int64_t row_argmax(const void *logits, int dtype, int64_t row, int64_t V)
+{
+    int64_t best = 0;
+    double bv = logit_at(logits, dtype, row * V);
+    if (isnan(bv))
+        return 0;
+    for (int64_t i = 1; i < V; ++i) {
+        double v = logit_at(logits, dtype, row * V + i);
+        if (isnan(v))
+            return i;
+        if (v > bv) {
+            bv = v;
+            best = i;
+        }
+    }
+    return best;
+}
+
+int w12ref_argmax(const void *logits, int dtype, int64_t rows, int64_t V, int64_t *idx)
+{
+    if ((dtype != W12REF_F32 && dtype != W12REF_BF16) || rows < 0 || V < 1 || !idx)
+        return W12REF_ERR_ARG;
+    for (int64_t r = 0; r < rows; ++r)
+        idx[r] = row_argmax(logits, dtype, r, V);
+    return W12REF_OK;
+}
+
+/* logits: [R*T][V]; draft: [R][T-1]; row r*T+i is the target's prediction
+ * after the block input [last committed token, d0 .. d(T-2)] position i,
+ * so it is compared with draft token i.  accept_len = first i < T-1 where
+ * they differ (T-1 if none); next = the target's token at that position. */
+int w12ref_verify_greedy(const void *logits, int dtype, int64_t R, int64_t T, int64_t V,
+                         const int32_t *draft, int32_t *accept_len, int32_t *next)
+{
+    if ((dtype != W12REF_F32 && dtype != W12REF_BF16) || R < 0 || T < 1 || V < 1)
+        return W12REF_ERR_SHAPE;
+    if (!accept_len || !next || (R > 0 && !logits) || (R > 0 && T > 1 && !draft))
+        return W12REF_ERR_ARG;
+    for (int64_t r = 0; r < R; ++r) {
+        int64_t L = T - 1;
+        for (int64_t i = 0; i < T - 1; ++i) {
+            int64_t g = row_argmax(logits, dtype, r * T + i, V);
+            if ((int64_t)draft[r * (T - 1) + i] != g) {
+                L = i;
+                break;
+            }
+        }
+        accept_len[r] = (int32_t)L;
+        next[r] = (int32_t)row_argmax(logits, dtype, r * T + L, V);
+    }
+    return W12REF_OK;
+}
