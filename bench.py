@@ -1,0 +1,443 @@
+"""Benchmark of the W12 hot path on one GB300 (or N independent replicas).
+
+A step is one pass of a 27B-class dense decoder layer's six linears (q, k, v,
+o, gate_up, down; hidden 5120) through the W12 decode-GEMM at M = 1 tokens,
+weights and activations resident in HBM.  The layer's 511 MB of W12 weights
+exceed the 129 MB L2, so every step streams them from HBM.  The headline
+value is the effective weight-stream rate 1.5 B x K x N summed over the six
+GEMMs / step time.  Alongside: the same through the public API with host
+buffers (e2e), a sweep at M = 16 / 32 / 128, the fused lm_head verify step,
+a cuBLAS BF16 GEMM of the same shapes, the dominant kernel's roofline, and
+the CPU oracle on a bounded sample of the same workload.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl w12|reference]
+Under torchrun each rank runs its own replica (the layer does not need any
+exchange); rank 0 prints one JSON line.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from lossless_bit_weight_w12_gb300 import synth  # noqa: E402
+
+METRIC = "W12 GEMM effective weight GB/s (% of GB300 HBM peak) at M=1/16/32"
+UNIT = "GB/s"
+WORKLOAD = "27B-class dense decoder layer (q 5120->6144, k/v 5120->1024, o 6144->5120, " \
+           "gate_up 5120->34816, down 17408->5120), W12 weights, M=1, seed 1"
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+DOMINANT = "gate_up"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _layer_bytes():
+    return sum(synth.weight_bytes_w12(K, N) for _, K, N in synth.LAYER_SHAPES)
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while running (median SM clock, reasons)."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                c = [x.strip() for x in line.split(",")]
+                if len(c) < 9:
+                    continue
+                try:
+                    sm.append(float(c[1]))
+                    smax = float(c[2])
+                except ValueError:
+                    continue
+                for nm, v in zip(names, c[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(nm)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- setup
+
+def build_layer(w12, dev, seed=1, M_list=(1,)):
+    """Encode the layer's six weights (seed `seed` streams) and draw x per M."""
+    import torch
+    shapes = synth.LAYER_SHAPES
+    rng = synth.streams(seed, len(shapes) + 8)
+    layer = []
+    for i, (name, K, N) in enumerate(shapes):
+        w = synth.weights(rng[i], K, N)
+        d, blob = w12.encode(w, w12.LAYOUT_NK)
+        layer.append({"name": name, "K": K, "N": N, "desc": d, "blob": w12.upload(blob, dev),
+                      "w_bf16": None, "w_np": w})
+    xs = {}
+    for M in M_list:
+        xr = synth.streams(seed * 1000 + M, len(shapes))
+        xs[M] = [torch.from_numpy(synth.activations(xr[i], M, K).view(np.int16)).to(dev)
+                 for i, (_, K, _) in enumerate(shapes)]
+    return layer, xs
+
+
+def make_bufs(w12, dev, layer, M):
+    import torch
+    ys = [torch.empty((M, g["N"]), dtype=torch.float32, device=dev) for g in layer]
+    wss = [w12.workspace(w12.gemm_workspace_size(g["desc"], M), dev) for g in layer]
+    return ys, wss
+
+
+def run_step(w12, layer, xs, ys, wss, events=None):
+    for i, g in enumerate(layer):
+        if events is not None:
+            events[i][0].record()
+        w12.gemm(g["desc"], g["blob"], xs[i], ys[i], wss[i])
+        if events is not None:
+            events[i][1].record()
+
+
+def time_steps(torch, fn, steps, barrier):
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    start.record()
+    for _ in range(steps):
+        fn()
+    stop.record()
+    torch.cuda.synchronize()
+    barrier()
+    return start.elapsed_time(stop) / 1000.0  # seconds
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "lossless_bit_weight_w12_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel_key):
+    """Per-launch DRAM bytes of the dominant kernel from the committed ncu
+    summary, if it was taken on the current kernel sources; else None."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            t = json.load(f)
+        e = t[kernel_key]
+        if e.get("kernel_hash") != kernel_hash():
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------- CPU oracle
+
+def oracle_prepare(every, seed=1):
+    """The oracle's own encoding of every `every`-th column of each of the
+    layer's six weights, with the M = 1 activations (set-up, not timed)."""
+    import oracle
+    rng = synth.streams(seed, len(synth.LAYER_SHAPES) + 8)
+    xr = synth.streams(seed * 1000 + 1, len(synth.LAYER_SHAPES))
+    work = []
+    for i, (name, K, N) in enumerate(synth.LAYER_SHAPES):
+        cols = np.arange(0, N, every)
+        w = synth.weights(rng[i], K, N)[cols]
+        x = synth.activations(xr[i], 1, K)
+        d, blob = oracle.encode(w, oracle.LAYOUT_NK)
+        work.append((d, blob, x, K * len(cols)))
+    return work
+
+
+def oracle_run(work):
+    """Time the oracle's fp64 W12 GEMM over the prepared sample.
+    Returns (effective GB/s at 1.5 B per weight, weights, seconds)."""
+    import oracle
+    t0 = time.perf_counter()
+    nw = 0
+    for d, blob, x, n in work:
+        oracle.gemm(d, blob, x)
+        nw += n
+    dt = time.perf_counter() - t0
+    return 1.5 * nw / dt / 1e9, nw, dt
+
+
+# ----------------------------------------------------------------- arms
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args):
+    world, rank, _ = dist_setup(args)
+    if rank != 0:
+        return
+    from oracle import build as ob
+    ob.build()
+    every = 16
+    work = oracle_prepare(every)
+    # warm-up steps (untimed), then K timed steps, each a bounded sample
+    for _ in range(args.warmup):
+        oracle_run(work[:1])
+    total_w, total_t = 0, 0.0
+    for _ in range(args.steps):
+        _, nw, dt = oracle_run(work)
+        total_w += nw
+        total_t += dt
+    value = 1.5 * total_w / total_t / 1e9
+    cores = 1
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total_t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": 1, "sample": f"every {every}th column of each GEMM"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"fp64 oracle GEMM on every {every}th column of each of the "
+                                   f"six layer weights, M=1; {total_w} weight-MACs per run"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_w12(args):
+    import torch
+    world, rank, local = dist_setup(args)
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+
+        def barrier():
+            dist.barrier()
+    else:
+        torch.cuda.set_device(0)
+
+        def barrier():
+            pass
+    dev = torch.device("cuda", torch.cuda.current_device())
+    from lossless_bit_weight_w12_gb300 import build_lib, w12
+    build_lib.build()
+    w12.lib()
+    hbm_peak, peak_kind = _peaks()
+
+    sweep_ms = (16, 32, 128)
+    layer, xs = build_layer(w12, dev, seed=1, M_list=(1,) + sweep_ms)
+    ys, wss = make_bufs(w12, dev, layer, 1)
+    x1 = xs[1]
+    nbytes = _layer_bytes()
+
+    for _ in range(args.warmup):
+        run_step(w12, layer, x1, ys, wss)
+    torch.cuda.synchronize()
+
+    # ---- timed region: K steps, per-GEMM events for the roofline
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in layer]
+          for _ in range(args.steps)]
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    it = iter(ev)
+    dt = time_steps(torch, lambda: run_step(w12, layer, x1, ys, wss, next(it)), args.steps, barrier)
+    clk = clocks.stop()
+    per_gemm = {g["name"]: statistics.mean(ev[s][i][0].elapsed_time(ev[s][i][1])
+                                           for s in range(args.steps)) / 1000.0
+                for i, g in enumerate(layer)}
+    if world > 1:
+        t = torch.tensor([dt], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        dt = float(t.item())
+    value = world * nbytes * args.steps / dt / 1e9
+    for wsb in wss:
+        assert w12.get_device_error(wsb) == 0
+
+    # ---- e2e: through the public API with host buffers, copies inside
+    pin_x = [x.cpu().pin_memory() for x in x1]
+    pin_y = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in ys]
+    xd = [torch.empty_like(x) for x in x1]
+
+    def e2e_step():
+        for i, g in enumerate(layer):
+            xd[i].copy_(pin_x[i], non_blocking=True)
+            w12.gemm(g["desc"], g["blob"], xd[i], ys[i], wss[i])
+            pin_y[i].copy_(ys[i], non_blocking=True)
+    for _ in range(2):
+        e2e_step()
+    dt_e2e = time_steps(torch, e2e_step, args.steps, barrier)
+    h2d = sum(x.numel() * 2 for x in x1)
+    d2h = sum(y.numel() * 4 for y in ys)
+
+    # ---- sweep over M (same weights; inputs > L2)
+    sweep = {}
+    for M in sweep_ms:
+        ysM, wsM = make_bufs(w12, dev, layer, M)
+        for _ in range(3):
+            run_step(w12, layer, xs[M], ysM, wsM)
+        n = max(3, args.steps // 2)
+        t = time_steps(torch, lambda: run_step(w12, layer, xs[M], ysM, wsM), n, barrier)
+        sweep[str(M)] = {"gbs": nbytes * n / t / 1e9, "us_per_layer": 1e6 * t / n,
+                         "frac_of_peak": nbytes * n / t / 1e9 / hbm_peak}
+        del ysM, wsM
+
+    # ---- cuBLAS BF16 GEMM on the same shapes (the 16-bit weight stream)
+    bf16_rows = {}
+    for M in (1, 16):
+        wts = [torch.from_numpy(g["w_np"].view(np.int16)).to(dev).view(torch.bfloat16)
+               for g in layer]
+        xb = [x.view(torch.bfloat16) for x in xs[M]]
+
+        def bf16_step():
+            for i in range(len(layer)):
+                torch.nn.functional.linear(xb[i], wts[i])
+        for _ in range(3):
+            bf16_step()
+        n = max(3, args.steps // 2)
+        t = time_steps(torch, bf16_step, n, barrier)
+        bf16_rows[str(M)] = {"us_per_layer": 1e6 * t / n,
+                             "bf16_gbs": sum(2.0 * g["K"] * g["N"] for g in layer) * n / t / 1e9,
+                             "w12_speedup": (t / n) / (dt / args.steps)}
+        del wts
+
+    # ---- fused lm_head verify (R = 1, T = 16) on the 5120 -> 151936 head
+    verify = None
+    if args.verify:
+        verify = bench_lmhead(w12, torch, dev, args, barrier)
+
+    # ---- roofline of the dominant kernel
+    g = next(g for g in layer if g["name"] == DOMINANT)
+    t_dom = per_gemm[DOMINANT]
+    achieved = synth.weight_bytes_w12(g["K"], g["N"]) / t_dom / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac": achieved / hbm_peak, "traffic": traffic_for("gemv_gate_up_m1"),
+                "kernel": f"gemv_kernel ({DOMINANT}, K={g['K']}, N={g['N']}, M=1)",
+                "peak_kind": f"{peak_kind} hbm_gbs (copy)",
+                "algorithmic_bytes_per_launch": synth.weight_bytes_w12(g["K"], g["N"])}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        import oracle
+        oracle.lib()
+        every = 16
+        v, nw, tcpu = oracle_run(oracle_prepare(every))
+        cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"fp64 oracle GEMM on every {every}th column of each of the six layer "
+                         f"weights at M=1 ({nw} weight-MACs, {tcpu:.1f} s, one host thread)"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1000 * dt / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": 1, "w12_bytes_per_step": nbytes,
+                   "l2": "inputs larger than L2 (511 MB of W12 weights streamed per step)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "frac_of_peak": value / world / hbm_peak,
+        "per_gemm_us": {k: 1e6 * v for k, v in per_gemm.items()},
+        "e2e": {"value": world * nbytes * args.steps / dt_e2e / 1e9, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": len(layer) * args.steps,
+        "roofline": roofline,
+        "sweep": sweep,
+        "cublas_bf16": bf16_rows,
+        "lmhead_verify": verify,
+        "cpu_baseline": cpu,
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def bench_lmhead(w12, torch, dev, args, barrier):
+    """Fused lm_head (5120 -> 151936) + greedy verify, R = 1, T = 16."""
+    K, N = synth.LM_HEAD_SHAPE[1], synth.LM_HEAD_SHAPE[2]
+    R, T = 1, 16
+    rng = synth.streams(4, 3)
+    w = synth.weights(rng[0], K, N)
+    d, blob = w12.encode(w, w12.LAYOUT_NK)
+    blob_d = w12.upload(blob, dev)
+    hidden = torch.from_numpy(synth.activations(rng[1], R * T, K).view(np.int16)).to(dev)
+    draft = torch.from_numpy(rng[2].integers(0, N, (R, T - 1)).astype(np.int32)).to(dev)
+    acc = torch.empty(R, dtype=torch.int32, device=dev)
+    nxt = torch.empty(R, dtype=torch.int32, device=dev)
+    ws = w12.workspace(w12.verify_lmhead_workspace_size(d, R, T), dev)
+
+    def step():
+        w12.verify_greedy_lmhead(hidden, d, blob_d, R, T, draft, acc, nxt, ws)
+    for _ in range(3):
+        step()
+    n = max(5, args.steps)
+    t = time_steps(torch, step, n, barrier)
+    b = synth.weight_bytes_w12(K, N)
+    return {"us": 1e6 * t / n, "gbs": b * n / t / 1e9, "R": R, "T": T, "N": N, "K": K}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="w12", choices=["w12", "reference"])
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-verify", dest="verify", action="store_false")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_w12(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,230 @@
+/*
+ * w12.h -- C interface of libw12.so: the W12 lossless 12-bit BF16 weight
+ * format, the fused W12 decode-GEMM for skinny M, and greedy draft-block
+ * verification, for NVIDIA GB300 (sm_103a).
+ *
+ * Sources.  The SpecPilot summary pages (airadar.tv, English edition,
+ * "Reasons" bullet 2, and its French, Japanese and Korean editions) describe
+ * W12 as BF16 split into three 4-bit planes and rebuilt bit for bit inside the
+ * GEMM's registers; the hotrepo.ai page on StargazerX0/SpecPilot ("项目介绍",
+ * paragraph 2) adds that the decode is bit-exact and serves batch 1-32.  The
+ * same English page ("Risks", bullet 3) defines the greedy acceptance rule:
+ * every committed token is the target model's own greedy choice.  No layout,
+ * interface or kernel is printed there; the layout and calls below are this
+ * library's own.
+ *
+ * Conventions for every call:
+ *  - Status: every function returns an int status (W12_OK = 0 or a W12_ERR_*
+ *    code); w12_status_string() names it.  A non-zero status means nothing
+ *    was launched or written.
+ *  - Memory: the caller owns every buffer.  The library allocates no device
+ *    memory and no host memory beyond stack and OpenMP temporaries.
+ *  - Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *    default stream).  Device calls are asynchronous on that stream and never
+ *    synchronise, except w12_get_device_error().
+ *  - Pointers named *_dev are device pointers, *_host host pointers.
+ *  - Workspaces: a workspace of the size the matching *_workspace_size()
+ *    call returns, 256-byte aligned, zero-filled by the caller before its
+ *    first use.  Every kernel leaves its workspace counters at zero again, so
+ *    a workspace is reused without clearing.  Word 0 of a workspace is a
+ *    sticky device error code (see w12_get_device_error).  Calls that share
+ *    one workspace must be ordered (same stream, or events).
+ */
+#ifndef W12_H
+#define W12_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define W12_FORMAT_VERSION 1
+
+/* Status codes. */
+#define W12_OK 0
+#define W12_ERR_ARG 1               /* NULL pointer, bad enum, inconsistent desc   */
+#define W12_ERR_SHAPE 2             /* K % 128 != 0, negative sizes, M or T range  */
+#define W12_ERR_ALIGN 3             /* a pointer misses its required alignment     */
+#define W12_ERR_WORKSPACE 4         /* workspace NULL or smaller than required     */
+#define W12_ERR_BLOB 5              /* blob contents inconsistent with the desc    */
+#define W12_ERR_TOO_MANY_ESCAPES 6  /* 2^24 or more escapes in one matrix          */
+#define W12_ERR_CUDA 7              /* a CUDA runtime call or launch failed        */
+#define W12_ERR_TIMEOUT 8           /* a bounded device wait gave up               */
+#define W12_ERR_DEVICE 9            /* a kernel recorded an error (bad blob index) */
+
+/* Orientation of a dense weight matrix in memory. */
+#define W12_LAYOUT_KN 0 /* w[k*N + n]: row-major [K][N]                         */
+#define W12_LAYOUT_NK 1 /* w[n*K + k]: row-major [N][K] (a linear layer's weight) */
+
+/* Element types of y and of logits. */
+#define W12_F32 0
+#define W12_BF16 1
+
+/* GEMM paths (w12_gemm_ex). */
+#define W12_PATH_AUTO 0
+#define W12_PATH_GEMV 1 /* CUDA-core FFMA GEMV with warp-shuffle reduction, M <= 4 */
+#define W12_PATH_MMA 2  /* tensor-core mma tiles, M <= 128                        */
+
+#define W12_MAX_M 128
+
+/*
+ * Descriptor of one encoded K x N matrix (format v1).
+ *
+ * Logical format.  A group is 128 consecutive k of one output column n:
+ * group g = n*(K/128) + k/128, pos = k % 128.  A bf16 weight has sign s
+ * (bit 15), exponent e (bits 14..7) and mantissa m (bits 6..0).  Each group
+ * has a base b in [0, 241]: the b whose window [b, b+14] holds the most of
+ * the group's exponents, the largest such b on a tie.  A weight's exponent
+ * code is c = e - b inside the window and 15 ("escape") outside it.  Escaped
+ * weights get a 16-bit entry pos | e << 7 in the escape list, ordered by
+ * group then pos.  meta[g] = b | first_escape_index(g) << 8, and
+ * meta[G] = n_esc << 8.
+ *
+ * Physical format (byte offsets from the blob start; each section starts on
+ * a 256-byte boundary; the blob start itself must be 256-byte aligned):
+ *   H plane  at off_h:    N*K/2 bytes, nibble = s << 3 | m >> 4
+ *   L plane  at off_l:    N*K/2 bytes, nibble = m & 15
+ *   E plane  at off_e:    N*K/2 bytes, nibble = c
+ *   meta     at off_meta: (G+1) little-endian uint32
+ *   escapes  at off_esc:  n_esc little-endian uint16
+ * Planes are column-major: column n owns bytes [n*K/2, (n+1)*K/2).  The
+ * little-endian 32-bit word at index n*K/8 + k0/8 of a plane covers weights
+ * k0..k0+7 of column n; its nibble q (bits 4q..4q+3) holds weight k0+P[q]:
+ *   H: P = {4,0,5,1,6,2,7,3}   L: P = {0,5,1,6,2,7,3,4}   E: P = {0,2,4,6,1,3,5,7}
+ * total_bytes covers all five sections rounded up to 256.
+ */
+typedef struct w12_desc {
+    uint32_t version; /* W12_FORMAT_VERSION */
+    uint32_t reserved; /* 0 */
+    int64_t K, N, G;
+    uint64_t off_h, off_l, off_e, off_meta, off_esc;
+    uint64_t n_esc;
+    uint64_t total_bytes;
+} w12_desc;
+
+/* Name of a status code (static string, never NULL). */
+const char *w12_status_string(int status);
+
+/* Library format version (W12_FORMAT_VERSION). */
+int w12_version(void);
+
+/* --------------------------------------------------------------------- */
+/* Host encoder                                                          */
+/* --------------------------------------------------------------------- */
+
+/*
+ * Size the blob for a bf16 matrix w (host, layout W12_LAYOUT_KN or _NK,
+ * K % 128 == 0; K or N may be 0).  Fills every field of *d, counting the
+ * escapes.  Errors: W12_ERR_ARG, W12_ERR_SHAPE, W12_ERR_TOO_MANY_ESCAPES.
+ * Multithreaded (OpenMP) over groups.
+ */
+int w12_encode_plan(const uint16_t *w_host, int64_t K, int64_t N, int layout, w12_desc *d);
+
+/*
+ * Encode w into blob_host (d->total_bytes bytes, any alignment; padding is
+ * written as zeros).  *d must come from w12_encode_plan on the same w.
+ * Errors: W12_ERR_ARG (d does not match w), W12_ERR_SHAPE.
+ */
+int w12_encode(const uint16_t *w_host, int64_t K, int64_t N, int layout, const w12_desc *d,
+               void *blob_host);
+
+/*
+ * Check a host blob against its descriptor: the offsets and sizes, base
+ * range, meta monotonicity and sentinel, escape positions and order, that
+ * every code-15 nibble has exactly one escape entry and that every escape is
+ * canonical (its exponent lies outside the group window).  Returns W12_OK,
+ * W12_ERR_ARG or W12_ERR_BLOB.  The device calls do not run this check:
+ * they only bound every index they read, recording W12_ERR_DEVICE.
+ */
+int w12_validate(const w12_desc *d, const void *blob_host);
+
+/* --------------------------------------------------------------------- */
+/* Device calls                                                          */
+/* --------------------------------------------------------------------- */
+
+/*
+ * Decode a device blob (256-byte aligned) back to bf16 bit patterns in w_dev
+ * (K*N uint16, 16-byte aligned) in the given layout.  Bit-exact inverse of
+ * w12_encode.  Errors: W12_ERR_ARG, W12_ERR_ALIGN, W12_ERR_CUDA.  Escape
+ * indices are bounds-checked; a bad one is not followed (the weight keeps
+ * the garbage exponent) and W12_ERR_DEVICE goes to *err_dev if err_dev is
+ * not NULL.
+ */
+int w12_decode(const w12_desc *d, const void *blob_dev, uint16_t *w_dev, int layout,
+               int *err_dev, void *stream);
+
+/* Bytes of workspace w12_gemm needs for this matrix and M (>= 256). */
+size_t w12_gemm_workspace_size(const w12_desc *d, int64_t M);
+
+/*
+ * y[m, n] = sum_k x[m, k] * W[k, n] for m < M, n < N.
+ *   x_dev: [M][K] row-major bf16, 16-byte aligned.
+ *   y_dev: [M][N] row-major, y_dtype W12_F32 (4-byte aligned) or W12_BF16
+ *          (2-byte aligned; rounded to nearest even from the fp32 sum).
+ *   1 <= M <= W12_MAX_M.  Accumulation is fp32; the summation order is fixed
+ *   for a given (desc, M) so repeated calls give identical bits.
+ * Errors: W12_ERR_ARG, W12_ERR_SHAPE, W12_ERR_ALIGN, W12_ERR_WORKSPACE,
+ * W12_ERR_CUDA.  Device-detected blob errors: W12_ERR_DEVICE in word 0 of ws.
+ */
+int w12_gemm(const w12_desc *d, const void *blob_dev, const uint16_t *x_dev, int64_t M,
+             void *y_dev, int y_dtype, void *ws_dev, size_t ws_bytes, void *stream);
+
+/* w12_gemm with an explicit path (W12_PATH_*); W12_ERR_SHAPE if the path
+ * does not serve this M. */
+int w12_gemm_ex(const w12_desc *d, const void *blob_dev, const uint16_t *x_dev, int64_t M,
+                void *y_dev, int y_dtype, void *ws_dev, size_t ws_bytes, int path,
+                void *stream);
+
+/* Bytes of workspace w12_verify_greedy needs (>= 256). */
+size_t w12_verify_workspace_size(int64_t R, int64_t T, int64_t V);
+
+/*
+ * Greedy verification of R draft blocks of T positions on logits.
+ *   logits_dev: [R*T][V] row-major, dtype W12_F32 or W12_BF16, 16-byte aligned.
+ *   draft_dev:  [R][T-1] int32 (may be NULL when T == 1).
+ *   For each row i of block r, g[r,i] is the lowest index of the row maximum
+ *   (NaN above every number, the first NaN wins, -0 == +0).  Row i is the
+ *   target's prediction after block input [last token, d0 .. d(i-1)], so it
+ *   is compared with draft token i:
+ *     accept_len_dev[r] = first i < T-1 with draft[r,i] != g[r,i], else T-1;
+ *     next_tok_dev[r]   = g[r, accept_len[r]].
+ *   R >= 1, T >= 1, 1 <= V < 2^31.
+ * Errors: W12_ERR_ARG, W12_ERR_SHAPE, W12_ERR_ALIGN, W12_ERR_WORKSPACE,
+ * W12_ERR_CUDA.
+ */
+int w12_verify_greedy(const void *logits_dev, int dtype, int64_t R, int64_t T, int64_t V,
+                      const int32_t *draft_dev, int32_t *accept_len_dev, int32_t *next_tok_dev,
+                      void *ws_dev, size_t ws_bytes, void *stream);
+
+/* Bytes of workspace w12_verify_greedy_lmhead needs (>= 256). */
+size_t w12_verify_lmhead_workspace_size(const w12_desc *d_lm, int64_t R, int64_t T);
+
+/*
+ * Fused lm_head + greedy verification: logits = hidden @ W_lm (the W12
+ * decode-GEMM, fp32 accumulation), then the rule of w12_verify_greedy on
+ * those fp32 logits, without writing them unless logits_out_dev is given.
+ *   hidden_dev: [R*T][K] bf16, 16-byte aligned; R*T <= W12_MAX_M.
+ *   logits_out_dev: NULL, or [R*T][N] fp32 receiving the exact logits the
+ *   argmax was taken on.
+ * Errors: as w12_gemm and w12_verify_greedy.
+ */
+int w12_verify_greedy_lmhead(const uint16_t *hidden_dev, const w12_desc *d_lm,
+                             const void *blob_lm_dev, int64_t R, int64_t T,
+                             const int32_t *draft_dev, int32_t *accept_len_dev,
+                             int32_t *next_tok_dev, float *logits_out_dev, void *ws_dev,
+                             size_t ws_bytes, void *stream);
+
+/*
+ * Read (and clear) the sticky device error word of a workspace: waits for
+ * `stream`, copies word 0 to *err_host, then zeroes it.  Returns W12_OK or
+ * W12_ERR_CUDA.  *err_host is W12_OK or W12_ERR_DEVICE.
+ */
+int w12_get_device_error(void *ws_dev, int *err_host, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W12_H */

@@ -1,0 +1,377 @@
+// abi.cu -- the extern "C" entry points of libw12.so (declared in include/w12.h):
+// argument checks, work planning and dispatch to the kernels.  Host code only.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+
+#include "w12_internal.h"
+
+namespace w12 {
+
+namespace {
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// The descriptor must be exactly what the v1 layout gives for its K, N, n_esc.
+int check_desc(const w12_desc *d) {
+    if (!d) return W12_ERR_ARG;
+    if (d->version != W12_FORMAT_VERSION || d->K < 0 || d->N < 0 || d->K % kGroup != 0)
+        return W12_ERR_ARG;
+    if (d->n_esc >= kMaxEscapes) return W12_ERR_BLOB;
+    w12_desc want;
+    layout_v1(d->K, d->N, d->n_esc, &want);
+    if (std::memcmp(&want, d, sizeof want) != 0) return W12_ERR_BLOB;
+    if (d->N >= (int64_t(1) << 31)) return W12_ERR_SHAPE;
+    return W12_OK;
+}
+
+struct Device {
+    int sms = 0;
+};
+
+int query_device(Device *dv) { return device_sm_count(&dv->sms); }
+
+// Makespan model: tiles are dealt out in contiguous balanced ranges, so the
+// busiest CTA runs ceil(T / grid) tiles of `tile_work` weights each.  A small
+// per-split charge prefers fewer splits among equal makespans.
+double makespan(int64_t T, int64_t grid, double tile_work, int nks, int64_t N, int64_t M,
+                int64_t K) {
+    const double rounds = double(ceil_div(T, grid));
+    const double split_bytes = nks > 1 ? double(nks) * double(N) * double(M) * 8.0 : 0.0;
+    const double per_cta_split = split_bytes / double(grid) / 1.5;  // in weight-equivalents
+    (void)K;
+    return rounds * tile_work + per_cta_split + 1e-3 * nks * tile_work;
+}
+
+void finish_ws_layout(GemmPlan *p, int64_t M, int64_t N, bool fused) {
+    size_t off = kWsHeader;
+    p->off_counters = off;
+    off += round256(4u * uint64_t(std::max<int64_t>(p->NB, 1)));
+    p->off_partial = off;
+    if (p->nks > 1) off += round256(uint64_t(p->nks) * uint64_t(M) * uint64_t(N) * 4u);
+    p->off_best = off;
+    if (fused) off += round256(uint64_t(p->grid) * uint64_t(M) * 8u);
+    p->off_gbuf = off;
+    if (fused) off += round256(uint64_t(M) * 4u);
+    p->ws_bytes = off;
+}
+
+int plan_gemv(const w12_desc *d, int64_t M, const Device &dv, GemmPlan *p) {
+    struct V {
+        int id, cpw, mt;
+    };
+    static const V vs[] = {{0, 1, 1}, {1, 2, 1}, {2, 4, 1}, {3, 1, 2}, {4, 2, 2}, {5, 1, 4}};
+    const int mt = M <= 1 ? 1 : M <= 2 ? 2 : 4;
+    const int64_t steps = ceil_div(d->K, 1024);
+    double best = 1e300;
+    bool found = false;
+    for (const V &v : vs) {
+        if (v.mt != mt) continue;
+        int occ = 0;
+        if (gemv_occupancy(v.id, &occ) != W12_OK) return W12_ERR_CUDA;
+        if (occ < 1) continue;
+        const int64_t grid = int64_t(dv.sms) * occ;
+        const int64_t NB = ceil_div(d->N, 8 * v.cpw);
+        for (int64_t nks = 1; nks <= steps; ++nks) {
+            const int64_t cs = ceil_div(steps, nks);
+            const int64_t eff = ceil_div(steps, cs);
+            if (eff != nks) continue;
+            const int64_t T = NB * eff;
+            const double work = double(8 * v.cpw) * double(cs * 1024);
+            const double c = makespan(T, grid, work, int(eff), d->N, M, d->K) / (1.0 + 0.02 * v.cpw);
+            if (c < best) {
+                best = c;
+                found = true;
+                p->path = W12_PATH_GEMV;
+                p->variant = v.id;
+                p->grid = int(std::min<int64_t>(grid, T));
+                p->NB = NB;
+                p->cols_per_tile = 8 * v.cpw;
+                p->nks = int(eff);
+                p->kchunk = cs * 1024;
+                p->xchunk = 0;
+            }
+        }
+    }
+    if (!found) return W12_ERR_CUDA;
+    finish_ws_layout(p, M, d->N, false);
+    return W12_OK;
+}
+
+int plan_mma(const w12_desc *d, int64_t M, const Device &dv, bool fused, GemmPlan *p) {
+    int nt = 1, v = 0;
+    while (nt * 8 < M) {
+        nt *= 2;
+        ++v;
+    }
+    const int64_t mp = 8 * nt;
+    const int64_t groups = d->K / kGroup;
+    const int64_t xmax = std::max<int64_t>(1, 32768 / mp / kGroup) * kGroup;  // 64 KB of x
+    const int64_t NB = ceil_div(d->N, 128);
+    double best = 1e300;
+    bool found = false;
+    for (int64_t nks = 1; nks <= (fused ? 1 : groups); ++nks) {
+        const int64_t cg = ceil_div(groups, nks);
+        const int64_t eff = ceil_div(groups, cg);
+        if (eff != nks) continue;
+        const int64_t kchunk = cg * kGroup;
+        const int64_t xchunk = std::min(kchunk, xmax);
+        int occ = 0;
+        if (mma_occupancy(v, size_t(mp * xchunk * 2), &occ) != W12_OK) return W12_ERR_CUDA;
+        if (occ < 1) continue;
+        const int64_t grid = int64_t(dv.sms) * occ;
+        const int64_t T = NB * eff;
+        const double work = 128.0 * double(kchunk);
+        const double c = makespan(T, grid, work, int(eff), d->N, M, d->K);
+        if (c < best) {
+            best = c;
+            found = true;
+            p->path = W12_PATH_MMA;
+            p->variant = v;
+            p->grid = int(fused ? grid : std::min<int64_t>(grid, T));
+            p->NB = NB;
+            p->cols_per_tile = 128;
+            p->nks = int(eff);
+            p->kchunk = kchunk;
+            p->xchunk = xchunk;
+        }
+    }
+    if (!found) return W12_ERR_CUDA;
+    finish_ws_layout(p, M, d->N, fused);
+    return W12_OK;
+}
+
+GemmArgs make_args(const w12_desc *d, const void *blob, const uint16_t *x, int64_t M, void *y,
+                   int y_dtype, void *ws, const GemmPlan &p) {
+    const uint8_t *b = static_cast<const uint8_t *>(blob);
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    GemmArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.H = reinterpret_cast<const uint32_t *>(b + d->off_h);
+    a.L = reinterpret_cast<const uint32_t *>(b + d->off_l);
+    a.E = reinterpret_cast<const uint32_t *>(b + d->off_e);
+    a.meta = reinterpret_cast<const uint32_t *>(b + d->off_meta);
+    a.esc = reinterpret_cast<const uint16_t *>(b + d->off_esc);
+    a.n_esc = d->n_esc;
+    a.K = d->K;
+    a.N = d->N;
+    a.KW = d->K / 8;
+    a.KG = d->K / kGroup;
+    a.x = x;
+    a.M = int(M);
+    a.y = y;
+    a.y_dtype = y_dtype;
+    a.partial = reinterpret_cast<float *>(w + p.off_partial);
+    a.counters = reinterpret_cast<uint32_t *>(w + p.off_counters);
+    a.err = reinterpret_cast<int *>(w);
+    a.NB = p.NB;
+    a.cols_per_tile = p.cols_per_tile;
+    a.nks = p.nks;
+    a.kchunk = p.kchunk;
+    a.xchunk = p.xchunk;
+    a.T = p.NB * p.nks;
+    return a;
+}
+
+int choose_plan(const w12_desc *d, int64_t M, int path, bool fused, GemmPlan *p) {
+    Device dv;
+    if (query_device(&dv) != W12_OK) return W12_ERR_CUDA;
+    if (path == W12_PATH_AUTO) path = (M == 1 && !fused) ? W12_PATH_GEMV : W12_PATH_MMA;
+    if (path == W12_PATH_GEMV) {
+        if (M > 4 || fused) return W12_ERR_SHAPE;
+        return plan_gemv(d, M, dv, p);
+    }
+    if (path == W12_PATH_MMA) return plan_mma(d, M, dv, fused, p);
+    return W12_ERR_ARG;
+}
+
+int launch_plan(const GemmPlan &p, const GemmArgs &a, void *stream) {
+    return p.path == W12_PATH_GEMV ? launch_gemv(p, a, stream) : launch_mma(p, a, stream);
+}
+
+int verify_plan(int64_t rows, int64_t V, int *grid, int64_t *splits, int64_t *chunk) {
+    Device dv;
+    if (query_device(&dv) != W12_OK) return W12_ERR_CUDA;
+    int64_t sp = std::max<int64_t>(1, ceil_div(4 * int64_t(dv.sms), rows));
+    sp = std::min<int64_t>(sp, std::max<int64_t>(1, ceil_div(V, 1024)));
+    int64_t ch = ceil_div(ceil_div(V, sp), 8) * 8;
+    sp = ceil_div(V, ch);
+    *splits = sp;
+    *chunk = ch;
+    *grid = int(std::min<int64_t>(rows * sp, int64_t(dv.sms) * 8));
+    return W12_OK;
+}
+
+size_t verify_ws(int64_t rows, int64_t splits) {
+    return kWsHeader + 256 + round256(uint64_t(rows * splits) * 8u) + round256(uint64_t(rows) * 4u);
+}
+
+}  // namespace
+
+}  // namespace w12
+
+using namespace w12;
+
+extern "C" const char *w12_status_string(int status) {
+    switch (status) {
+        case W12_OK: return "W12_OK";
+        case W12_ERR_ARG: return "W12_ERR_ARG: bad argument";
+        case W12_ERR_SHAPE: return "W12_ERR_SHAPE: unsupported shape";
+        case W12_ERR_ALIGN: return "W12_ERR_ALIGN: pointer misaligned";
+        case W12_ERR_WORKSPACE: return "W12_ERR_WORKSPACE: workspace missing or too small";
+        case W12_ERR_BLOB: return "W12_ERR_BLOB: blob or descriptor inconsistent";
+        case W12_ERR_TOO_MANY_ESCAPES: return "W12_ERR_TOO_MANY_ESCAPES: 2^24 or more escapes";
+        case W12_ERR_CUDA: return "W12_ERR_CUDA: CUDA call failed";
+        case W12_ERR_TIMEOUT: return "W12_ERR_TIMEOUT: bounded wait expired";
+        case W12_ERR_DEVICE: return "W12_ERR_DEVICE: kernel detected a bad blob index";
+    }
+    return "unknown W12 status";
+}
+
+extern "C" int w12_version(void) { return W12_FORMAT_VERSION; }
+
+extern "C" int w12_decode(const w12_desc *d, const void *blob, uint16_t *w, int layout, int *err,
+                          void *stream) {
+    int st = check_desc(d);
+    if (st != W12_OK) return st;
+    if (layout != W12_LAYOUT_KN && layout != W12_LAYOUT_NK) return W12_ERR_ARG;
+    if (d->G == 0) return W12_OK;
+    if (!blob || !w) return W12_ERR_ARG;
+    if (!aligned(blob, 256) || !aligned(w, 16)) return W12_ERR_ALIGN;
+    return launch_decode(d, blob, w, layout, err, stream);
+}
+
+extern "C" size_t w12_gemm_workspace_size(const w12_desc *d, int64_t M) {
+    if (check_desc(d) != W12_OK || M < 1 || M > W12_MAX_M) return 0;
+    GemmPlan p;
+    if (choose_plan(d, M, W12_PATH_AUTO, false, &p) != W12_OK) return 0;
+    // room for any path this M can take, so w12_gemm_ex can switch paths
+    size_t need = p.ws_bytes;
+    GemmPlan q;
+    if (M <= 4 && choose_plan(d, M, W12_PATH_GEMV, false, &q) == W12_OK) need = std::max(need, q.ws_bytes);
+    if (choose_plan(d, M, W12_PATH_MMA, false, &q) == W12_OK) need = std::max(need, q.ws_bytes);
+    return need;
+}
+
+extern "C" int w12_gemm_ex(const w12_desc *d, const void *blob, const uint16_t *x, int64_t M,
+                           void *y, int y_dtype, void *ws, size_t ws_bytes, int path,
+                           void *stream) {
+    int st = check_desc(d);
+    if (st != W12_OK) return st;
+    if (M < 1 || M > W12_MAX_M) return W12_ERR_SHAPE;
+    if (y_dtype != W12_F32 && y_dtype != W12_BF16) return W12_ERR_ARG;
+    if (path < W12_PATH_AUTO || path > W12_PATH_MMA) return W12_ERR_ARG;
+    if (d->N == 0) return W12_OK;
+    if (!y) return W12_ERR_ARG;
+    if (!aligned(y, y_dtype == W12_F32 ? 4 : 2)) return W12_ERR_ALIGN;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (d->K == 0) {
+        const size_t bytes = size_t(M) * size_t(d->N) * (y_dtype == W12_F32 ? 4 : 2);
+        return cudaMemsetAsync(y, 0, bytes, s) == cudaSuccess ? W12_OK : W12_ERR_CUDA;
+    }
+    if (!blob || !x) return W12_ERR_ARG;
+    if (!aligned(blob, 256) || !aligned(x, 16)) return W12_ERR_ALIGN;
+    GemmPlan p;
+    st = choose_plan(d, M, path, false, &p);
+    if (st != W12_OK) return st;
+    if (!ws || ws_bytes < p.ws_bytes) return W12_ERR_WORKSPACE;
+    if (!aligned(ws, 256)) return W12_ERR_ALIGN;
+    const GemmArgs a = make_args(d, blob, x, M, y, y_dtype, ws, p);
+    return launch_plan(p, a, stream);
+}
+
+extern "C" int w12_gemm(const w12_desc *d, const void *blob, const uint16_t *x, int64_t M, void *y,
+                        int y_dtype, void *ws, size_t ws_bytes, void *stream) {
+    return w12_gemm_ex(d, blob, x, M, y, y_dtype, ws, ws_bytes, W12_PATH_AUTO, stream);
+}
+
+extern "C" size_t w12_verify_workspace_size(int64_t R, int64_t T, int64_t V) {
+    if (R < 1 || T < 1 || V < 1 || V >= (int64_t(1) << 31)) return 0;
+    int grid;
+    int64_t splits, chunk;
+    if (verify_plan(R * T, V, &grid, &splits, &chunk) != W12_OK) return 0;
+    return verify_ws(R * T, splits);
+}
+
+extern "C" int w12_verify_greedy(const void *logits, int dtype, int64_t R, int64_t T, int64_t V,
+                                 const int32_t *draft, int32_t *accept_len, int32_t *next_tok,
+                                 void *ws, size_t ws_bytes, void *stream) {
+    if (dtype != W12_F32 && dtype != W12_BF16) return W12_ERR_ARG;
+    if (R < 1 || T < 1 || V < 1 || V >= (int64_t(1) << 31)) return W12_ERR_SHAPE;
+    if (!logits || !accept_len || !next_tok || (T > 1 && !draft)) return W12_ERR_ARG;
+    if (!aligned(logits, dtype == W12_F32 ? 4 : 2) || !aligned(accept_len, 4) ||
+        !aligned(next_tok, 4) || (draft && !aligned(draft, 4)))
+        return W12_ERR_ALIGN;
+    VerifyArgs a;
+    int grid;
+    a.rows = R * T;
+    if (verify_plan(a.rows, V, &grid, &a.splits, &a.chunk) != W12_OK) return W12_ERR_CUDA;
+    if (!ws || ws_bytes < verify_ws(a.rows, a.splits)) return W12_ERR_WORKSPACE;
+    if (!aligned(ws, 256)) return W12_ERR_ALIGN;
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    a.logits = logits;
+    a.dtype = dtype;
+    a.R = R;
+    a.T = T;
+    a.V = V;
+    a.draft = draft;
+    a.accept_len = accept_len;
+    a.next_tok = next_tok;
+    a.counter = reinterpret_cast<uint32_t *>(w + kWsHeader);
+    a.partial = reinterpret_cast<unsigned long long *>(w + kWsHeader + 256);
+    a.gbuf = reinterpret_cast<int32_t *>(w + kWsHeader + 256 + round256(uint64_t(a.rows * a.splits) * 8u));
+    return launch_verify(a, grid, stream);
+}
+
+extern "C" size_t w12_verify_lmhead_workspace_size(const w12_desc *d, int64_t R, int64_t T) {
+    if (check_desc(d) != W12_OK || R < 1 || T < 1 || R * T > W12_MAX_M) return 0;
+    GemmPlan p;
+    if (choose_plan(d, R * T, W12_PATH_MMA, true, &p) != W12_OK) return 0;
+    return p.ws_bytes;
+}
+
+extern "C" int w12_verify_greedy_lmhead(const uint16_t *hidden, const w12_desc *d,
+                                        const void *blob, int64_t R, int64_t T,
+                                        const int32_t *draft, int32_t *accept_len,
+                                        int32_t *next_tok, float *logits_out, void *ws,
+                                        size_t ws_bytes, void *stream) {
+    int st = check_desc(d);
+    if (st != W12_OK) return st;
+    if (R < 1 || T < 1 || R * T > W12_MAX_M || d->N < 1 || d->K < kGroup) return W12_ERR_SHAPE;
+    if (!hidden || !blob || !accept_len || !next_tok || (T > 1 && !draft)) return W12_ERR_ARG;
+    if (!aligned(blob, 256) || !aligned(hidden, 16) || !aligned(accept_len, 4) ||
+        !aligned(next_tok, 4) || (draft && !aligned(draft, 4)) ||
+        (logits_out && !aligned(logits_out, 4)))
+        return W12_ERR_ALIGN;
+    const int64_t M = R * T;
+    GemmPlan p;
+    st = choose_plan(d, M, W12_PATH_MMA, true, &p);
+    if (st != W12_OK) return st;
+    if (!ws || ws_bytes < p.ws_bytes) return W12_ERR_WORKSPACE;
+    if (!aligned(ws, 256)) return W12_ERR_ALIGN;
+    GemmArgs a = make_args(d, blob, hidden, M, nullptr, W12_F32, ws, p);
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    a.row_best = reinterpret_cast<unsigned long long *>(w + p.off_best);
+    a.gbuf = reinterpret_cast<int32_t *>(w + p.off_gbuf);
+    a.logits_out = logits_out;
+    a.vR = R;
+    a.vT = T;
+    a.draft = draft;
+    a.accept_len = accept_len;
+    a.next_tok = next_tok;
+    return launch_mma(p, a, stream);
+}
+
+extern "C" int w12_get_device_error(void *ws, int *err_host, void *stream) {
+    if (!ws || !err_host) return W12_ERR_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int v = 0;
+    if (cudaMemcpyAsync(&v, ws, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess) return W12_ERR_CUDA;
+    if (cudaMemsetAsync(ws, 0, sizeof v, s) != cudaSuccess) return W12_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return W12_ERR_CUDA;
+    *err_host = v;
+    return W12_OK;
+}

@@ -1,0 +1,128 @@
+// device_common.cuh -- register-level W12 rebuild shared by the kernels.
+//
+// "Reconstructing bit by bit in GEMM registers" (SpecPilot summary,
+// airadar.tv English edition, "Reasons" bullet 2): one 32-bit word from each
+// of the H, L and E planes covers 8 consecutive k of one column; the
+// nibble order inside each word (include/w12.h) is chosen so that the 8
+// bf16 values come out as 4 bf16x2 registers (k0,k0+1), (k0+2,k0+3), ...
+// in 20 integer instructions:
+//   SMA = (H & 0xF0F0F0F0) | (L & 0x0F0F0F0F)   sign|mantissa bytes of k0..k0+3
+//   SMB = rotl((H & 0x0F0F0F0F) | (L & 0xF0F0F0F0), 4)              k0+4..k0+7
+//   P_i = prmt(SM, sign-replicating selector)  mantissa in bits 0-6, sign in 15
+//   X_i = ((E >> 4i') & 0x000F000F) << 7 + b * 0x00800080   exponent b + c
+//   out_i = (P_i & 0x807F807F) | (X_i & 0x7F807F80)
+// An escape (code 15) leaves a wrong exponent that patch_escapes() replaces.
+#pragma once
+
+#include <cstdint>
+
+#include "../../include/w12.h"
+
+namespace w12 {
+
+constexpr uint32_t kSignManMask = 0x807F807Fu;
+
+// Streaming 16-byte load: read once, keep out of L1, ask L2 for 256-byte lines.
+__device__ __forceinline__ uint4 ldg_stream(const void *p) {
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t ldg_u32(const uint32_t *p) {
+    uint32_t r;
+    asm("ld.global.nc.u32 %0, [%1];" : "=r"(r) : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint4 ldg_v4(const void *p) {
+    uint4 r;
+    asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+// prmt with the sign-replicate bit honoured (bit 3 of each selector nibble).
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(d) : "r"(a), "r"(sel));
+    return d;
+}
+
+// Rebuild 8 weights (one word of each plane) into 4 bf16x2 registers.
+// b2 = base * 0x00800080.
+__device__ __forceinline__ void rebuild8(uint32_t h, uint32_t l, uint32_t e, uint32_t b2,
+                                         uint32_t out[4]) {
+    const uint32_t sma = (h & 0xF0F0F0F0u) | (l & 0x0F0F0F0Fu);
+    const uint32_t xx = (h & 0x0F0F0F0Fu) | (l & 0xF0F0F0F0u);
+    const uint32_t smb = __funnelshift_l(xx, xx, 4);
+    const uint32_t e8 = e >> 8;
+    const uint32_t x0 = (e & 0x000F000Fu) * 128u + b2;
+    const uint32_t x1 = (e & 0x00F000F0u) * 8u + b2;
+    const uint32_t x2 = (e8 & 0x000F000Fu) * 128u + b2;
+    const uint32_t x3 = (e8 & 0x00F000F0u) * 8u + b2;
+    out[0] = (prmt(sma, 0x9180u) & kSignManMask) | (x0 & ~kSignManMask);
+    out[1] = (prmt(sma, 0xB3A2u) & kSignManMask) | (x1 & ~kSignManMask);
+    out[2] = (prmt(smb, 0x9180u) & kSignManMask) | (x2 & ~kSignManMask);
+    out[3] = (prmt(smb, 0xB3A2u) & kSignManMask) | (x3 & ~kSignManMask);
+}
+
+// Rebuild the 32 weights of one 16-byte vector of each plane.
+__device__ __forceinline__ void rebuild32(const uint4 &h, const uint4 &l, const uint4 &e,
+                                          uint32_t b2, uint32_t out[16]) {
+    rebuild8(h.x, l.x, e.x, b2, out + 0);
+    rebuild8(h.y, l.y, e.y, b2, out + 4);
+    rebuild8(h.z, l.z, e.z, b2, out + 8);
+    rebuild8(h.w, l.w, e.w, b2, out + 12);
+}
+
+// Replace the exponent of escaped weights among the 32 weights
+// [pos0, pos0 + 32) of a group held in out[16] (pair r/2 of word r/8 ...).
+// m0 = meta[g], m1 = meta[g+1].  Indices are bounds-checked; a corrupt entry
+// range records W12_ERR_DEVICE and is skipped.
+__device__ __forceinline__ void patch_escapes(uint32_t out[16], uint32_t m0, uint32_t m1,
+                                                  uint32_t pos0, const uint16_t *esc,
+                                                  uint64_t n_esc, int *err) {
+    const uint32_t lo = m0 >> 8, hi = m1 >> 8;
+    if (hi < lo || uint64_t(hi) > n_esc || hi - lo > 128u) {
+        if (err) *err = W12_ERR_DEVICE;
+        return;
+    }
+    for (uint32_t i = lo; i < hi; ++i) {
+        const uint32_t ent = esc[i];
+        const uint32_t pos = ent & 0x7Fu;
+        if ((pos & ~31u) != pos0) continue;
+        const uint32_t j = pos & 31u;
+        const uint32_t idx = (j >> 3) * 4 + ((j & 7u) >> 1);
+        const uint32_t sh = (j & 1u) * 16u;
+        const uint32_t mask = 0x7F80u << sh;
+        const uint32_t val = (ent & 0x7F80u) << sh;
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+            if (uint32_t(q) == idx) out[q] = (out[q] & ~mask) | val;
+    }
+}
+
+// Float ordering key for the argmax: larger key = larger value; NaN above
+// everything; -0 and +0 equal.  Packed with ~index so ties go to the lowest.
+__device__ __forceinline__ uint32_t order_key(float f) {
+    uint32_t u = __float_as_uint(f);
+    if ((u & 0x7FFFFFFFu) > 0x7F800000u) return 0xFFFFFFFFu;  // NaN
+    if ((u & 0x7FFFFFFFu) == 0u) u = 0u;                      // -0 -> +0
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ unsigned long long pack_key(float f, uint32_t idx) {
+    return (static_cast<unsigned long long>(order_key(f)) << 32) | (0xFFFFFFFFu - idx);
+}
+
+__device__ __forceinline__ uint32_t key_index(unsigned long long k) {
+    return 0xFFFFFFFFu - static_cast<uint32_t>(k & 0xFFFFFFFFull);
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
+
+}  // namespace w12

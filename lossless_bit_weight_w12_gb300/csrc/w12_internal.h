@@ -1,0 +1,91 @@
+// w12_internal.h -- declarations shared by the library's own translation units.
+// Not installed; the public interface is include/w12.h.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/w12.h"
+
+namespace w12 {
+
+constexpr int kGroup = 128;        // weights per group along k
+constexpr int kMaxBase = 241;      // 241 + 14 = 255
+constexpr uint32_t kMaxEscapes = 1u << 24;
+
+inline uint64_t round256(uint64_t x) { return (x + 255u) & ~uint64_t(255); }
+
+// Offsets and sizes of format v1 for K x N with n_esc escapes.
+void layout_v1(int64_t K, int64_t N, uint64_t n_esc, w12_desc *d);
+
+// Workspace layout shared by the device calls: word 0 is the sticky error
+// code, counters start at byte 256, the fp32 partials after them.
+constexpr size_t kWsHeader = 256;
+
+// Kernel argument block for the GEMM paths (plain pointers, device side).
+struct GemmArgs {
+    const uint32_t *H, *L, *E;  // plane words, column-major, K/8 words per column
+    const uint32_t *meta;       // G + 1 words
+    const uint16_t *esc;        // n_esc entries
+    uint64_t n_esc;
+    int64_t K, N, KW, KG;       // KW = K/8, KG = K/128
+    const uint16_t *x;          // [M][K] bf16
+    int M;
+    void *y;                    // [M][N]
+    int y_dtype;                // W12_F32 / W12_BF16
+    float *partial;             // [nks][M][N] when nks > 1
+    uint32_t *counters;         // [NB] arrival counters when nks > 1
+    int *err;                   // workspace word 0
+    int64_t NB;                 // column tiles
+    int64_t cols_per_tile;
+    int nks;                    // k splits
+    int64_t kchunk;             // k per split (multiple of 128)
+    int64_t T;                  // NB * nks tiles
+    int64_t xchunk;             // k staged in shared memory at a time (MMA path)
+    // fused argmax + acceptance epilogue (lm_head verify); row_best NULL otherwise
+    unsigned long long *row_best;  // [grid][M] per-CTA best keys
+    float *logits_out;             // optional [M][N] copy of the fp32 logits
+    int64_t vR, vT;                // draft blocks: M = vR * vT
+    const int32_t *draft;          // [vR][vT-1]
+    int32_t *accept_len, *next_tok;
+    int32_t *gbuf;                 // [M] greedy tokens (scratch)
+};
+
+struct GemmPlan {
+    int path;        // W12_PATH_GEMV / W12_PATH_MMA
+    int variant;     // kernel template selector
+    int grid;
+    int64_t NB, cols_per_tile;
+    int nks;
+    int64_t kchunk, xchunk;
+    size_t ws_bytes;
+    // workspace offsets (bytes from the workspace start)
+    size_t off_counters, off_partial, off_best, off_gbuf;
+};
+
+int plan_gemm(const w12_desc *d, int64_t M, int path, int fused_argmax, GemmPlan *p);
+
+// Launchers (return W12_OK or W12_ERR_CUDA).
+int launch_decode(const w12_desc *d, const void *blob, uint16_t *w, int layout, int *err,
+                  void *stream);
+int launch_gemv(const GemmPlan &p, const GemmArgs &a, void *stream);
+int launch_mma(const GemmPlan &p, const GemmArgs &a, void *stream);
+int gemv_occupancy(int variant, int *blocks_per_sm);
+int mma_occupancy(int variant, size_t smem, int *blocks_per_sm);
+int device_sm_count(int *sms);
+
+struct VerifyArgs {
+    const void *logits;
+    int dtype;
+    int64_t R, T, V, rows;
+    const int32_t *draft;
+    int32_t *accept_len, *next_tok;
+    unsigned long long *partial;  // [rows][splits] keys
+    uint32_t *counter;
+    int32_t *gbuf;                // [rows] greedy tokens (scratch)
+    int64_t splits;
+    int64_t chunk;                // columns per split
+};
+int launch_verify(const VerifyArgs &a, int grid, void *stream);
+
+}  // namespace w12

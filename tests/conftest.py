@@ -18,3 +18,23 @@ def oracle():
     import oracle as o
     o.lib()
     return o
+
+
+@pytest.fixture(scope="session")
+def dev():
+    """cuda:0 with libw12.so built and loaded; GPU tests fail (not skip) without a GPU."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("GPU test collected on a machine without CUDA")
+    from lossless_bit_weight_w12_gb300 import build_lib, w12
+    build_lib.build()
+    w12.lib()
+    d = torch.device("cuda:0")
+    torch.cuda.set_device(d)
+    return d
+
+
+@pytest.fixture(scope="session")
+def w12mod(dev):
+    from lossless_bit_weight_w12_gb300 import w12
+    return w12

@@ -1,0 +1,186 @@
+"""W12 decode-GEMM on the GPU against the oracle's fp64 product.
+
+Acceptance (element by element): |y - y_ref| <= 2e-3 * sum_k |x_k w_k| + 1e-6
+for fp32 y; bf16 y adds 2^-8 |y_ref|.  One-hot activations must reproduce a
+weight row exactly: that pins the in-register rebuild and the escape patch
+bit for bit inside the GEMM (SpecPilot repository page, "项目介绍": decoded
+bit-exactly inside the GEMM).
+"""
+import numpy as np
+import pytest
+
+from helpers import bf16_bits_to_f64, check_gemm, dev_bits_to_np, to_dev_bits
+from lossless_bit_weight_w12_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(w12mod, dev, d, blob_d, x, path, y_dtype="f32"):
+    import torch
+    M = x.shape[0]
+    x_d = to_dev_bits(x, dev)
+    y_d = torch.empty((M, d.N), dtype=torch.float32 if y_dtype == "f32" else torch.bfloat16,
+                      device=dev)
+    ws = w12mod.workspace(w12mod.gemm_workspace_size(d, M), dev)
+    w12mod.gemm(d, blob_d, x_d, y_d, ws, path=path)
+    torch.cuda.synchronize()
+    assert w12mod.get_device_error(ws) == 0
+    if y_dtype == "f32":
+        return y_d.cpu().numpy().astype(np.float64)
+    return bf16_bits_to_f64(dev_bits_to_np(y_d))
+
+
+def _paths(M):
+    return [1, 2] if M <= 4 else [2]
+
+
+SHAPES = [(128, 1), (128, 7), (384, 33), (1024, 130), (1152, 257), (5120, 96), (6144, 64)]
+MS = [1, 2, 3, 4, 5, 8, 9, 16, 17, 32, 33, 64, 100, 128]
+
+
+@pytest.mark.parametrize("K,N", SHAPES)
+@pytest.mark.parametrize("M", MS)
+def test_gemm_random_vs_oracle(dev, w12mod, oracle, K, N, M):
+    rng = synth.streams(1000 + K + N + M, 2)
+    w = synth.weights(rng[0], K, N)
+    x = synth.activations(rng[1], M, K)
+    d, blob = w12mod.encode(w, w12mod.LAYOUT_NK)
+    od, oblob = oracle.encode(w, oracle.LAYOUT_NK)
+    y_ref, s_ref = oracle.gemm(od, oblob, x)
+    blob_d = w12mod.upload(blob, dev)
+    for path in _paths(M):
+        y = _run(w12mod, dev, d, blob_d, x, path)
+        check_gemm(y, y_ref, s_ref, what=f"K={K} N={N} M={M} path={path}")
+
+
+@pytest.mark.parametrize("M", [1, 3, 16, 40])
+def test_gemm_bf16_output(dev, w12mod, oracle, M):
+    K, N = 1024, 200
+    rng = synth.streams(77 + M, 2)
+    w = synth.weights(rng[0], K, N)
+    x = synth.activations(rng[1], M, K)
+    d, blob = w12mod.encode(w, w12mod.LAYOUT_NK)
+    y_ref, s_ref = oracle.gemm(*oracle.encode(w, oracle.LAYOUT_NK), x)
+    blob_d = w12mod.upload(blob, dev)
+    for path in _paths(M):
+        y = _run(w12mod, dev, d, blob_d, x, path, "bf16")
+        check_gemm(y, y_ref, s_ref, bf16=True, what=f"bf16 M={M} path={path}")
+
+
+@pytest.mark.parametrize("M", [1, 2, 4, 8, 16, 32, 128])
+def test_gemm_one_hot_is_exact(dev, w12mod, M):
+    """x = one-hot rows: y must equal the selected weight rows bit for bit,
+    escapes included (the recipe plants zeros and subnormals, and this matrix
+    adds NaN payloads and Infs)."""
+    K, N = 2048, 300
+    rng = synth.streams(5 + M, 2)
+    w = synth.weights(rng[0], K, N)
+    w[::7, 3] = 0x7FC1   # NaN payload rows in column 3 (escapes)
+    w[5, ::11] = 0xFF80  # -Inf in row 5 (escapes)
+    d, blob = w12mod.encode(w, w12mod.LAYOUT_NK)
+    blob_d = w12mod.upload(blob, dev)
+    ks = rng[1].integers(0, K, M)
+    x = np.zeros((M, K), dtype=np.uint16)
+    x[np.arange(M), ks] = 0x3F80
+    want = bf16_bits_to_f64(w[:, ks].T)  # [M, N]
+    for path in _paths(M):
+        y = _run(w12mod, dev, d, blob_d, x, path)
+        nan = np.isnan(want)
+        assert np.array_equal(np.isnan(y), nan)
+        np.testing.assert_array_equal(y[~nan], want[~nan])
+
+
+def test_gemm_nonfinite(dev, w12mod, oracle):
+    K, N, M = 512, 40, 3
+    rng = synth.streams(9, 2)
+    w = synth.weights(rng[0], K, N)
+    w[10, 3] = 0x7F80  # +Inf
+    w[200, 7] = 0x7FC0  # NaN
+    w[300, 9] = 0xFF80  # -Inf
+    x = synth.activations(rng[1], M, K)
+    x[:, :] = np.where(x == 0, 0x3F80, x)  # no zero activations (0 * Inf = NaN)
+    d, blob = w12mod.encode(w, w12mod.LAYOUT_NK)
+    y_ref, s_ref = oracle.gemm(*oracle.encode(w, oracle.LAYOUT_NK), x)
+    blob_d = w12mod.upload(blob, dev)
+    for path in _paths(M):
+        y = _run(w12mod, dev, d, blob_d, x, path)
+        check_gemm(y, y_ref, s_ref, what=f"nonfinite path={path}")
+
+
+def test_gemm_deterministic(dev, w12mod):
+    import torch
+    K, N, M = 17408, 640, 16
+    rng = synth.streams(3, 2)
+    w = synth.weights(rng[0], K, N)
+    x = to_dev_bits(synth.activations(rng[1], M, K), dev)
+    d, blob = w12mod.encode(w, w12mod.LAYOUT_NK)
+    blob_d = w12mod.upload(blob, dev)
+    ws = w12mod.workspace(w12mod.gemm_workspace_size(d, M), dev)
+    ys = []
+    for _ in range(3):
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+        w12mod.gemm(d, blob_d, x, y, ws)
+        ys.append(y)
+    assert torch.equal(ys[0], ys[1]) and torch.equal(ys[1], ys[2])
+
+
+@pytest.mark.parametrize("M", [1, 16, 32, 128])
+def test_gemm_full_layer_sampled(dev, w12mod, oracle, M):
+    """Config-1..3 layer shapes at full size, in the launch configuration the
+    bench times, checked on 24 sampled columns x all M rows each."""
+    seed = {1: 1, 16: 2, 32: 3, 128: 3}[M]
+    rng = synth.streams(seed, len(synth.LAYER_SHAPES) + 8)
+    for i, (name, K, N) in enumerate(synth.LAYER_SHAPES):
+        w = synth.weights(rng[i], K, N)
+        x = synth.activations(rng[len(synth.LAYER_SHAPES) + i], M, K)
+        d, blob = w12mod.encode(w, w12mod.LAYOUT_NK)
+        blob_d = w12mod.upload(blob, dev)
+        y = _run(w12mod, dev, d, blob_d, x, 0)
+        pick = np.random.default_rng(i)
+        ns = np.unique(np.r_[pick.integers(0, N, 22), [0, N - 1]])
+        # the oracle encodes and multiplies only the sampled columns
+        od, oblob = oracle.encode(w[ns], oracle.LAYOUT_NK)
+        y_ref, s_ref = oracle.gemm(od, oblob, x)
+        check_gemm(y[:, ns], y_ref, s_ref, what=f"{name} M={M}")
+        del blob_d
+
+
+def test_gemm_argument_errors(dev, w12mod):
+    import torch
+    K, N = 256, 16
+    w = np.full((N, K), 0x3F80, dtype=np.uint16)
+    d, blob = w12mod.encode(w, w12mod.LAYOUT_NK)
+    blob_d = w12mod.upload(blob, dev)
+    x = torch.zeros((4, K), dtype=torch.int16, device=dev)
+    y = torch.empty((4, N), dtype=torch.float32, device=dev)
+    need = w12mod.gemm_workspace_size(d, 4)
+    assert need >= 256
+    small = w12mod.workspace(256, dev)[:128]
+    with pytest.raises(w12mod.W12Error) as e:
+        w12mod.gemm(d, blob_d, x, y, small)
+    assert e.value.status == w12mod.ERR_WORKSPACE
+    ws = w12mod.workspace(need, dev)
+    with pytest.raises(w12mod.W12Error) as e:  # the GEMV path serves M <= 4 only
+        w12mod.gemm(d, blob_d, torch.zeros((5, K), dtype=torch.int16, device=dev),
+                    torch.empty((5, N), dtype=torch.float32, device=dev), ws,
+                    path=w12mod.PATH_GEMV)
+    assert e.value.status == w12mod.ERR_SHAPE
+    with pytest.raises(w12mod.W12Error) as e:
+        w12mod.gemm(d, blob_d, torch.zeros((129, K), dtype=torch.int16, device=dev),
+                    torch.empty((129, N), dtype=torch.float32, device=dev), ws)
+    assert e.value.status == w12mod.ERR_SHAPE
+    xs = torch.zeros(4 * K + 8, dtype=torch.int16, device=dev)[1:1 + 4 * K].view(4, K)
+    with pytest.raises(w12mod.W12Error) as e:
+        w12mod.gemm(d, blob_d, xs, y, ws)
+    assert e.value.status == w12mod.ERR_ALIGN
+
+
+def test_gemm_k_zero_writes_zeros(dev, w12mod):
+    import torch
+    w = np.zeros((9, 0), dtype=np.uint16)
+    d, blob = w12mod.encode(w, w12mod.LAYOUT_NK)
+    y = torch.full((2, 9), 5.0, dtype=torch.float32, device=dev)
+    x = torch.zeros((2, 0), dtype=torch.int16, device=dev)
+    ws = w12mod.workspace(256, dev)
+    w12mod.gemm(d, w12mod.workspace(256, dev), x, y, ws)
+    assert torch.count_nonzero(y).item() == 0
