@@ -13,10 +13,11 @@
  *    rebuilt bit for bit ("SpecPilot" summary pages, p5 "Reasons", second
  *    bullet; p4 "项目介绍", second paragraph: decoded bit-exactly inside the
  *    GEMM).  The pages give no layout; the one coded here is the documented
- *    W12 v1 layout: plane H = sign and the top 3 mantissa bits, plane L = the
- *    low 4 mantissa bits, plane E = the exponent as a 4-bit offset from a base
- *    shared by a group of 128 consecutive k of one output column, with code 15
- *    meaning "escape: the true exponent is in a side list".
+ *    W12 v1 layout: planes H and L = the high and low nibble of the byte
+ *    (mantissa << 1 | sign of the pair partner), plane E = the exponent as a
+ *    4-bit offset from a base shared by a group of 128 consecutive k of one
+ *    output column, with code 15 meaning "escape: the true exponent is in a
+ *    side list".
  *  - The GEMM: y[m,n] = sum_k x[m,k] * w[k,n], accumulated in fp64 in k order
  *    (products of two bf16 values are exact in fp64).
  *  - Greedy verification (p5 "Risks", third bullet: under greedy decoding
@@ -48,7 +49,7 @@
 #define W12REF_GROUP 128   /* weights per group, along k                  */
 #define W12REF_WINDOW 15   /* exponent offsets 0..14 are coded directly   */
 #define W12REF_ESC_CODE 15 /* code meaning "exponent is in the side list" */
-#define W12REF_MAX_BASE 241 /* largest base: 241 + 14 = 255                */
+#define W12REF_MAX_BASE 240 /* largest base: 240 + 15 = 255 fits a byte      */
 #define W12REF_MAX_ESC (1u << 24)
 
 typedef struct {
@@ -85,7 +86,7 @@ static uint16_t weight_at(const uint16_t *w, int64_t K, int64_t N, int layout, i
 /* Logical codec: base, codes, escapes                                      */
 /* ---------------------------------------------------------------------- */
 
-/* Base of one group of 128 exponents: the b in [0, 241] whose window
+/* Base of one group of 128 exponents: the b in [0, 240] whose window
  * [b, b+14] holds the most exponents; among equally good b, the largest. */
 int w12ref_group_base(const uint16_t *vals)
 {
@@ -130,10 +131,16 @@ static void gather_group(const uint16_t *w, int64_t K, int64_t N, int layout, in
  * little-endian 32-bit word of a plane covers the 8 weights k0..k0+7
  * (k0 a multiple of 8); its nibble q (bits 4q..4q+3) holds the nibble of
  * weight k0 + PERM[q], with one permutation per plane.
+ *
+ * Weights pair up as (k0, k0+1), (k0+2, k0+3), ...  The two mantissa planes
+ * together hold, for weight j, the byte SM'(j) = m(j) << 1 | s(j ^ 1): its
+ * 7-bit mantissa shifted up one place and the SIGN OF ITS PAIR PARTNER in
+ * bit 0.  H holds the high nibble of SM'(j), L the low nibble.  E holds the
+ * exponent code.
  */
 static const int PERM_H[8] = {4, 0, 5, 1, 6, 2, 7, 3};
 static const int PERM_L[8] = {0, 5, 1, 6, 2, 7, 3, 4};
-static const int PERM_E[8] = {0, 2, 4, 6, 1, 3, 5, 7};
+static const int PERM_E[8] = {0, 4, 1, 5, 2, 6, 3, 7};
 
 static int slot_of(const int *perm, int r)
 {
@@ -243,10 +250,12 @@ int w12ref_encode(const uint16_t *w, int64_t K, int64_t N, int layout, const w12
         for (int p = 0; p < W12REF_GROUP; ++p) {
             uint16_t v = grp[p];
             int64_t k = kg * W12REF_GROUP + p;
-            unsigned s = bf16_sign(v), e = bf16_exp(v), m = bf16_man(v);
+            unsigned e = bf16_exp(v), m = bf16_man(v);
+            unsigned partner_sign = bf16_sign(grp[p ^ 1]); /* pairs never straddle a group */
+            unsigned smp = (m << 1) | partner_sign;
             unsigned c = exp_code(e, b);
-            put_nibble(H, K, k, n, PERM_H, (s << 3) | (m >> 4));
-            put_nibble(L, K, k, n, PERM_L, m & 0xFu);
+            put_nibble(H, K, k, n, PERM_H, smp >> 4);
+            put_nibble(L, K, k, n, PERM_L, smp & 0xFu);
             put_nibble(E, K, k, n, PERM_E, c);
             if (c == W12REF_ESC_CODE) {
                 if (next >= d->n_esc)
@@ -272,6 +281,8 @@ static int weight_from_blob(const w12ref_desc *d, const uint8_t *blob, int64_t k
     const uint16_t *esc = (const uint16_t *)(blob + d->off_esc);
     unsigned h = get_nibble(blob + d->off_h, K, k, n, PERM_H);
     unsigned l = get_nibble(blob + d->off_l, K, k, n, PERM_L);
+    /* the sign of weight k sits in bit 0 of its pair partner's L nibble */
+    unsigned l_partner = get_nibble(blob + d->off_l, K, k ^ 1, n, PERM_L);
     unsigned c = get_nibble(blob + d->off_e, K, k, n, PERM_E);
     unsigned b = meta[g] & 0xFFu;
     unsigned e;
@@ -295,7 +306,8 @@ static int weight_from_blob(const w12ref_desc *d, const uint8_t *blob, int64_t k
     }
     if (e > 255u)
         return W12REF_ERR_BLOB;
-    unsigned s = (h >> 3) & 1u, m = ((h & 7u) << 4) | l;
+    unsigned smp = (h << 4) | l;          /* m << 1 | sign of the partner */
+    unsigned m = smp >> 1, s = l_partner & 1u;
     *out = (uint16_t)((s << 15) | (e << 7) | m);
     return W12REF_OK;
 }

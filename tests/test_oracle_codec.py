@@ -61,7 +61,7 @@ def test_roundtrip_recipe_and_escape_count(oracle):
         for kg in range(w.shape[1] // 128):
             e = _exp(w[n, kg * 128:(kg + 1) * 128])
             hist = np.bincount(e, minlength=256)
-            cover = np.array([hist[b:b + 15].sum() for b in range(242)])
+            cover = np.array([hist[b:b + 15].sum() for b in range(241)])
             total += 128 - cover.max()
     assert d.n_esc == total
     assert total > 0  # the recipe plants zeros and subnormals
@@ -116,11 +116,14 @@ def _group(exps, sign=0, man=0):
 def test_base_closed_forms(oracle):
     # span <= 14: the window starting at the minimum holds everything
     assert oracle.group_base(_group(np.r_[[100] * 64, [110] * 64])) == 100
-    # one value everywhere: b = e, clamped to 241 at the top
+    # one value everywhere: b = e, clamped to 240 at the top
     assert oracle.group_base(_group([77] * 128)) == 77
     assert oracle.group_base(_group([0] * 128)) == 0           # all +0
-    assert oracle.group_base(_group([255] * 128)) == 241       # all Inf/NaN
-    assert oracle.group_base(_group([250] * 128)) == 241
+    # the base stops at 240 (so b + 15 fits a byte): a group of Inf/NaN
+    # (e = 255) is covered by no window; every window ties at 0 -> b = 240
+    assert oracle.group_base(_group([255] * 128)) == 240
+    assert oracle.group_base(_group([250] * 128)) == 240       # window [240, 254]
+    assert oracle.group_base(_group([254] * 128)) == 240
     # two clusters 20 apart: the larger cluster wins; largest b covering it
     assert oracle.group_base(_group(np.r_[[100] * 100, [120] * 28])) == 100
     assert oracle.group_base(_group(np.r_[[100] * 28, [120] * 100])) == 120
@@ -140,8 +143,8 @@ def test_base_bruteforce_random(oracle):
         vals = _group(e, sign=int(rng.integers(0, 2)), man=int(rng.integers(0, 128)))
         b = oracle.group_base(vals)
         hist = np.bincount(e, minlength=256)
-        cover = np.array([hist[x:x + 15].sum() for x in range(242)])
-        assert 0 <= b <= 241
+        cover = np.array([hist[x:x + 15].sum() for x in range(241)])
+        assert 0 <= b <= 240
         assert cover[b] == cover.max()
         assert b == int(np.flatnonzero(cover == cover.max()).max())
 
