@@ -75,24 +75,26 @@ extern "C" {
  * Logical format.  A group is 128 consecutive k of one output column n:
  * group g = n*(K/128) + k/128, pos = k % 128.  A bf16 weight has sign s
  * (bit 15), exponent e (bits 14..7) and mantissa m (bits 6..0).  Each group
- * has a base b in [0, 241]: the b whose window [b, b+14] holds the most of
+ * has a base b in [0, 240]: the b whose window [b, b+14] holds the most of
  * the group's exponents, the largest such b on a tie.  A weight's exponent
  * code is c = e - b inside the window and 15 ("escape") outside it.  Escaped
  * weights get a 16-bit entry pos | e << 7 in the escape list, ordered by
  * group then pos.  meta[g] = b | first_escape_index(g) << 8, and
- * meta[G] = n_esc << 8.
+ * meta[G] = n_esc << 8.  Weights k and k^1 (an even k and the next) form a
+ * pair; each stores its pair partner's sign.
  *
  * Physical format (byte offsets from the blob start; each section starts on
  * a 256-byte boundary; the blob start itself must be 256-byte aligned):
- *   H plane  at off_h:    N*K/2 bytes, nibble = s << 3 | m >> 4
- *   L plane  at off_l:    N*K/2 bytes, nibble = m & 15
- *   E plane  at off_e:    N*K/2 bytes, nibble = c
+ *   H plane  at off_h:    N*K/2 bytes, nibble = SM'(k) >> 4
+ *   L plane  at off_l:    N*K/2 bytes, nibble = SM'(k) & 15
+ *   E plane  at off_e:    N*K/2 bytes, nibble = c(k)
  *   meta     at off_meta: (G+1) little-endian uint32
  *   escapes  at off_esc:  n_esc little-endian uint16
+ * with SM'(k) = m(k) << 1 | s(k ^ 1).
  * Planes are column-major: column n owns bytes [n*K/2, (n+1)*K/2).  The
  * little-endian 32-bit word at index n*K/8 + k0/8 of a plane covers weights
  * k0..k0+7 of column n; its nibble q (bits 4q..4q+3) holds weight k0+P[q]:
- *   H: P = {4,0,5,1,6,2,7,3}   L: P = {0,5,1,6,2,7,3,4}   E: P = {0,2,4,6,1,3,5,7}
+ *   H: P = {4,0,5,1,6,2,7,3}   L: P = {0,5,1,6,2,7,3,4}   E: P = {0,4,1,5,2,6,3,7}
  * total_bytes covers all five sections rounded up to 256.
  */
 typedef struct w12_desc {

@@ -59,45 +59,31 @@ void finish_ws_layout(GemmPlan *p, int64_t M, int64_t N, bool fused) {
     p->ws_bytes = off;
 }
 
+// GEMV: stream-K over units of one stage (gemv_cols_per_tile() columns x
+// gemv_stage_k() k); every CTA gets the same number of units.
 int plan_gemv(const w12_desc *d, int64_t M, const Device &dv, GemmPlan *p) {
-    struct V {
-        int id, cpw, mt;
-    };
-    static const V vs[] = {{0, 1, 1}, {1, 2, 1}, {2, 4, 1}, {3, 1, 2}, {4, 2, 2}, {5, 1, 4}};
-    const int mt = M <= 1 ? 1 : M <= 2 ? 2 : 4;
-    const int64_t steps = ceil_div(d->K, 1024);
-    double best = 1e300;
-    bool found = false;
-    for (const V &v : vs) {
-        if (v.mt != mt) continue;
-        int occ = 0;
-        if (gemv_occupancy(v.id, &occ) != W12_OK) return W12_ERR_CUDA;
-        if (occ < 1) continue;
-        const int64_t grid = int64_t(dv.sms) * occ;
-        const int64_t NB = ceil_div(d->N, 8 * v.cpw);
-        for (int64_t nks = 1; nks <= steps; ++nks) {
-            const int64_t cs = ceil_div(steps, nks);
-            const int64_t eff = ceil_div(steps, cs);
-            if (eff != nks) continue;
-            const int64_t T = NB * eff;
-            const double work = double(8 * v.cpw) * double(cs * 1024);
-            const double c = makespan(T, grid, work, int(eff), d->N, M, d->K) / (1.0 + 0.02 * v.cpw);
-            if (c < best) {
-                best = c;
-                found = true;
-                p->path = W12_PATH_GEMV;
-                p->variant = v.id;
-                p->grid = int(std::min<int64_t>(grid, T));
-                p->NB = NB;
-                p->cols_per_tile = 8 * v.cpw;
-                p->nks = int(eff);
-                p->kchunk = cs * 1024;
-                p->xchunk = 0;
-            }
-        }
-    }
-    if (!found) return W12_ERR_CUDA;
-    finish_ws_layout(p, M, d->N, false);
+    const int variant = M <= 1 ? 0 : M <= 2 ? 1 : 2;
+    const int64_t cpt = gemv_cols_per_tile(), sk = gemv_stage_k();
+    int occ = 0;
+    if (gemv_occupancy(variant, &occ) != W12_OK) return W12_ERR_CUDA;
+    if (occ < 1) return W12_ERR_CUDA;
+    std::memset(p, 0, sizeof *p);
+    p->path = W12_PATH_GEMV;
+    p->variant = variant;
+    p->steps = ceil_div(d->K, sk);
+    p->NB = ceil_div(d->N, cpt);
+    p->U = p->NB * p->steps;
+    p->grid = int(std::min<int64_t>(int64_t(dv.sms) * occ, p->U));
+    p->cols_per_tile = cpt;
+    p->nks = 1;
+    p->kchunk = sk;
+    size_t off = kWsHeader;
+    p->off_counters = off;
+    off += round256(4u * uint64_t(p->NB));
+    p->off_partial = off;
+    off += round256(uint64_t(p->U) * uint64_t(M) * uint64_t(cpt) * 4u);
+    p->off_best = p->off_gbuf = off;
+    p->ws_bytes = off;
     return W12_OK;
 }
 
@@ -172,11 +158,14 @@ GemmArgs make_args(const w12_desc *d, const void *blob, const uint16_t *x, int64
     a.nks = p.nks;
     a.kchunk = p.kchunk;
     a.xchunk = p.xchunk;
-    a.T = p.NB * p.nks;
+    a.T = p.path == W12_PATH_GEMV ? p.U : p.NB * p.nks;
+    a.U = p.U;
+    a.steps = p.steps;
     return a;
 }
 
 int choose_plan(const w12_desc *d, int64_t M, int path, bool fused, GemmPlan *p) {
+    std::memset(p, 0, sizeof *p);
     Device dv;
     if (query_device(&dv) != W12_OK) return W12_ERR_CUDA;
     if (path == W12_PATH_AUTO) path = (M == 1 && !fused) ? W12_PATH_GEMV : W12_PATH_MMA;

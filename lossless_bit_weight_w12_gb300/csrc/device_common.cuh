@@ -2,16 +2,21 @@
 //
 // "Reconstructing bit by bit in GEMM registers" (SpecPilot summary,
 // airadar.tv English edition, "Reasons" bullet 2): one 32-bit word from each
-// of the H, L and E planes covers 8 consecutive k of one column; the
-// nibble order inside each word (include/w12.h) is chosen so that the 8
-// bf16 values come out as 4 bf16x2 registers (k0,k0+1), (k0+2,k0+3), ...
-// in 20 integer instructions:
-//   SMA = (H & 0xF0F0F0F0) | (L & 0x0F0F0F0F)   sign|mantissa bytes of k0..k0+3
-//   SMB = rotl((H & 0x0F0F0F0F) | (L & 0xF0F0F0F0), 4)              k0+4..k0+7
-//   P_i = prmt(SM, sign-replicating selector)  mantissa in bits 0-6, sign in 15
-//   X_i = ((E >> 4i') & 0x000F000F) << 7 + b * 0x00800080   exponent b + c
-//   out_i = (P_i & 0x807F807F) | (X_i & 0x7F807F80)
-// An escape (code 15) leaves a wrong exponent that patch_escapes() replaces.
+// of the H, L and E planes covers 8 consecutive k of one column; the nibble
+// order inside each word (include/w12.h) is chosen so that the 8 bf16 values
+// come out as 4 bf16x2 registers (k0,k0+1), (k0+2,k0+3), ... in 16 integer
+// instructions (14 on the ALU pipe, 2 adds that can run as IMAD):
+//   SMA = (H & 0xF0F0F0F0) | (L & 0x0F0F0F0F)   bytes SM'(k0..k0+3)
+//   SMB = rotl((H & 0x0F0F0F0F) | (L & 0xF0F0F0F0), 4)      SM'(k0+4..k0+7)
+//   XE  = (E & 0x0F0F0F0F) + b * 0x01010101      exponents of k0..k0+3
+//   XO  = ((E >> 4) & 0x0F0F0F0F) + b * 0x01010101           k0+4..k0+7
+//   P_i = rotr(prmt(SM, X, [SM'lo, e lo, SM'hi, e hi]), 1)
+// where SM'(j) = m(j) << 1 | s(partner of j): after the byte gather a pair
+// word reads [e_hi | m_hi | s_lo | e_lo | m_lo | s_hi] and one 32-bit rotate
+// right moves every field of both halves into its bf16 place, the two signs
+// crossing over.  The base is at most 240, so b + code (<= 255) never carries
+// between bytes.  An escape (code 15) leaves a wrong exponent that
+// patch_escapes() replaces.
 #pragma once
 
 #include <cstdint>
@@ -45,38 +50,49 @@ __device__ __forceinline__ uint4 ldg_v4(const void *p) {
     return r;
 }
 
-// prmt with the sign-replicate bit honoured (bit 3 of each selector nibble).
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t sel) {
+// Byte gather from two registers: selector nibble i picks byte (0-3 of a,
+// 4-7 of b) for result byte i.
+__device__ __forceinline__ uint32_t prmt2(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t d;
-    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(d) : "r"(a), "r"(sel));
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
     return d;
 }
 
 // Rebuild 8 weights (one word of each plane) into 4 bf16x2 registers.
-// b2 = base * 0x00800080.
-__device__ __forceinline__ void rebuild8(uint32_t h, uint32_t l, uint32_t e, uint32_t b2,
+// b4 = base * 0x01010101.
+__device__ __forceinline__ void rebuild8(uint32_t h, uint32_t l, uint32_t e, uint32_t b4,
                                          uint32_t out[4]) {
     const uint32_t sma = (h & 0xF0F0F0F0u) | (l & 0x0F0F0F0Fu);
     const uint32_t xx = (h & 0x0F0F0F0Fu) | (l & 0xF0F0F0F0u);
     const uint32_t smb = __funnelshift_l(xx, xx, 4);
-    const uint32_t e8 = e >> 8;
-    const uint32_t x0 = (e & 0x000F000Fu) * 128u + b2;
-    const uint32_t x1 = (e & 0x00F000F0u) * 8u + b2;
-    const uint32_t x2 = (e8 & 0x000F000Fu) * 128u + b2;
-    const uint32_t x3 = (e8 & 0x00F000F0u) * 8u + b2;
-    out[0] = (prmt(sma, 0x9180u) & kSignManMask) | (x0 & ~kSignManMask);
-    out[1] = (prmt(sma, 0xB3A2u) & kSignManMask) | (x1 & ~kSignManMask);
-    out[2] = (prmt(smb, 0x9180u) & kSignManMask) | (x2 & ~kSignManMask);
-    out[3] = (prmt(smb, 0xB3A2u) & kSignManMask) | (x3 & ~kSignManMask);
+    const uint32_t xe = (e & 0x0F0F0F0Fu) + b4;
+    const uint32_t xo = ((e >> 4) & 0x0F0F0F0Fu) + b4;
+    const uint32_t p0 = prmt2(sma, xe, 0x5140u), p1 = prmt2(sma, xe, 0x7362u);
+    const uint32_t p2 = prmt2(smb, xo, 0x5140u), p3 = prmt2(smb, xo, 0x7362u);
+    out[0] = __funnelshift_r(p0, p0, 1);
+    out[1] = __funnelshift_r(p1, p1, 1);
+    out[2] = __funnelshift_r(p2, p2, 1);
+    out[3] = __funnelshift_r(p3, p3, 1);
 }
 
 // Rebuild the 32 weights of one 16-byte vector of each plane.
 __device__ __forceinline__ void rebuild32(const uint4 &h, const uint4 &l, const uint4 &e,
-                                          uint32_t b2, uint32_t out[16]) {
-    rebuild8(h.x, l.x, e.x, b2, out + 0);
-    rebuild8(h.y, l.y, e.y, b2, out + 4);
-    rebuild8(h.z, l.z, e.z, b2, out + 8);
-    rebuild8(h.w, l.w, e.w, b2, out + 12);
+                                          uint32_t b4, uint32_t out[16]) {
+    rebuild8(h.x, l.x, e.x, b4, out + 0);
+    rebuild8(h.y, l.y, e.y, b4, out + 4);
+    rebuild8(h.z, l.z, e.z, b4, out + 8);
+    rebuild8(h.w, l.w, e.w, b4, out + 12);
+}
+
+__device__ __forceinline__ uint32_t base4(uint32_t meta_word) { return (meta_word & 0xFFu) * 0x01010101u; }
+
+// acc_lo += w.lo * x.lo, acc_hi += w.hi * x.hi: bf16 operands, fp32
+// accumulate, one rounding (the product of two bf16 values is exact in fp32).
+__device__ __forceinline__ void fma_bf16x2(float &acc_lo, float &acc_hi, uint32_t w, uint32_t x) {
+    asm("{\n .reg .b16 wl, wh, xl, xh;\n mov.b32 {wl, wh}, %2;\n mov.b32 {xl, xh}, %3;\n"
+        " fma.rn.f32.bf16 %0, wl, xl, %0;\n fma.rn.f32.bf16 %1, wh, xh, %1;\n}\n"
+        : "+f"(acc_lo), "+f"(acc_hi)
+        : "r"(w), "r"(x));
 }
 
 // Replace the exponent of escaped weights among the 32 weights

@@ -1,9 +1,10 @@
 // encode.cpp -- host encoder and validator for the W12 v1 blob.
 //
 // W12 splits each bf16 weight into three 4-bit planes (SpecPilot summary,
-// airadar.tv English edition, "Reasons" bullet 2): sign + top mantissa bits,
-// low mantissa bits, and a 4-bit exponent code relative to a per-group base
-// with an escape list for exponents outside the group window.  The layout is
+// airadar.tv English edition, "Reasons" bullet 2): the high and low nibble of
+// the byte (mantissa << 1 | sign of the pair partner), and a 4-bit exponent
+// code relative to a per-group base with an escape list for exponents
+// outside the group window.  The layout is
 // the one documented in include/w12.h.  Groups are independent, so both
 // passes run OpenMP-parallel over groups.
 #include <cstring>
@@ -18,7 +19,7 @@ namespace {
 // Nibble slot -> weight index inside an 8-weight word, per plane.
 constexpr int kPermH[8] = {4, 0, 5, 1, 6, 2, 7, 3};
 constexpr int kPermL[8] = {0, 5, 1, 6, 2, 7, 3, 4};
-constexpr int kPermE[8] = {0, 2, 4, 6, 1, 3, 5, 7};
+constexpr int kPermE[8] = {0, 4, 1, 5, 2, 6, 3, 7};
 
 inline unsigned exp_of(uint16_t v) { return (v >> 7) & 0xFFu; }
 
@@ -185,9 +186,13 @@ extern "C" int w12_encode(const uint16_t *w, int64_t K, int64_t N, int layout, c
             const uint16_t *q = v + 8 * wi;
             uint32_t hw = 0, lw = 0, ew = 0;
             for (int s = 0; s < 8; ++s) {
-                const uint16_t vh = q[kPermH[s]], vl = q[kPermL[s]], ve = q[kPermE[s]];
-                const uint32_t hn = ((vh >> 15) << 3) | ((vh & 0x7Fu) >> 4);
-                const uint32_t ln = vl & 0xFu;
+                // byte m << 1 | sign of the pair partner (weights 2i and 2i+1)
+                const int jh = kPermH[s], jl = kPermL[s];
+                const uint32_t smh = ((q[jh] & 0x7Fu) << 1) | (q[jh ^ 1] >> 15);
+                const uint32_t sml = ((q[jl] & 0x7Fu) << 1) | (q[jl ^ 1] >> 15);
+                const uint16_t ve = q[kPermE[s]];
+                const uint32_t hn = smh >> 4;
+                const uint32_t ln = sml & 0xFu;
                 const unsigned ee = exp_of(ve);
                 const uint32_t en = in_window(ee, b) ? ee - b : 15u;
                 hw |= hn << (4 * s);
@@ -234,7 +239,7 @@ extern "C" int w12_validate(const w12_desc *d, const void *blob_host) {
         for (int wi = 0; wi < kGroup / 8; ++wi) {
             const uint32_t ew = load_u32(E + 4 * (uint64_t(n) * KW + uint64_t(kg) * 16 + wi));
             for (int r = 0; r < 8; ++r) {
-                const int s = (r & 1) ? 4 + (r >> 1) : (r >> 1);  // slot of weight r in E
+                const int s = (r < 4) ? 2 * r : 2 * (r - 4) + 1;  // slot of weight r in E
                 if (((ew >> (4 * s)) & 0xFu) == 15u) flagged[nf++] = 8 * wi + r;
             }
         }

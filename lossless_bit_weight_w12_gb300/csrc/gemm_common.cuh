@@ -39,25 +39,68 @@ __device__ __forceinline__ void emit(const GemmArgs &a, int64_t kc, int64_t m, i
         a.partial[(kc * a.M + m) * a.N + n] = v;
 }
 
-// Called by every thread of the CTA after its tile's outputs are emitted.
-__device__ __forceinline__ void finish_tile(const GemmArgs &a, int64_t nb, int *s_last) {
+// Barrier over the threads taking part in the epilogue: the whole CTA, or
+// the first nthreads of it (named barrier 1) when a producer warp is apart.
+__device__ __forceinline__ void epi_sync(int nthreads) {
+    if (nthreads == int(blockDim.x))
+        __syncthreads();
+    else
+        asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+// Called by every epilogue thread (tid < nthreads) after its tile's outputs
+// are emitted.
+__device__ __forceinline__ void finish_tile(const GemmArgs &a, int64_t nb, int *s_last, int tid,
+                                            int nthreads) {
     if (a.nks == 1) return;
     __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) *s_last = (atomicAdd(&a.counters[nb], 1u) == uint32_t(a.nks - 1));
-    __syncthreads();
+    epi_sync(nthreads);
+    if (tid == 0) *s_last = (atomicAdd(&a.counters[nb], 1u) == uint32_t(a.nks - 1));
+    epi_sync(nthreads);
     if (*s_last) {
         __threadfence();
         const int64_t cpt = a.cols_per_tile;
-        for (int64_t o = threadIdx.x; o < cpt * a.M; o += blockDim.x) {
+        for (int64_t o = tid; o < cpt * a.M; o += nthreads) {
             const int64_t m = o / cpt, n = nb * cpt + o % cpt;
             if (n >= a.N) continue;
             float s = 0.f;
             for (int kc = 0; kc < a.nks; ++kc) s += __ldcg(&a.partial[(kc * a.M + m) * a.N + n]);
             store_y(a, m, n, s);
         }
-        if (threadIdx.x == 0) a.counters[nb] = 0u;
+        if (tid == 0) a.counters[nb] = 0u;
     }
+    epi_sync(nthreads);  // s_last is reused by the next tile
+}
+
+// Stream-K fix-up of column tile nb after a CTA covered `count` of its
+// `steps` stages and stored its partial sums in slot (nb, first stage).  The
+// CTA that completes the tile sums the slots in stage order (deterministic),
+// writes y, and zeroes the slots and the counter for the next call.
+__device__ __forceinline__ void streamk_fixup(const GemmArgs &a, int64_t nb, int64_t count,
+                                              int *s_last, int tid, int nthreads) {
+    __threadfence();
+    epi_sync(nthreads);
+    if (tid == 0) {
+        const uint32_t old = atomicAdd(&a.counters[nb], uint32_t(count));
+        *s_last = (int64_t(old) + count == a.steps);
+    }
+    epi_sync(nthreads);
+    if (*s_last) {
+        __threadfence();
+        const int64_t cpt = a.cols_per_tile;
+        for (int64_t o = tid; o < cpt * a.M; o += nthreads) {
+            const int64_t m = o / cpt, c = o % cpt, n = nb * cpt + c;
+            float s = 0.f;
+            for (int64_t ks = 0; ks < a.steps; ++ks) {
+                float *slot = &a.partial[((nb * a.steps + ks) * a.M + m) * cpt + c];
+                s += __ldcg(slot);
+                *slot = 0.f;
+            }
+            if (n < a.N) store_y(a, m, n, s);
+        }
+        if (tid == 0) a.counters[nb] = 0u;
+    }
+    epi_sync(nthreads);
 }
 
 }  // namespace w12

@@ -30,7 +30,7 @@ __device__ __forceinline__ void decode_vector(const DecodeArgs &a, int64_t v, ui
     const uint4 e = ldg_stream(a.E + 4 * v);
     const int64_t g = v >> 2;  // 4 vectors per group
     const uint32_t m0 = ldg_u32(a.meta + g), m1 = ldg_u32(a.meta + g + 1);
-    rebuild32(h, l, e, (m0 & 0xFFu) * 0x00800080u, out);
+    rebuild32(h, l, e, base4(m0), out);
     if (m0 >> 8 != m1 >> 8) patch_escapes(out, m0, m1, uint32_t(v & 3) * 32u, a.esc, a.n_esc, a.err);
 }
 

@@ -1,29 +1,47 @@
-// kernels_gemv.cu -- W12 GEMV for M <= 4: CUDA-core FFMA, warp-shuffle reduce.
+// kernels_gemv.cu -- W12 GEMV for M <= 4: cp.async-pipelined weight stream,
+// mixed bf16 x bf16 -> fp32 FMA on the CUDA cores, warp-shuffle reduction.
 //
 // At M = 1 a skinny decode step is a pure weight stream (SpecPilot summary,
-// airadar.tv English edition, first paragraph: a single request reads all
-// target weights per step), so the kernel is built around HBM: each lane
-// streams 16-byte vectors of the three planes (32 consecutive k of one
-// column, L1 bypassed), rebuilds them in registers (rebuild32: ~2.5 integer
-// ops per weight), and feeds packed fp32x2 FMAs (Blackwell FFMA2, 0.5 issue
-// slots per weight).  A warp covers 1024 k of CPW columns per step; the lane
-// partial sums are combined by a transposing shuffle reduction (log2(32)
-// shuffles in total for all CPW*MT values instead of 5 per value).
-//
-// Layout of one tile: 8 warps x CPW columns, k range [kc*kchunk, +kchunk).
+// airadar.tv English edition, first paragraph: a single request reads all the
+// target's weights every step), so the kernel is built around HBM:
+//  - stream-K: the work is cut into units of one stage (16 columns x 1024 k)
+//    and every CTA takes the same number of consecutive units; a column tile
+//    cut by a CTA boundary is finished by a deterministic partial-sum fix-up;
+//  - each warp owns 2 of a unit's columns and lane l the 32 weights
+//    k = 32l .. 32l+31: the lane streams its own 16-byte vectors of the three
+//    planes (and its two meta words) with cp.async into private,
+//    lane-interleaved shared-memory slots kStages units ahead, so every load
+//    is coalesced (a warp reads 512 contiguous bytes per plane and column),
+//    the reads back are conflict-free, and a thread only ever waits for its
+//    own copies (cp.async.wait_group: no barrier, no spin);
+//  - the lane rebuilds its 32 bf16 weights in registers (rebuild32, ~1.75 ALU
+//    ops per weight), patches escapes, and multiplies with fma.rn.f32.bf16
+//    straight from the bf16 halves of weights and activations;
+//  - per tile the lane partial sums are combined by a transposing shuffle
+//    reduction.
 #include <cuda_runtime.h>
 
+#include "async_common.cuh"
 #include "gemm_common.cuh"
 
 namespace w12 {
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kCW = 2;                         // columns per warp
+constexpr int kCols = kWarps * kCW;            // columns per unit / tile
+constexpr int kStageK = 1024;                  // k per unit
+constexpr int kRows = 3 * kCW + 1;             // per warp and slot: 6 plane rows + 1 meta row
+constexpr int kRowBytes = 32 * 16;             // one 16-byte chunk per lane
 
-__device__ __forceinline__ float2 unpack_bf16x2(uint32_t p) {
-    return make_float2(__uint_as_float(p << 16), __uint_as_float(p & 0xFFFF0000u));
-}
+template <int MT>
+struct GemvCfg {
+    static constexpr int kStages = MT == 1 ? 4 : 3;
+    static constexpr int kMinBlocks = MT == 4 ? 1 : 2;
+    static constexpr int kSmem = kWarps * kStages * kRows * kRowBytes;
+};
 
 __device__ __forceinline__ uint32_t word_of(const uint4 &v, int c) {
     return c == 0 ? v.x : c == 1 ? v.y : c == 2 ? v.z : v.w;
@@ -57,147 +75,183 @@ __device__ __forceinline__ void transpose_reduce(float (&v)[NV], int lane) {
 
 template <int NV>
 struct Log2 {
-    static constexpr int value = NV <= 1 ? 0 : 1 + Log2<NV / 2>::value;
+    static constexpr int value = 1 + Log2<NV / 2>::value;
 };
 template <>
 struct Log2<1> {
     static constexpr int value = 0;
 };
 
-template <int CPW, int MT>
-__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemmArgs a) {
+template <int MT>
+__global__ void __launch_bounds__(kThreads, GemvCfg<MT>::kMinBlocks) gemv_kernel(const GemmArgs a) {
+    constexpr int S = GemvCfg<MT>::kStages;
+    extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int s_last;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int64_t t0, t1;
-    tile_range(a.T, t0, t1);
-    for (int64_t t = t0; t < t1; ++t) {
-        const int64_t kc = t / a.NB, nb = t % a.NB;
-        const int64_t kbeg = kc * a.kchunk;
-        const int64_t kend = min(a.K, kbeg + a.kchunk);
-        const int64_t col0 = nb * a.cols_per_tile + int64_t(warp) * CPW;
+    const uint32_t my = smem_addr(smem) + uint32_t(warp * S * kRows * kRowBytes + lane * 16);
+    const uint64_t pol = l2_evict_first_policy();
+    int64_t u0, u1;
+    tile_range(a.T, u0, u1);
 
-        float2 acc[CPW][MT];
+    // Start the copies of unit u into slot s (this lane's chunks only).
+    auto issue = [&](int64_t u, int s) {
+        const int64_t nb = u / a.steps, kl = (u % a.steps) * kStageK + 32 * lane;
+        if (kl >= a.K) return;
+        const uint32_t slot = my + uint32_t(s * kRows * kRowBytes);
 #pragma unroll
-        for (int j = 0; j < CPW; ++j)
+        for (int j = 0; j < kCW; ++j) {
+            const int64_t n = nb * kCols + warp * kCW + j;
+            if (n < a.N) {
+                const int64_t wo = n * a.KW + (kl >> 3);
+                cp_async16_stream(slot + (3 * j + 0) * kRowBytes, a.H + wo, pol);
+                cp_async16_stream(slot + (3 * j + 1) * kRowBytes, a.L + wo, pol);
+                cp_async16_stream(slot + (3 * j + 2) * kRowBytes, a.E + wo, pol);
+                const int64_t g = n * a.KG + (kl >> 7);
+                cp_async4(slot + 6 * kRowBytes + 8 * j, a.meta + g);
+                cp_async4(slot + 6 * kRowBytes + 8 * j + 4, a.meta + g + 1);
+            }
+        }
+    };
+    // This lane's 32 activations of unit u for every token (zeros past K or M).
+    auto load_x = [&](int64_t u, uint4 (&xv)[MT][4]) {
+        const int64_t kl = (u % a.steps) * kStageK + 32 * lane;
 #pragma unroll
-            for (int m = 0; m < MT; ++m) acc[j][m] = make_float2(0.f, 0.f);
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                xv[m][q] = (kl < a.K && m < a.M) ? ldg_v4(a.x + int64_t(m) * a.K + kl + 8 * q)
+                                                 : make_uint4(0u, 0u, 0u, 0u);
+    };
 
-        for (int64_t k0 = kbeg; k0 < kend; k0 += 1024) {
-            const int64_t kl = k0 + int64_t(lane) * 32;
-            if (kl < kend) {
-                // issue every load of the step before any arithmetic
-                uint4 h[CPW], l[CPW], e[CPW];
-                uint32_t m0[CPW], m1[CPW];
 #pragma unroll
-                for (int j = 0; j < CPW; ++j) {
-                    const int64_t n = col0 + j;
-                    if (n < a.N) {
-                        const int64_t wo = n * a.KW + (kl >> 3);
-                        h[j] = ldg_stream(a.H + wo);
-                        l[j] = ldg_stream(a.L + wo);
-                        e[j] = ldg_stream(a.E + wo);
-                        const int64_t g = n * a.KG + (kl >> 7);
-                        m0[j] = ldg_u32(a.meta + g);
-                        m1[j] = ldg_u32(a.meta + g + 1);
-                    }
-                }
-                uint4 xv[MT][4];
+    for (int i = 0; i < S - 1; ++i) {
+        if (u0 + i < u1) issue(u0 + i, i);
+        cp_async_commit();
+    }
+    uint4 xnext[MT][4];
+    if (u0 < u1) load_x(u0, xnext);
+
+    uint32_t it = 0;
+    for (int64_t u = u0; u < u1;) {
+        const int64_t nb = u / a.steps, first = nb * a.steps;
+        const int64_t ua = u, ub = min(u1, first + a.steps);
+        const int64_t col0 = nb * kCols;
+
+        float acc[kCW][MT][2];
 #pragma unroll
-                for (int m = 0; m < MT; ++m) {
+        for (int j = 0; j < kCW; ++j)
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        xv[m][q] = (m < a.M) ? ldg_v4(a.x + int64_t(m) * a.K + kl + 8 * q)
-                                             : make_uint4(0u, 0u, 0u, 0u);
-                    }
-                }
-                // MT == 1: widen x once per step and reuse it for all CPW columns;
-                // MT > 1: widen at the point of use to keep register pressure down.
-                float2 xf[MT == 1 ? 16 : 1];
-                if (MT == 1) {
+            for (int m = 0; m < MT; ++m) acc[j][m][0] = acc[j][m][1] = 0.f;
+
+        for (; u < ub; ++u, ++it) {
+            if (u + S - 1 < u1) issue(u + S - 1, int((it + S - 1) % S));
+            cp_async_commit();
+            cp_async_wait<S - 1>();  // this lane's copies of unit u have landed
+            uint4 xv[MT][4];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) xf[MT == 1 ? i : 0] = unpack_bf16x2(word_of(xv[0][i >> 2], i & 3));
-                }
+            for (int m = 0; m < MT; ++m)
 #pragma unroll
-                for (int j = 0; j < CPW; ++j) {
-                    if (col0 + j < a.N) {
+                for (int q = 0; q < 4; ++q) xv[m][q] = xnext[m][q];
+            if (u + 1 < u1) load_x(u + 1, xnext);
+
+            const int64_t kl = (u - first) * kStageK + 32 * lane;
+            if (kl < a.K) {
+                const uint32_t slot = my + uint32_t((it % S) * kRows * kRowBytes);
+#pragma unroll
+                for (int j = 0; j < kCW; ++j) {
+                    if (col0 + warp * kCW + j < a.N) {
+                        const uint4 h = lds128(slot + (3 * j + 0) * kRowBytes);
+                        const uint4 l = lds128(slot + (3 * j + 1) * kRowBytes);
+                        const uint4 e = lds128(slot + (3 * j + 2) * kRowBytes);
+                        const uint32_t m0 = lds32(slot + 6 * kRowBytes + 8 * j);
+                        const uint32_t m1 = lds32(slot + 6 * kRowBytes + 8 * j + 4);
                         uint32_t w[16];
-                        rebuild32(h[j], l[j], e[j], (m0[j] & 0xFFu) * 0x00800080u, w);
-                        if ((m0[j] >> 8) != (m1[j] >> 8))
-                            patch_escapes(w, m0[j], m1[j], uint32_t(kl & 127), a.esc, a.n_esc,
-                                          a.err);
+                        rebuild32(h, l, e, base4(m0), w);
+                        if ((m0 >> 8) != (m1 >> 8))
+                            patch_escapes(w, m0, m1, uint32_t(32 * (lane & 3)), a.esc, a.n_esc, a.err);
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            const float2 wf = unpack_bf16x2(w[i]);
 #pragma unroll
-                            for (int m = 0; m < MT; ++m) {
-                                const float2 xi = (MT == 1) ? xf[MT == 1 ? i : 0]
-                                                            : unpack_bf16x2(word_of(xv[m][i >> 2], i & 3));
-                                acc[j][m] = __ffma2_rn(wf, xi, acc[j][m]);
-                            }
+                            for (int m = 0; m < MT; ++m)
+                                fma_bf16x2(acc[j][m][0], acc[j][m][1], w[i], word_of(xv[m][i >> 2], i & 3));
                         }
                     }
                 }
             }
         }
 
-        constexpr int NV = CPW * MT;
+        constexpr int NV = kCW * MT;
         float v[NV];
 #pragma unroll
-        for (int j = 0; j < CPW; ++j)
+        for (int j = 0; j < kCW; ++j)
 #pragma unroll
-            for (int m = 0; m < MT; ++m) v[j * MT + m] = acc[j][m].x + acc[j][m].y;
+            for (int m = 0; m < MT; ++m) v[j * MT + m] = acc[j][m][0] + acc[j][m][1];
         transpose_reduce<NV>(v, lane);
         constexpr int kShift = 5 - Log2<NV>::value;
+        const bool whole = (ua == first) && (ub == first + a.steps);
         if ((lane & ((1 << kShift) - 1)) == 0) {
             const int vi = lane >> kShift;
             const int j = vi / MT, m = vi % MT;
-            const int64_t n = col0 + j;
-            if (n < a.N && m < a.M) emit(a, kc, m, n, v[0]);
+            const int c = warp * kCW + j;
+            if (col0 + c < a.N && m < a.M) {
+                if (whole)
+                    store_y(a, m, col0 + c, v[0]);
+                else
+                    a.partial[(ua * a.M + m) * kCols + c] = v[0];
+            }
         }
-        finish_tile(a, nb, &s_last);
+        if (!whole) streamk_fixup(a, nb, ub - ua, &s_last, threadIdx.x, kThreads);
     }
+    cp_async_wait<0>();
 }
 
-template <int CPW, int MT>
+template <int MT>
+int prepare_t() {
+    return cudaFuncSetAttribute(gemv_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                GemvCfg<MT>::kSmem) == cudaSuccess
+               ? W12_OK
+               : W12_ERR_CUDA;
+}
+
+template <int MT>
 int launch_t(const GemmPlan &p, const GemmArgs &a, cudaStream_t s) {
-    gemv_kernel<CPW, MT><<<unsigned(p.grid), kThreads, 0, s>>>(a);
+    if (prepare_t<MT>() != W12_OK) return W12_ERR_CUDA;
+    gemv_kernel<MT><<<unsigned(p.grid), kThreads, GemvCfg<MT>::kSmem, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? W12_OK : W12_ERR_CUDA;
 }
 
-template <int CPW, int MT>
+template <int MT>
 int occ_t(int *blocks) {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, gemv_kernel<CPW, MT>, kThreads, 0) ==
-                   cudaSuccess
+    if (prepare_t<MT>() != W12_OK) return W12_ERR_CUDA;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, gemv_kernel<MT>, kThreads,
+                                                         GemvCfg<MT>::kSmem) == cudaSuccess
                ? W12_OK
                : W12_ERR_CUDA;
 }
 
 }  // namespace
 
-// variant -> (columns per warp, tokens); the set the planner chooses from.
-#define W12_GEMV_VARIANTS(X) X(0, 1, 1) X(1, 2, 1) X(2, 4, 1) X(3, 1, 2) X(4, 2, 2) X(5, 1, 4)
-
+// variant = log2(MT): tokens 1, 2, 4.
 int launch_gemv(const GemmPlan &p, const GemmArgs &a, void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     switch (p.variant) {
-#define X(id, cpw, mt) \
-    case id:           \
-        return launch_t<cpw, mt>(p, a, s);
-        W12_GEMV_VARIANTS(X)
-#undef X
+        case 0: return launch_t<1>(p, a, s);
+        case 1: return launch_t<2>(p, a, s);
+        case 2: return launch_t<4>(p, a, s);
     }
     return W12_ERR_ARG;
 }
 
 int gemv_occupancy(int variant, int *blocks) {
     switch (variant) {
-#define X(id, cpw, mt) \
-    case id:           \
-        return occ_t<cpw, mt>(blocks);
-        W12_GEMV_VARIANTS(X)
-#undef X
+        case 0: return occ_t<1>(blocks);
+        case 1: return occ_t<2>(blocks);
+        case 2: return occ_t<4>(blocks);
     }
     return W12_ERR_ARG;
 }
+
+int gemv_cols_per_tile() { return kCols; }
+int gemv_stage_k() { return kStageK; }
 
 }  // namespace w12

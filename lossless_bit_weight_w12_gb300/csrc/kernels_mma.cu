@@ -138,8 +138,8 @@ __global__ void __launch_bounds__(kThreads, NT >= 8 ? 1 : 2) mma_kernel(const Ge
             for (int64_t k = xb; k < xe; k += 128) {
                 if (k + 128 < kend) load_a(a, nrow0, k + 128, t, nxt);
                 uint32_t wa[16], wb[16];
-                rebuild32(cur.h[0], cur.l[0], cur.e[0], (cur.m0[0] & 0xFFu) * 0x00800080u, wa);
-                rebuild32(cur.h[1], cur.l[1], cur.e[1], (cur.m0[1] & 0xFFu) * 0x00800080u, wb);
+                rebuild32(cur.h[0], cur.l[0], cur.e[0], base4(cur.m0[0]), wa);
+                rebuild32(cur.h[1], cur.l[1], cur.e[1], base4(cur.m0[1]), wb);
                 if ((cur.m0[0] >> 8) != (cur.m1[0] >> 8))
                     patch_escapes(wa, cur.m0[0], cur.m1[0], uint32_t(32 * t), a.esc, a.n_esc, a.err);
                 if ((cur.m0[1] >> 8) != (cur.m1[1] >> 8))
@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, NT >= 8 ? 1 : 2) mma_kernel(const Ge
                     if (n < a.N && m < a.M) emit(a, kc, m, n, acc[j][q]);
                 }
             }
-            finish_tile(a, nb, &s_last);
+            finish_tile(a, nb, &s_last, threadIdx.x, kThreads);
         }
     }
     if (FUSED) {

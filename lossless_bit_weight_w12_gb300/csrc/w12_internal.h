@@ -10,7 +10,7 @@
 namespace w12 {
 
 constexpr int kGroup = 128;        // weights per group along k
-constexpr int kMaxBase = 241;      // 241 + 14 = 255
+constexpr int kMaxBase = 240;      // 240 + 15 = 255: b + code never leaves a byte
 constexpr uint32_t kMaxEscapes = 1u << 24;
 
 inline uint64_t round256(uint64_t x) { return (x + 255u) & ~uint64_t(255); }
@@ -42,6 +42,9 @@ struct GemmArgs {
     int64_t kchunk;             // k per split (multiple of 128)
     int64_t T;                  // NB * nks tiles
     int64_t xchunk;             // k staged in shared memory at a time (MMA path)
+    // stream-K (GEMV path): U units of one stage each, `steps` units per tile;
+    // partial[((nb * steps + ks) * M + m) * cols_per_tile + c] zero between calls
+    int64_t U, steps;
     // fused argmax + acceptance epilogue (lm_head verify); row_best NULL otherwise
     unsigned long long *row_best;  // [grid][M] per-CTA best keys
     float *logits_out;             // optional [M][N] copy of the fp32 logits
@@ -58,6 +61,7 @@ struct GemmPlan {
     int64_t NB, cols_per_tile;
     int nks;
     int64_t kchunk, xchunk;
+    int64_t U, steps;  // stream-K (GEMV): units and units per tile
     size_t ws_bytes;
     // workspace offsets (bytes from the workspace start)
     size_t off_counters, off_partial, off_best, off_gbuf;
@@ -71,6 +75,8 @@ int launch_decode(const w12_desc *d, const void *blob, uint16_t *w, int layout, 
 int launch_gemv(const GemmPlan &p, const GemmArgs &a, void *stream);
 int launch_mma(const GemmPlan &p, const GemmArgs &a, void *stream);
 int gemv_occupancy(int variant, int *blocks_per_sm);
+int gemv_cols_per_tile();
+int gemv_stage_k();
 int mma_occupancy(int variant, size_t smem, int *blocks_per_sm);
 int device_sm_count(int *sms);
 

@@ -83,6 +83,12 @@ def test_gemm_one_hot_is_exact(dev, w12mod, M):
     x = np.zeros((M, K), dtype=np.uint16)
     x[np.arange(M), ks] = 0x3F80
     want = bf16_bits_to_f64(w[:, ks].T)  # [M, N]
+    # IEEE: the zero terms still turn an Inf or NaN weight elsewhere in the column into NaN
+    nonfinite = ~np.isfinite(bf16_bits_to_f64(w))  # [N, K]
+    for m, k in enumerate(ks):
+        other = nonfinite.copy()
+        other[:, k] = False
+        want[m, other.any(axis=1)] = np.nan
     for path in _paths(M):
         y = _run(w12mod, dev, d, blob_d, x, path)
         nan = np.isnan(want)
@@ -94,9 +100,9 @@ def test_gemm_nonfinite(dev, w12mod, oracle):
     K, N, M = 512, 40, 3
     rng = synth.streams(9, 2)
     w = synth.weights(rng[0], K, N)
-    w[10, 3] = 0x7F80  # +Inf
-    w[200, 7] = 0x7FC0  # NaN
-    w[300, 9] = 0xFF80  # -Inf
+    w[3, 10] = 0x7F80  # +Inf   (w is [N, K])
+    w[7, 200] = 0x7FC0  # NaN
+    w[9, 300] = 0xFF80  # -Inf
     x = synth.activations(rng[1], M, K)
     x[:, :] = np.where(x == 0, 0x3F80, x)  # no zero activations (0 * Inf = NaN)
     d, blob = w12mod.encode(w, w12mod.LAYOUT_NK)

@@ -69,7 +69,7 @@ def test_validate_catches_corruption(w12):
     d, blob = w12.encode(w, w12.LAYOUT_NK)
     assert d.n_esc > 0
     bad = blob.copy()
-    bad[d.off_meta] = 250  # base of group 0 above 241
+    bad[d.off_meta] = 250  # base of group 0 above 240
     assert w12.validate(d, bad) == w12.ERR_BLOB
     bad = blob.copy()
     meta = bad[d.off_meta:d.off_meta + 4 * (d.G + 1)].view(np.uint32)
