@@ -4,6 +4,9 @@
 
 #include <algorithm>
 #include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "w12_internal.h"
 
@@ -29,10 +32,46 @@ int check_desc(const w12_desc *d) {
 }
 
 struct Device {
+    int id = 0;
     int sms = 0;
 };
 
-int query_device(Device *dv) { return device_sm_count(&dv->sms); }
+// Per-device facts the planner needs on every call (SM count, occupancy of
+// each kernel variant), queried once: the queries cost microseconds of host
+// time, as much as a small GEMM takes on the device.
+struct DeviceCache {
+    int sms = 0;
+    std::map<std::pair<int, size_t>, int> occ;  // (kernel key, smem) -> CTAs per SM
+};
+std::mutex g_cache_mu;
+std::map<int, DeviceCache> g_cache;
+
+int query_device(Device *dv) {
+    if (cudaGetDevice(&dv->id) != cudaSuccess) return W12_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_cache_mu);
+    DeviceCache &c = g_cache[dv->id];
+    if (c.sms == 0 && device_sm_count(&c.sms) != W12_OK) return W12_ERR_CUDA;
+    dv->sms = c.sms;
+    return W12_OK;
+}
+
+// key: 0..15 GEMV variants, 16.. MMA variants
+int cached_occupancy(const Device &dv, int key, size_t smem, int *blocks) {
+    {
+        std::lock_guard<std::mutex> lock(g_cache_mu);
+        auto &m = g_cache[dv.id].occ;
+        auto it = m.find({key, smem});
+        if (it != m.end()) {
+            *blocks = it->second;
+            return W12_OK;
+        }
+    }
+    const int st = key < 16 ? gemv_occupancy(key, blocks) : mma_occupancy(key - 16, smem, blocks);
+    if (st != W12_OK) return st;
+    std::lock_guard<std::mutex> lock(g_cache_mu);
+    g_cache[dv.id].occ[{key, smem}] = *blocks;
+    return W12_OK;
+}
 
 // Makespan model: tiles are dealt out in contiguous balanced ranges, so the
 // busiest CTA runs ceil(T / grid) tiles of `tile_work` weights each.  A small
@@ -65,7 +104,7 @@ int plan_gemv(const w12_desc *d, int64_t M, const Device &dv, GemmPlan *p) {
     const int variant = M <= 1 ? 0 : M <= 2 ? 1 : 2;
     const int64_t cpt = gemv_cols_per_tile(), sk = gemv_stage_k();
     int occ = 0;
-    if (gemv_occupancy(variant, &occ) != W12_OK) return W12_ERR_CUDA;
+    if (cached_occupancy(dv, variant, 0, &occ) != W12_OK) return W12_ERR_CUDA;
     if (occ < 1) return W12_ERR_CUDA;
     std::memset(p, 0, sizeof *p);
     p->path = W12_PATH_GEMV;
@@ -106,7 +145,7 @@ int plan_mma(const w12_desc *d, int64_t M, const Device &dv, bool fused, GemmPla
         const int64_t kchunk = cg * kGroup;
         const int64_t xchunk = std::min(kchunk, xmax);
         int occ = 0;
-        if (mma_occupancy(v, size_t(mp * xchunk * 2), &occ) != W12_OK) return W12_ERR_CUDA;
+        if (cached_occupancy(dv, 16 + v, size_t(mp * xchunk * 2), &occ) != W12_OK) return W12_ERR_CUDA;
         if (occ < 1) continue;
         const int64_t grid = int64_t(dv.sms) * occ;
         const int64_t T = NB * eff;

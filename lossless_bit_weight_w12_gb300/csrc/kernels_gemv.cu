@@ -93,14 +93,30 @@ __global__ void __launch_bounds__(kThreads, GemvCfg<MT>::kMinBlocks) gemv_kernel
     int64_t u0, u1;
     tile_range(a.T, u0, u1);
 
-    // Start the copies of unit u into slot s (this lane's chunks only).
-    auto issue = [&](int64_t u, int s) {
-        const int64_t nb = u / a.steps, kl = (u % a.steps) * kStageK + 32 * lane;
+    // Unit u covers column tile u / steps and k = (u % steps) * kStageK.  The
+    // three positions the loop needs (copy issue S-1 units ahead, activation
+    // prefetch one unit ahead, compute) are advanced by increments: no
+    // division inside the loop.
+    struct Pos {
+        int64_t nb, ks;
+        __device__ void next(int64_t steps) {
+            if (++ks == steps) {
+                ks = 0;
+                ++nb;
+            }
+        }
+    };
+    const int64_t steps = a.steps;
+    Pos pc{u0 / steps, u0 % steps};  // compute position
+
+    // Start the copies of the unit at p into slot s (this lane's chunks only).
+    auto issue = [&](const Pos &p, int s) {
+        const int64_t kl = p.ks * kStageK + 32 * lane;
         if (kl >= a.K) return;
         const uint32_t slot = my + uint32_t(s * kRows * kRowBytes);
 #pragma unroll
         for (int j = 0; j < kCW; ++j) {
-            const int64_t n = nb * kCols + warp * kCW + j;
+            const int64_t n = p.nb * kCols + warp * kCW + j;
             if (n < a.N) {
                 const int64_t wo = n * a.KW + (kl >> 3);
                 cp_async16_stream(slot + (3 * j + 0) * kRowBytes, a.H + wo, pol);
@@ -112,9 +128,9 @@ __global__ void __launch_bounds__(kThreads, GemvCfg<MT>::kMinBlocks) gemv_kernel
             }
         }
     };
-    // This lane's 32 activations of unit u for every token (zeros past K or M).
-    auto load_x = [&](int64_t u, uint4 (&xv)[MT][4]) {
-        const int64_t kl = (u % a.steps) * kStageK + 32 * lane;
+    // This lane's 32 activations of the unit at p for every token (zeros past K or M).
+    auto load_x = [&](const Pos &p, uint4 (&xv)[MT][4]) {
+        const int64_t kl = p.ks * kStageK + 32 * lane;
 #pragma unroll
         for (int m = 0; m < MT; ++m)
 #pragma unroll
@@ -123,18 +139,22 @@ __global__ void __launch_bounds__(kThreads, GemvCfg<MT>::kMinBlocks) gemv_kernel
                                                  : make_uint4(0u, 0u, 0u, 0u);
     };
 
+    Pos pi = pc;  // copy-issue position
 #pragma unroll
     for (int i = 0; i < S - 1; ++i) {
-        if (u0 + i < u1) issue(u0 + i, i);
+        if (u0 + i < u1) issue(pi, i);
+        pi.next(steps);
         cp_async_commit();
     }
     uint4 xnext[MT][4];
-    if (u0 < u1) load_x(u0, xnext);
+    Pos px = pc;  // activation prefetch position
+    if (u0 < u1) load_x(px, xnext);
+    px.next(steps);
 
-    uint32_t it = 0;
+    uint32_t it = 0, slot_i = S - 1, slot_c = 0;
     for (int64_t u = u0; u < u1;) {
-        const int64_t nb = u / a.steps, first = nb * a.steps;
-        const int64_t ua = u, ub = min(u1, first + a.steps);
+        const int64_t nb = pc.nb, first = nb * steps;
+        const int64_t ua = u, ub = min(u1, first + steps);
         const int64_t col0 = nb * kCols;
 
         float acc[kCW][MT][2];
@@ -144,7 +164,9 @@ __global__ void __launch_bounds__(kThreads, GemvCfg<MT>::kMinBlocks) gemv_kernel
             for (int m = 0; m < MT; ++m) acc[j][m][0] = acc[j][m][1] = 0.f;
 
         for (; u < ub; ++u, ++it) {
-            if (u + S - 1 < u1) issue(u + S - 1, int((it + S - 1) % S));
+            if (u + S - 1 < u1) issue(pi, int(slot_i));
+            pi.next(steps);
+            slot_i = (slot_i + 1 == uint32_t(S)) ? 0u : slot_i + 1;
             cp_async_commit();
             cp_async_wait<S - 1>();  // this lane's copies of unit u have landed
             uint4 xv[MT][4];
@@ -152,11 +174,13 @@ __global__ void __launch_bounds__(kThreads, GemvCfg<MT>::kMinBlocks) gemv_kernel
             for (int m = 0; m < MT; ++m)
 #pragma unroll
                 for (int q = 0; q < 4; ++q) xv[m][q] = xnext[m][q];
-            if (u + 1 < u1) load_x(u + 1, xnext);
+            if (u + 1 < u1) load_x(px, xnext);
+            px.next(steps);
 
-            const int64_t kl = (u - first) * kStageK + 32 * lane;
+            const int64_t kl = pc.ks * kStageK + 32 * lane;
+            pc.next(steps);
             if (kl < a.K) {
-                const uint32_t slot = my + uint32_t((it % S) * kRows * kRowBytes);
+                const uint32_t slot = my + slot_c * uint32_t(kRows * kRowBytes);
 #pragma unroll
                 for (int j = 0; j < kCW; ++j) {
                     if (col0 + warp * kCW + j < a.N) {
@@ -178,6 +202,7 @@ __global__ void __launch_bounds__(kThreads, GemvCfg<MT>::kMinBlocks) gemv_kernel
                     }
                 }
             }
+            slot_c = (slot_c + 1 == uint32_t(S)) ? 0u : slot_c + 1;
         }
 
         constexpr int NV = kCW * MT;
@@ -213,9 +238,10 @@ int prepare_t() {
                : W12_ERR_CUDA;
 }
 
+// The dynamic shared-memory limit is raised once per device, by occ_t(),
+// which the planner always runs before the first launch on a device.
 template <int MT>
 int launch_t(const GemmPlan &p, const GemmArgs &a, cudaStream_t s) {
-    if (prepare_t<MT>() != W12_OK) return W12_ERR_CUDA;
     gemv_kernel<MT><<<unsigned(p.grid), kThreads, GemvCfg<MT>::kSmem, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? W12_OK : W12_ERR_CUDA;
 }

@@ -205,12 +205,14 @@ __global__ void __launch_bounds__(kThreads, NT >= 8 ? 1 : 2) mma_kernel(const Ge
     }
 }
 
+constexpr int kMaxXSmem = 64 * 1024;  // the planner keeps MP * xchunk * 2 within this
+
+// The dynamic shared-memory limit is raised once per device, by occ_t(),
+// which the planner always runs before the first launch on a device.
 template <int NT, bool FUSED>
 int launch_t(const GemmPlan &p, const GemmArgs &a, cudaStream_t s) {
     const size_t smem = size_t(NT) * 8 * size_t(a.xchunk) * 2;
-    if (cudaFuncSetAttribute(mma_kernel<NT, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(smem)) != cudaSuccess)
-        return W12_ERR_CUDA;
+    if (smem > size_t(kMaxXSmem)) return W12_ERR_ARG;
     mma_kernel<NT, FUSED><<<unsigned(p.grid), kThreads, smem, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? W12_OK : W12_ERR_CUDA;
 }
@@ -218,7 +220,9 @@ int launch_t(const GemmPlan &p, const GemmArgs &a, cudaStream_t s) {
 template <int NT>
 int occ_t(int *blocks, size_t smem) {
     if (cudaFuncSetAttribute(mma_kernel<NT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(smem)) != cudaSuccess)
+                             kMaxXSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(mma_kernel<NT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kMaxXSmem) != cudaSuccess)
         return W12_ERR_CUDA;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, mma_kernel<NT, false>, kThreads,
                                                          smem) == cudaSuccess
