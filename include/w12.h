@@ -219,6 +219,42 @@ int w12_verify_greedy_lmhead(const uint16_t *hidden_dev, const w12_desc *d_lm,
                              size_t ws_bytes, void *stream);
 
 /*
+ * Scratch memory that w12_verify_greedy_noalloc() keeps, once, on every GPU
+ * that loads this library (held until the process exits).
+ */
+#define W12_NOALLOC_SCRATCH_BYTES (256u * 1024u)
+
+/*
+ * w12_verify_greedy() for callers that cannot allocate device memory: a
+ * serving loop whose device memory is planned once and may not grow, a host
+ * framework that owns every device allocation and passes only inputs and
+ * outputs, or a latency-critical path that cannot afford cudaMalloc's
+ * implicit device synchronisation.  The paper has no counterpart: this entry
+ * point exists only for such callers.
+ *
+ * Same arguments and results as w12_verify_greedy() without the workspace:
+ * the scratch (an arrival counter, the per-slice argmax keys and the
+ * per-row tokens) is a fixed W12_NOALLOC_SCRATCH_BYTES array inside the
+ * library.  The call allocates nothing, host or device.
+ *  - Size limit: a call needs 512 + 8 * R*T * splits + 4 * R*T bytes (each
+ *    term rounded up to 256), with splits = max(1, ceil(4 * SMs / (R*T)))
+ *    capped at ceil(V / 1024); beyond W12_NOALLOC_SCRATCH_BYTES (about 20000
+ *    rows of R*T) it returns W12_ERR_WORKSPACE and launches nothing.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current) and caches it; make
+ *    that first call before any stream capture begins.
+ *  - Every call on a device shares the one array, which keeps the previous
+ *    call's contents; each call clears what has to start at zero.  Calls
+ *    that may overlap on the GPU (different streams without ordering, or
+ *    several host threads) race on the array and give wrong results:
+ *    order them.
+ * Errors: as w12_verify_greedy, plus W12_ERR_WORKSPACE for the size limit.
+ */
+int w12_verify_greedy_noalloc(const void *logits_dev, int dtype, int64_t R, int64_t T, int64_t V,
+                              const int32_t *draft_dev, int32_t *accept_len_dev,
+                              int32_t *next_tok_dev, void *stream);
+
+/*
  * Read (and clear) the sticky device error word of a workspace: waits for
  * `stream`, copies word 0 to *err_host, then zeroes it.  Returns W12_OK or
  * W12_ERR_CUDA.  *err_host is W12_OK or W12_ERR_DEVICE.

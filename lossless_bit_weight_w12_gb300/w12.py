@@ -30,7 +30,7 @@ EXPORTS = (
     "w12_status_string", "w12_version", "w12_encode_plan", "w12_encode", "w12_validate",
     "w12_decode", "w12_gemm_workspace_size", "w12_gemm", "w12_gemm_ex",
     "w12_verify_workspace_size", "w12_verify_greedy", "w12_verify_lmhead_workspace_size",
-    "w12_verify_greedy_lmhead", "w12_get_device_error",
+    "w12_verify_greedy_lmhead", "w12_get_device_error", "w12_verify_greedy_noalloc",
 )
 
 
@@ -104,6 +104,7 @@ def lib():
         L.w12_verify_lmhead_workspace_size.argtypes = [D, I64, I64]
         L.w12_verify_greedy_lmhead.argtypes = [P, D, P, I64, I64, P, P, P, P, P, SZ, P]
         L.w12_get_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_int), P]
+        L.w12_verify_greedy_noalloc.argtypes = [P, I, I64, I64, I64, P, P, P, P]
         _lib = L
     return _lib
 
@@ -227,6 +228,18 @@ def verify_greedy_lmhead(hidden_dev, d: Desc, blob_dev, R: int, T: int, draft_de
                                           _dptr(next_dev), _dptr(logits_out_dev), _dptr(ws_dev),
                                           ws_dev.numel() * ws_dev.element_size(),
                                           _stream(stream)), "w12_verify_greedy_lmhead")
+
+
+def verify_greedy_noalloc(logits_dev, R: int, T: int, draft_dev, accept_dev, next_dev,
+                          stream=None):
+    """verify_greedy() on the library's own fixed scratch array: for callers
+    that cannot allocate device memory (see include/w12.h)."""
+    import torch
+    dtype = F32 if logits_dev.dtype == torch.float32 else BF16
+    V = logits_dev.shape[-1]
+    _check(lib().w12_verify_greedy_noalloc(_dptr(logits_dev), dtype, R, T, V, _dptr(draft_dev),
+                                           _dptr(accept_dev), _dptr(next_dev), _stream(stream)),
+           "w12_verify_greedy_noalloc")
 
 
 def get_device_error(ws_dev, stream=None) -> int:
