@@ -21,7 +21,6 @@ import os
 import statistics
 import subprocess
 import sys
-import tempfile
 import time
 
 import numpy as np
@@ -67,40 +66,47 @@ class ClockSampler:
         self.path = None
 
     def start(self):
+        import threading
+        self.lines = []
         try:
-            fd, self.path = tempfile.mkstemp(suffix=".csv")
-            os.close(fd)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200", "-f", self.path],
-                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
+            return
+
+        def pump():
+            for line in self.proc.stdout:
+                self.lines.append(line)
+        self.thread = threading.Thread(target=pump, daemon=True)
+        self.thread.start()
 
     def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
+        self.thread.join(timeout=5)
         sm, smax, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        with open(self.path) as f:
-            for line in f:
-                c = [x.strip() for x in line.split(",")]
-                if len(c) < 9:
-                    continue
-                try:
-                    sm.append(float(c[1]))
-                    smax = float(c[2])
-                except ValueError:
-                    continue
-                for nm, v in zip(names, c[5:9]):
-                    if v.lower() == "active":
-                        reasons.add(nm)
-        os.unlink(self.path)
+        for line in self.lines:
+            c = [x.strip() for x in line.split(",")]
+            if len(c) < 9:
+                continue
+            try:
+                sm.append(float(c[1]))
+                smax = float(c[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, c[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
                 "reasons": sorted(reasons), "samples": len(sm)}
 
@@ -133,16 +139,16 @@ def make_bufs(w12, dev, layer, M):
     return ys, wss
 
 
-def run_step(w12, layer, xs, ys, wss, events=None):
+def run_step(w12, layer, xs, ys, wss, mark=None):
     for i, g in enumerate(layer):
-        if events is not None:
-            events[i][0].record()
+        done = mark(g["name"]) if mark is not None else None
         w12.gemm(g["desc"], g["blob"], xs[i], ys[i], wss[i])
-        if events is not None:
-            events[i][1].record()
+        if done is not None:
+            done()
 
 
 def time_steps(torch, fn, steps, barrier):
+    """Eager timing: K calls of fn between two events on the current stream."""
     start = torch.cuda.Event(enable_timing=True)
     stop = torch.cuda.Event(enable_timing=True)
     barrier()
@@ -154,6 +160,67 @@ def time_steps(torch, fn, steps, barrier):
     torch.cuda.synchronize()
     barrier()
     return start.elapsed_time(stop) / 1000.0  # seconds
+
+
+def _timing_event(torch):
+    """An event whose record becomes a node of a captured CUDA graph."""
+    try:
+        return torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:  # older torch: no external events
+        return None
+
+
+class GraphSteps:
+    """`steps` repetitions of a step captured into one CUDA graph, with an
+    event record node before and after every launch the step makes through
+    `mark` (when the installed torch supports external events).  Replaying
+    the graph once is one timed region of `steps` steps."""
+
+    def __init__(self, torch, step, steps):
+        self.torch = torch
+        self.marks = []  # per step: list of (name, start event, end event)
+        self.ok_events = _timing_event(torch) is not None
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            step(lambda name: None)  # one eager pass on the capture stream (plans, attributes)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=s):
+            for _ in range(steps):
+                marks = []
+
+                def mark(name, marks=marks):
+                    if not self.ok_events:
+                        return lambda: None
+                    a, b = _timing_event(torch), _timing_event(torch)
+                    a.record()
+                    marks.append((name, a, b))
+                    return b.record
+                step(mark)
+                self.marks.append(marks)
+
+    def run(self, barrier):
+        torch = self.torch
+        start = torch.cuda.Event(enable_timing=True)
+        stop = torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        start.record()
+        self.graph.replay()
+        stop.record()
+        torch.cuda.synchronize()
+        barrier()
+        return start.elapsed_time(stop) / 1000.0
+
+    def per_launch(self):
+        """Mean duration (s) of each marked launch over the replayed steps."""
+        out = {}
+        for marks in self.marks:
+            for name, a, b in marks:
+                out.setdefault(name, []).append(a.elapsed_time(b) / 1000.0)
+        return {k: statistics.mean(v) for k, v in out.items()}
 
 
 def kernel_hash():
@@ -278,21 +345,15 @@ def run_w12(args):
     x1 = xs[1]
     nbytes = _layer_bytes()
 
-    for _ in range(args.warmup):
-        run_step(w12, layer, x1, ys, wss)
-    torch.cuda.synchronize()
-
-    # ---- timed region: K steps, per-GEMM events for the roofline
-    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in layer]
-          for _ in range(args.steps)]
+    # ---- timed region: K steps in one CUDA graph, an event pair per GEMM
+    gsteps = GraphSteps(torch, lambda mark: run_step(w12, layer, x1, ys, wss, mark), args.steps)
+    gwarm = GraphSteps(torch, lambda mark: run_step(w12, layer, x1, ys, wss), args.warmup)
+    gwarm.run(barrier)
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
-    it = iter(ev)
-    dt = time_steps(torch, lambda: run_step(w12, layer, x1, ys, wss, next(it)), args.steps, barrier)
+    dt = gsteps.run(barrier)
     clk = clocks.stop()
-    per_gemm = {g["name"]: statistics.mean(ev[s][i][0].elapsed_time(ev[s][i][1])
-                                           for s in range(args.steps)) / 1000.0
-                for i, g in enumerate(layer)}
+    per_gemm = gsteps.per_launch()
     if world > 1:
         t = torch.tensor([dt], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -321,13 +382,13 @@ def run_w12(args):
     sweep = {}
     for M in sweep_ms:
         ysM, wsM = make_bufs(w12, dev, layer, M)
-        for _ in range(3):
-            run_step(w12, layer, xs[M], ysM, wsM)
         n = max(3, args.steps // 2)
-        t = time_steps(torch, lambda: run_step(w12, layer, xs[M], ysM, wsM), n, barrier)
+        gM = GraphSteps(torch, lambda mark: run_step(w12, layer, xs[M], ysM, wsM), n)
+        gM.run(barrier)
+        t = gM.run(barrier)
         sweep[str(M)] = {"gbs": nbytes * n / t / 1e9, "us_per_layer": 1e6 * t / n,
                          "frac_of_peak": nbytes * n / t / 1e9 / hbm_peak}
-        del ysM, wsM
+        del ysM, wsM, gM
 
     # ---- cuBLAS BF16 GEMM on the same shapes (the 16-bit weight stream)
     bf16_rows = {}
@@ -336,13 +397,14 @@ def run_w12(args):
                for g in layer]
         xb = [x.view(torch.bfloat16) for x in xs[M]]
 
-        def bf16_step():
+        def bf16_step(mark=None):
             for i in range(len(layer)):
                 torch.nn.functional.linear(xb[i], wts[i])
-        for _ in range(3):
-            bf16_step()
         n = max(3, args.steps // 2)
-        t = time_steps(torch, bf16_step, n, barrier)
+        gb = GraphSteps(torch, bf16_step, n)
+        gb.run(barrier)
+        t = gb.run(barrier)
+        del gb
         bf16_rows[str(M)] = {"us_per_layer": 1e6 * t / n,
                              "bf16_gbs": sum(2.0 * g["K"] * g["N"] for g in layer) * n / t / 1e9,
                              "w12_speedup": (t / n) / (dt / args.steps)}
@@ -355,10 +417,11 @@ def run_w12(args):
 
     # ---- roofline of the dominant kernel
     g = next(g for g in layer if g["name"] == DOMINANT)
-    t_dom = per_gemm[DOMINANT]
-    achieved = synth.weight_bytes_w12(g["K"], g["N"]) / t_dom / 1e9
+    t_dom = per_gemm.get(DOMINANT)
+    achieved = synth.weight_bytes_w12(g["K"], g["N"]) / t_dom / 1e9 if t_dom else None
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                "frac": achieved / hbm_peak, "traffic": traffic_for("gemv_gate_up_m1"),
+                "frac": achieved / hbm_peak if achieved else None,
+                "traffic": traffic_for("gemv_gate_up_m1"),
                 "kernel": f"gemv_kernel ({DOMINANT}, K={g['K']}, N={g['N']}, M=1)",
                 "peak_kind": f"{peak_kind} hbm_gbs (copy)",
                 "algorithmic_bytes_per_launch": synth.weight_bytes_w12(g["K"], g["N"])}
@@ -382,6 +445,7 @@ def run_w12(args):
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "frac_of_peak": value / world / hbm_peak,
         "per_gemm_us": {k: 1e6 * v for k, v in per_gemm.items()},
+        "timing": "K steps replayed from one CUDA graph; per-GEMM times from event nodes in it",
         "e2e": {"value": world * nbytes * args.steps / dt_e2e / 1e9, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": len(layer) * args.steps,
@@ -412,14 +476,37 @@ def bench_lmhead(w12, torch, dev, args, barrier):
     nxt = torch.empty(R, dtype=torch.int32, device=dev)
     ws = w12.workspace(w12.verify_lmhead_workspace_size(d, R, T), dev)
 
-    def step():
+    def step(mark=None):
         w12.verify_greedy_lmhead(hidden, d, blob_d, R, T, draft, acc, nxt, ws)
-    for _ in range(3):
-        step()
     n = max(5, args.steps)
-    t = time_steps(torch, step, n, barrier)
+    gl = GraphSteps(torch, step, n)
+    gl.run(barrier)
+    t = gl.run(barrier)
     b = synth.weight_bytes_w12(K, N)
     return {"us": 1e6 * t / n, "gbs": b * n / t / 1e9, "R": R, "T": T, "N": N, "K": K}
+
+
+def run_kernel_only(args):
+    """One layer GEMM (by name) at M = args.m, eager launches: the case the
+    ncu captures under profiles/ are taken on."""
+    import torch
+    from lossless_bit_weight_w12_gb300 import build_lib, w12
+    build_lib.build()
+    dev = torch.device("cuda", 0)
+    i, (name, K, N) = next((i, t) for i, t in enumerate(synth.LAYER_SHAPES) if t[0] == args.kernel_only)
+    rng = synth.streams(1, len(synth.LAYER_SHAPES) + 8)
+    d, blob = w12.encode(synth.weights(rng[i], K, N), w12.LAYOUT_NK)
+    blob_d = w12.upload(blob, dev)
+    xr = synth.streams(1000 + args.m, len(synth.LAYER_SHAPES))
+    x = torch.from_numpy(synth.activations(xr[i], args.m, K).view(np.int16)).to(dev)
+    y = torch.empty((args.m, N), dtype=torch.float32, device=dev)
+    ws = w12.workspace(w12.gemm_workspace_size(d, args.m), dev)
+    for _ in range(args.warmup):
+        w12.gemm(d, blob_d, x, y, ws)
+    t = time_steps(torch, lambda: w12.gemm(d, blob_d, x, y, ws), args.steps, lambda: None)
+    print(json.dumps({"kernel_only": name, "K": K, "N": N, "M": args.m,
+                      "us": 1e6 * t / args.steps,
+                      "gbs": synth.weight_bytes_w12(K, N) * args.steps / t / 1e9}))
 
 
 def main():
@@ -430,10 +517,14 @@ def main():
     ap.add_argument("--impl", default="w12", choices=["w12", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-verify", dest="verify", action="store_false")
+    ap.add_argument("--kernel-only", default=None, help="time one layer GEMM by name (for ncu)")
+    ap.add_argument("--m", type=int, default=1, help="tokens for --kernel-only")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.kernel_only:
+        run_kernel_only(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_w12(args)
