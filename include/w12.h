@@ -179,6 +179,28 @@ int w12_gemm_ex(const w12_desc *d, const void *blob_dev, const uint16_t *x_dev, 
                 void *y_dev, int y_dtype, void *ws_dev, size_t ws_bytes, int path,
                 void *stream);
 
+#define W12_MAX_BATCH 8
+
+/* Bytes of workspace w12_gemm_batched needs for these matrices and M (0 on
+ * invalid arguments). */
+size_t w12_gemm_batched_workspace_size(const w12_desc *descs, int count, int64_t M);
+
+/*
+ * count independent products y_i = x_i . W_i (1 <= count <= W12_MAX_BATCH,
+ * every K_i, N_i > 0) with one M, e.g. the linears of a decoder layer.  With
+ * M <= 4 all of them run in ONE launch of the GEMV kernel: its work units of
+ * all products are split evenly over the GPU, so small products (a layer's
+ * k and v) neither run alone on a part of the SMs nor pay their own launch
+ * and tail.  With larger M the products run one after the other on the
+ * tensor-core path.  descs, blobs_dev, x_dev, y_dev are host arrays of count
+ * entries (device pointers in the last three), with the layouts and
+ * alignments of w12_gemm.  Errors: as w12_gemm; W12_ERR_SHAPE for an empty
+ * product.
+ */
+int w12_gemm_batched(const w12_desc *descs, const void *const *blobs_dev,
+                     const uint16_t *const *x_dev, int64_t M, void *const *y_dev, int y_dtype,
+                     int count, void *ws_dev, size_t ws_bytes, void *stream);
+
 /* Bytes of workspace w12_verify_greedy needs (>= 256). */
 size_t w12_verify_workspace_size(int64_t R, int64_t T, int64_t V);
 

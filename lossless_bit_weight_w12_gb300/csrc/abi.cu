@@ -316,6 +316,130 @@ extern "C" int w12_gemm(const w12_desc *d, const void *blob, const uint16_t *x, 
     return w12_gemm_ex(d, blob, x, M, y, y_dtype, ws, ws_bytes, W12_PATH_AUTO, stream);
 }
 
+namespace w12 {
+namespace {
+
+// Workspace layout of a batch: header, then per product its counters and
+// partial slots (GEMV path) or its own w12_gemm workspace (tensor-core path).
+struct BatchPlan {
+    bool gemv = false;
+    int variant = 0, grid = 0;
+    int64_t U = 0;
+    size_t off[kMaxBatch] = {}, bytes[kMaxBatch] = {}, counters[kMaxBatch] = {}, partial[kMaxBatch] = {};
+    int64_t steps[kMaxBatch] = {}, NB[kMaxBatch] = {}, ubase[kMaxBatch] = {};
+    size_t total = 0;
+};
+
+int plan_batch(const w12_desc *d, int count, int64_t M, BatchPlan *bp) {
+    if (!d || count < 1 || count > kMaxBatch || M < 1 || M > W12_MAX_M) return W12_ERR_ARG;
+    for (int i = 0; i < count; ++i) {
+        const int st = check_desc(&d[i]);
+        if (st != W12_OK) return st;
+    }
+    size_t off = kWsHeader;
+    bp->gemv = M <= 4;
+    if (bp->gemv) {
+        Device dv;
+        if (query_device(&dv) != W12_OK) return W12_ERR_CUDA;
+        bp->variant = M <= 1 ? 0 : M <= 2 ? 1 : 2;
+        int occ = 0;
+        if (cached_occupancy(dv, bp->variant, 0, &occ) != W12_OK || occ < 1) return W12_ERR_CUDA;
+        const int64_t cpt = gemv_cols_per_tile(), sk = gemv_stage_k();
+        for (int i = 0; i < count; ++i) {
+            bp->steps[i] = ceil_div(d[i].K, sk);
+            bp->NB[i] = ceil_div(d[i].N, cpt);
+            bp->ubase[i] = bp->U;
+            bp->U += bp->steps[i] * bp->NB[i];
+            bp->counters[i] = off;
+            off += round256(4u * uint64_t(std::max<int64_t>(bp->NB[i], 1)));
+            bp->partial[i] = off;
+            off += round256(uint64_t(bp->steps[i] * bp->NB[i]) * uint64_t(M) * uint64_t(cpt) * 4u);
+        }
+        bp->grid = int(std::min<int64_t>(int64_t(dv.sms) * occ, std::max<int64_t>(bp->U, 1)));
+    } else {
+        for (int i = 0; i < count; ++i) {
+            GemmPlan p;
+            const int st = choose_plan(&d[i], M, W12_PATH_MMA, false, &p);
+            if (st != W12_OK) return st;
+            bp->off[i] = off;
+            bp->bytes[i] = p.ws_bytes;
+            off += round256(p.ws_bytes);
+        }
+    }
+    bp->total = off;
+    return W12_OK;
+}
+
+}  // namespace
+}  // namespace w12
+
+extern "C" size_t w12_gemm_batched_workspace_size(const w12_desc *d, int count, int64_t M) {
+    BatchPlan bp;
+    return plan_batch(d, count, M, &bp) == W12_OK ? bp.total : 0;
+}
+
+extern "C" int w12_gemm_batched(const w12_desc *d, const void *const *blobs, const uint16_t *const *xs,
+                                int64_t M, void *const *ys, int y_dtype, int count, void *ws,
+                                size_t ws_bytes, void *stream) {
+    if (!blobs || !xs || !ys) return W12_ERR_ARG;
+    if (y_dtype != W12_F32 && y_dtype != W12_BF16) return W12_ERR_ARG;
+    BatchPlan bp;
+    int st = plan_batch(d, count, M, &bp);
+    if (st != W12_OK) return st;
+    for (int i = 0; i < count; ++i) {
+        if (d[i].N == 0 || d[i].K == 0) return W12_ERR_SHAPE;  // empty products: use w12_gemm
+        if (!blobs[i] || !xs[i] || !ys[i]) return W12_ERR_ARG;
+        if (!aligned(blobs[i], 256) || !aligned(xs[i], 16) || !aligned(ys[i], y_dtype == W12_F32 ? 4 : 2))
+            return W12_ERR_ALIGN;
+    }
+    if (!ws || ws_bytes < bp.total) return W12_ERR_WORKSPACE;
+    if (!aligned(ws, 256)) return W12_ERR_ALIGN;
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    if (!bp.gemv) {
+        // tensor-core path: the products one after the other, each with its
+        // own part of the workspace (they share the error word at offset 0)
+        for (int i = 0; i < count; ++i) {
+            GemmPlan p;
+            st = choose_plan(&d[i], M, W12_PATH_MMA, false, &p);
+            if (st != W12_OK) return st;
+            GemmArgs a = make_args(&d[i], blobs[i], xs[i], M, ys[i], y_dtype, w + bp.off[i], p);
+            a.err = reinterpret_cast<int *>(w);
+            st = launch_mma(p, a, stream);
+            if (st != W12_OK) return st;
+        }
+        return W12_OK;
+    }
+    GemvBatch b;
+    std::memset(&b, 0, sizeof b);
+    b.count = count;
+    b.M = int(M);
+    b.y_dtype = y_dtype;
+    b.err = reinterpret_cast<int *>(w);
+    b.U = bp.U;
+    for (int i = 0; i < count; ++i) {
+        const uint8_t *bl = static_cast<const uint8_t *>(blobs[i]);
+        GemvOne &g = b.g[i];
+        g.H = reinterpret_cast<const uint32_t *>(bl + d[i].off_h);
+        g.L = reinterpret_cast<const uint32_t *>(bl + d[i].off_l);
+        g.E = reinterpret_cast<const uint32_t *>(bl + d[i].off_e);
+        g.meta = reinterpret_cast<const uint32_t *>(bl + d[i].off_meta);
+        g.esc = reinterpret_cast<const uint16_t *>(bl + d[i].off_esc);
+        g.n_esc = d[i].n_esc;
+        g.K = d[i].K;
+        g.N = d[i].N;
+        g.KW = d[i].K / 8;
+        g.KG = d[i].K / kGroup;
+        g.steps = bp.steps[i];
+        g.NB = bp.NB[i];
+        g.ubase = bp.ubase[i];
+        g.x = xs[i];
+        g.y = ys[i];
+        g.partial = reinterpret_cast<float *>(w + bp.partial[i]);
+        g.counters = reinterpret_cast<uint32_t *>(w + bp.counters[i]);
+    }
+    return launch_gemv_batch(b, bp.variant, bp.grid, stream);
+}
+
 extern "C" size_t w12_verify_workspace_size(int64_t R, int64_t T, int64_t V) {
     if (R < 1 || T < 1 || V < 1 || V >= (int64_t(1) << 31)) return 0;
     int grid;

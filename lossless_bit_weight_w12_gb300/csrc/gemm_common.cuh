@@ -72,6 +72,44 @@ __device__ __forceinline__ void finish_tile(const GemmArgs &a, int64_t nb, int *
     epi_sync(nthreads);  // s_last is reused by the next tile
 }
 
+// Store one output of a batched GEMV (y row-major [M][N], fp32 or bf16).
+__device__ __forceinline__ void store_out(void *y, int y_dtype, int64_t N, int64_t m, int64_t n, float v) {
+    if (y_dtype == W12_F32)
+        static_cast<float *>(y)[m * N + n] = v;
+    else
+        static_cast<__nv_bfloat16 *>(y)[m * N + n] = __float2bfloat16_rn(v);
+}
+
+// Stream-K fix-up on explicit buffers (the batched GEMV): same protocol as
+// streamk_fixup below; slots are partial[((nb * steps + ks) * M + m) * cpt + c].
+__device__ __forceinline__ void streamk_fixup_raw(uint32_t *counters, float *partial, int64_t steps,
+                                                  int M, int64_t N, void *y, int y_dtype, int64_t cpt,
+                                                  int64_t nb, int64_t count, int *s_last, int tid,
+                                                  int nthreads) {
+    __threadfence();
+    epi_sync(nthreads);
+    if (tid == 0) {
+        const uint32_t old = atomicAdd(&counters[nb], uint32_t(count));
+        *s_last = (int64_t(old) + count == steps);
+    }
+    epi_sync(nthreads);
+    if (*s_last) {
+        __threadfence();
+        for (int64_t o = tid; o < cpt * M; o += nthreads) {
+            const int64_t m = o / cpt, c = o % cpt, n = nb * cpt + c;
+            float s = 0.f;
+            for (int64_t ks = 0; ks < steps; ++ks) {
+                float *slot = &partial[((nb * steps + ks) * M + m) * cpt + c];
+                s += __ldcg(slot);
+                *slot = 0.f;
+            }
+            if (n < N) store_out(y, y_dtype, N, m, n, s);
+        }
+        if (tid == 0) counters[nb] = 0u;
+    }
+    epi_sync(nthreads);
+}
+
 // Stream-K fix-up of column tile nb after a CTA covered `count` of its
 // `steps` stages and stored its partial sums in slot (nb, first stage).  The
 // CTA that completes the tile sums the slots in stage order (deterministic),

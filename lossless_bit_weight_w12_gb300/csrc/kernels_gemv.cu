@@ -82,8 +82,34 @@ struct Log2<1> {
     static constexpr int value = 0;
 };
 
+// Unit cursor over the concatenated units of the batch: GEMM gi, column
+// tile nb, k step ks.  Advanced by increments (no division in the loop).
+struct Cur {
+    int gi;
+    int64_t nb, ks;
+};
+
+__device__ __forceinline__ void cur_next(const GemvBatch &b, Cur &c) {
+    if (++c.ks == b.g[c.gi].steps) {
+        c.ks = 0;
+        if (++c.nb == b.g[c.gi].NB) {
+            c.nb = 0;
+            ++c.gi;
+        }
+    }
+}
+
+__device__ __forceinline__ Cur cur_at(const GemvBatch &b, int64_t u) {
+    Cur c{0, 0, 0};
+    while (c.gi + 1 < b.count && u >= b.g[c.gi + 1].ubase) ++c.gi;
+    const int64_t local = u - b.g[c.gi].ubase;
+    c.nb = local / b.g[c.gi].steps;
+    c.ks = local % b.g[c.gi].steps;
+    return c;
+}
+
 template <int MT>
-__global__ void __launch_bounds__(kThreads, GemvCfg<MT>::kMinBlocks) gemv_kernel(const GemmArgs a) {
+__global__ void __launch_bounds__(kThreads, GemvCfg<MT>::kMinBlocks) gemv_kernel(const GemvBatch b) {
     constexpr int S = GemvCfg<MT>::kStages;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int s_last;
@@ -91,70 +117,64 @@ __global__ void __launch_bounds__(kThreads, GemvCfg<MT>::kMinBlocks) gemv_kernel
     const uint32_t my = smem_addr(smem) + uint32_t(warp * S * kRows * kRowBytes + lane * 16);
     const uint64_t pol = l2_evict_first_policy();
     int64_t u0, u1;
-    tile_range(a.T, u0, u1);
+    tile_range(b.U, u0, u1);
+    if (u0 >= u1) return;
+    const int M = b.M;
 
-    // Unit u covers column tile u / steps and k = (u % steps) * kStageK.  The
-    // three positions the loop needs (copy issue S-1 units ahead, activation
-    // prefetch one unit ahead, compute) are advanced by increments: no
-    // division inside the loop.
-    struct Pos {
-        int64_t nb, ks;
-        __device__ void next(int64_t steps) {
-            if (++ks == steps) {
-                ks = 0;
-                ++nb;
-            }
-        }
-    };
-    const int64_t steps = a.steps;
-    Pos pc{u0 / steps, u0 % steps};  // compute position
-
-    // Start the copies of the unit at p into slot s (this lane's chunks only).
-    auto issue = [&](const Pos &p, int s) {
-        const int64_t kl = p.ks * kStageK + 32 * lane;
-        if (kl >= a.K) return;
+    // Start the copies of the unit at c into slot s (this lane's chunks only).
+    auto issue = [&](const Cur &c, int s) {
+        const GemvOne &g = b.g[c.gi];
+        const int64_t kl = c.ks * kStageK + 32 * lane;
+        if (kl >= g.K) return;
         const uint32_t slot = my + uint32_t(s * kRows * kRowBytes);
 #pragma unroll
         for (int j = 0; j < kCW; ++j) {
-            const int64_t n = p.nb * kCols + warp * kCW + j;
-            if (n < a.N) {
-                const int64_t wo = n * a.KW + (kl >> 3);
-                cp_async16_stream(slot + (3 * j + 0) * kRowBytes, a.H + wo, pol);
-                cp_async16_stream(slot + (3 * j + 1) * kRowBytes, a.L + wo, pol);
-                cp_async16_stream(slot + (3 * j + 2) * kRowBytes, a.E + wo, pol);
-                const int64_t g = n * a.KG + (kl >> 7);
-                cp_async4(slot + 6 * kRowBytes + 8 * j, a.meta + g);
-                cp_async4(slot + 6 * kRowBytes + 8 * j + 4, a.meta + g + 1);
+            const int64_t n = c.nb * kCols + warp * kCW + j;
+            if (n < g.N) {
+                const int64_t wo = n * g.KW + (kl >> 3);
+                cp_async16_stream(slot + (3 * j + 0) * kRowBytes, g.H + wo, pol);
+                cp_async16_stream(slot + (3 * j + 1) * kRowBytes, g.L + wo, pol);
+                cp_async16_stream(slot + (3 * j + 2) * kRowBytes, g.E + wo, pol);
+                const int64_t gg = n * g.KG + (kl >> 7);
+                cp_async4(slot + 6 * kRowBytes + 8 * j, g.meta + gg);
+                cp_async4(slot + 6 * kRowBytes + 8 * j + 4, g.meta + gg + 1);
             }
         }
     };
-    // This lane's 32 activations of the unit at p for every token (zeros past K or M).
-    auto load_x = [&](const Pos &p, uint4 (&xv)[MT][4]) {
-        const int64_t kl = p.ks * kStageK + 32 * lane;
+    // This lane's 32 activations of the unit at c for every token (zeros past K or M).
+    auto load_x = [&](const Cur &c, uint4 (&xv)[MT][4]) {
+        const GemvOne &g = b.g[c.gi];
+        const int64_t kl = c.ks * kStageK + 32 * lane;
 #pragma unroll
         for (int m = 0; m < MT; ++m)
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-                xv[m][q] = (kl < a.K && m < a.M) ? ldg_v4(a.x + int64_t(m) * a.K + kl + 8 * q)
-                                                 : make_uint4(0u, 0u, 0u, 0u);
+                xv[m][q] = (kl < g.K && m < M) ? ldg_v4(g.x + int64_t(m) * g.K + kl + 8 * q)
+                                               : make_uint4(0u, 0u, 0u, 0u);
     };
 
-    Pos pi = pc;  // copy-issue position
+    const Cur c0 = cur_at(b, u0);
+    Cur ci = c0;  // copy-issue cursor
 #pragma unroll
     for (int i = 0; i < S - 1; ++i) {
-        if (u0 + i < u1) issue(pi, i);
-        pi.next(steps);
+        if (u0 + i < u1) {
+            issue(ci, i);
+            cur_next(b, ci);
+        }
         cp_async_commit();
     }
+    Cur cx = c0;  // activation prefetch cursor
     uint4 xnext[MT][4];
-    Pos px = pc;  // activation prefetch position
-    if (u0 < u1) load_x(px, xnext);
-    px.next(steps);
+    load_x(cx, xnext);
+    cur_next(b, cx);
 
-    uint32_t it = 0, slot_i = S - 1, slot_c = 0;
+    Cur cc = c0;  // compute cursor
+    uint32_t slot_i = S - 1, slot_c = 0;
     for (int64_t u = u0; u < u1;) {
-        const int64_t nb = pc.nb, first = nb * steps;
-        const int64_t ua = u, ub = min(u1, first + steps);
+        const int gi = cc.gi;
+        const GemvOne &g = b.g[gi];
+        const int64_t nb = cc.nb, first = g.ubase + nb * g.steps;
+        const int64_t ua = u, ub = min(u1, first + g.steps);
         const int64_t col0 = nb * kCols;
 
         float acc[kCW][MT][2];
@@ -163,9 +183,11 @@ __global__ void __launch_bounds__(kThreads, GemvCfg<MT>::kMinBlocks) gemv_kernel
 #pragma unroll
             for (int m = 0; m < MT; ++m) acc[j][m][0] = acc[j][m][1] = 0.f;
 
-        for (; u < ub; ++u, ++it) {
-            if (u + S - 1 < u1) issue(pi, int(slot_i));
-            pi.next(steps);
+        for (; u < ub; ++u) {
+            if (u + S - 1 < u1) {
+                issue(ci, int(slot_i));
+                cur_next(b, ci);
+            }
             slot_i = (slot_i + 1 == uint32_t(S)) ? 0u : slot_i + 1;
             cp_async_commit();
             cp_async_wait<S - 1>();  // this lane's copies of unit u have landed
@@ -174,16 +196,18 @@ __global__ void __launch_bounds__(kThreads, GemvCfg<MT>::kMinBlocks) gemv_kernel
             for (int m = 0; m < MT; ++m)
 #pragma unroll
                 for (int q = 0; q < 4; ++q) xv[m][q] = xnext[m][q];
-            if (u + 1 < u1) load_x(px, xnext);
-            px.next(steps);
+            if (u + 1 < u1) {
+                load_x(cx, xnext);
+                cur_next(b, cx);
+            }
 
-            const int64_t kl = pc.ks * kStageK + 32 * lane;
-            pc.next(steps);
-            if (kl < a.K) {
+            const int64_t kl = cc.ks * kStageK + 32 * lane;
+            cur_next(b, cc);
+            if (kl < g.K) {
                 const uint32_t slot = my + slot_c * uint32_t(kRows * kRowBytes);
 #pragma unroll
                 for (int j = 0; j < kCW; ++j) {
-                    if (col0 + warp * kCW + j < a.N) {
+                    if (col0 + warp * kCW + j < g.N) {
                         const uint4 h = lds128(slot + (3 * j + 0) * kRowBytes);
                         const uint4 l = lds128(slot + (3 * j + 1) * kRowBytes);
                         const uint4 e = lds128(slot + (3 * j + 2) * kRowBytes);
@@ -192,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, GemvCfg<MT>::kMinBlocks) gemv_kernel
                         uint32_t w[16];
                         rebuild32(h, l, e, base4(m0), w);
                         if ((m0 >> 8) != (m1 >> 8))
-                            patch_escapes(w, m0, m1, uint32_t(32 * (lane & 3)), a.esc, a.n_esc, a.err);
+                            patch_escapes(w, m0, m1, uint32_t(32 * (lane & 3)), g.esc, g.n_esc, b.err);
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
 #pragma unroll
@@ -213,19 +237,21 @@ __global__ void __launch_bounds__(kThreads, GemvCfg<MT>::kMinBlocks) gemv_kernel
             for (int m = 0; m < MT; ++m) v[j * MT + m] = acc[j][m][0] + acc[j][m][1];
         transpose_reduce<NV>(v, lane);
         constexpr int kShift = 5 - Log2<NV>::value;
-        const bool whole = (ua == first) && (ub == first + a.steps);
+        const bool whole = (ua == first) && (ub == first + g.steps);
         if ((lane & ((1 << kShift) - 1)) == 0) {
             const int vi = lane >> kShift;
             const int j = vi / MT, m = vi % MT;
             const int c = warp * kCW + j;
-            if (col0 + c < a.N && m < a.M) {
+            if (col0 + c < g.N && m < M) {
                 if (whole)
-                    store_y(a, m, col0 + c, v[0]);
+                    store_out(g.y, b.y_dtype, g.N, m, col0 + c, v[0]);
                 else
-                    a.partial[(ua * a.M + m) * kCols + c] = v[0];
+                    g.partial[((ua - g.ubase) * M + m) * kCols + c] = v[0];
             }
         }
-        if (!whole) streamk_fixup(a, nb, ub - ua, &s_last, threadIdx.x, kThreads);
+        if (!whole)
+            streamk_fixup_raw(g.counters, g.partial, g.steps, M, g.N, g.y, b.y_dtype, kCols, nb,
+                              ub - ua, &s_last, threadIdx.x, kThreads);
     }
     cp_async_wait<0>();
 }
@@ -241,8 +267,8 @@ int prepare_t() {
 // The dynamic shared-memory limit is raised once per device, by occ_t(),
 // which the planner always runs before the first launch on a device.
 template <int MT>
-int launch_t(const GemmPlan &p, const GemmArgs &a, cudaStream_t s) {
-    gemv_kernel<MT><<<unsigned(p.grid), kThreads, GemvCfg<MT>::kSmem, s>>>(a);
+int launch_t(const GemvBatch &b, int grid, cudaStream_t s) {
+    gemv_kernel<MT><<<unsigned(grid), kThreads, GemvCfg<MT>::kSmem, s>>>(b);
     return cudaGetLastError() == cudaSuccess ? W12_OK : W12_ERR_CUDA;
 }
 
@@ -258,14 +284,43 @@ int occ_t(int *blocks) {
 }  // namespace
 
 // variant = log2(MT): tokens 1, 2, 4.
-int launch_gemv(const GemmPlan &p, const GemmArgs &a, void *stream) {
+int launch_gemv_batch(const GemvBatch &b, int variant, int grid, void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    switch (p.variant) {
-        case 0: return launch_t<1>(p, a, s);
-        case 1: return launch_t<2>(p, a, s);
-        case 2: return launch_t<4>(p, a, s);
+    switch (variant) {
+        case 0: return launch_t<1>(b, grid, s);
+        case 1: return launch_t<2>(b, grid, s);
+        case 2: return launch_t<4>(b, grid, s);
     }
     return W12_ERR_ARG;
+}
+
+// A single GEMM is a batch of one.
+int launch_gemv(const GemmPlan &p, const GemmArgs &a, void *stream) {
+    GemvBatch b;
+    b.count = 1;
+    b.M = a.M;
+    b.y_dtype = a.y_dtype;
+    b.err = a.err;
+    b.U = p.U;
+    GemvOne &g = b.g[0];
+    g.H = a.H;
+    g.L = a.L;
+    g.E = a.E;
+    g.meta = a.meta;
+    g.esc = a.esc;
+    g.n_esc = a.n_esc;
+    g.K = a.K;
+    g.N = a.N;
+    g.KW = a.KW;
+    g.KG = a.KG;
+    g.steps = p.steps;
+    g.NB = p.NB;
+    g.ubase = 0;
+    g.x = a.x;
+    g.y = a.y;
+    g.partial = a.partial;
+    g.counters = a.counters;
+    return launch_gemv_batch(b, p.variant, p.grid, stream);
 }
 
 int gemv_occupancy(int variant, int *blocks) {

@@ -69,6 +69,28 @@ struct GemmPlan {
 
 int plan_gemm(const w12_desc *d, int64_t M, int path, int fused_argmax, GemmPlan *p);
 
+// Batched GEMV: up to kMaxBatch independent GEMMs with the same M in one
+// launch; stream-K runs over the concatenation of their units.
+constexpr int kMaxBatch = W12_MAX_BATCH;
+struct GemvOne {
+    const uint32_t *H, *L, *E, *meta;
+    const uint16_t *esc;
+    uint64_t n_esc;
+    int64_t K, N, KW, KG;
+    int64_t steps, NB, ubase;  // units per column tile, column tiles, first unit of this GEMM
+    const uint16_t *x;         // [M][K]
+    void *y;                   // [M][N]
+    float *partial;            // [NB * steps][M][cols] stream-K partial slots
+    uint32_t *counters;        // [NB]
+};
+struct GemvBatch {
+    GemvOne g[kMaxBatch];
+    int count, M, y_dtype;
+    int *err;
+    int64_t U;  // total units
+};
+int launch_gemv_batch(const GemvBatch &b, int variant, int grid, void *stream);
+
 // Launchers (return W12_OK or W12_ERR_CUDA).
 int launch_decode(const w12_desc *d, const void *blob, uint16_t *w, int layout, int *err,
                   void *stream);

@@ -31,6 +31,7 @@ EXPORTS = (
     "w12_decode", "w12_gemm_workspace_size", "w12_gemm", "w12_gemm_ex",
     "w12_verify_workspace_size", "w12_verify_greedy", "w12_verify_lmhead_workspace_size",
     "w12_verify_greedy_lmhead", "w12_get_device_error", "w12_verify_greedy_noalloc",
+    "w12_gemm_batched_workspace_size", "w12_gemm_batched",
 )
 
 
@@ -105,6 +106,9 @@ def lib():
         L.w12_verify_greedy_lmhead.argtypes = [P, D, P, I64, I64, P, P, P, P, P, SZ, P]
         L.w12_get_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_int), P]
         L.w12_verify_greedy_noalloc.argtypes = [P, I, I64, I64, I64, P, P, P, P]
+        L.w12_gemm_batched_workspace_size.restype = SZ
+        L.w12_gemm_batched_workspace_size.argtypes = [D, I, I64]
+        L.w12_gemm_batched.argtypes = [D, P, P, I64, P, I, I, P, SZ, P]
         _lib = L
     return _lib
 
@@ -198,6 +202,46 @@ def gemm(d: Desc, blob_dev, x_dev, y_dev, ws_dev, path: int = PATH_AUTO, stream=
     _check(lib().w12_gemm_ex(ctypes.byref(c), _dptr(blob_dev), _dptr(x_dev), M, _dptr(y_dev),
                              y_dtype, _dptr(ws_dev), ws_dev.numel() * ws_dev.element_size(),
                              path, _stream(stream)), "w12_gemm")
+
+
+def _desc_array(descs):
+    arr = (_CDesc * len(descs))()
+    for i, d in enumerate(descs):
+        arr[i] = d.c()
+    return arr
+
+
+def gemm_batched_workspace_size(descs, M: int) -> int:
+    return int(lib().w12_gemm_batched_workspace_size(_desc_array(descs), len(descs), M))
+
+
+class GemmBatch:
+    """Marshalled arguments of one w12_gemm_batched call (built once, reused:
+    the pointer arrays stay valid while the tensors live)."""
+
+    def __init__(self, descs, blobs, xs, ys, ws):
+        import torch
+        n = len(descs)
+        self.descs = _desc_array(descs)
+        self.blobs = (ctypes.c_void_p * n)(*[t.data_ptr() for t in blobs])
+        self.xs = (ctypes.c_void_p * n)(*[t.data_ptr() for t in xs])
+        self.ys = (ctypes.c_void_p * n)(*[t.data_ptr() for t in ys])
+        self.M = xs[0].shape[0]
+        self.y_dtype = F32 if ys[0].dtype == torch.float32 else BF16
+        self.count = n
+        self.ws = ws
+        self._keep = (blobs, xs, ys, ws)
+
+    def __call__(self, stream=None):
+        _check(lib().w12_gemm_batched(self.descs, self.blobs, self.xs, self.M, self.ys,
+                                      self.y_dtype, self.count, _dptr(self.ws),
+                                      self.ws.numel() * self.ws.element_size(), _stream(stream)),
+               "w12_gemm_batched")
+
+
+def gemm_batched(descs, blobs, xs, ys, ws, stream=None):
+    """ys[i] = xs[i] @ W_i for every i, one launch when M <= 4."""
+    GemmBatch(descs, blobs, xs, ys, ws)(stream)
 
 
 def verify_workspace_size(R: int, T: int, V: int) -> int:

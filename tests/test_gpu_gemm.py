@@ -190,3 +190,71 @@ def test_gemm_k_zero_writes_zeros(dev, w12mod):
     ws = w12mod.workspace(256, dev)
     w12mod.gemm(d, w12mod.workspace(256, dev), x, y, ws)
     assert torch.count_nonzero(y).item() == 0
+
+
+def _batched(w12mod, dev, items, M, y_dtype="f32"):
+    """items: list of (desc, blob_dev, x uint16 [M,K]); returns list of fp64 y."""
+    import torch
+    xs = [to_dev_bits(x, dev) for _, _, x in items]
+    ys = [torch.empty((M, d.N), dtype=torch.float32 if y_dtype == "f32" else torch.bfloat16, device=dev)
+          for d, _, _ in items]
+    descs = [d for d, _, _ in items]
+    ws = w12mod.workspace(w12mod.gemm_batched_workspace_size(descs, M), dev)
+    w12mod.gemm_batched(descs, [b for _, b, _ in items], xs, ys, ws)
+    torch.cuda.synchronize()
+    assert w12mod.get_device_error(ws) == 0
+    if y_dtype == "f32":
+        return [y.cpu().numpy().astype(np.float64) for y in ys]
+    return [bf16_bits_to_f64(dev_bits_to_np(y)) for y in ys]
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 16])
+def test_gemm_batched_mixed_shapes(dev, w12mod, oracle, M):
+    """One launch over products of different K and N (ragged tiles and unit
+    counts), each checked against the oracle."""
+    shapes = [(384, 33), (1024, 130), (128, 7), (1152, 257), (2048, 16)]
+    rng = synth.streams(4000 + M, 2 * len(shapes))
+    items, refs = [], []
+    for i, (K, N) in enumerate(shapes):
+        w = synth.weights(rng[2 * i], K, N)
+        x = synth.activations(rng[2 * i + 1], M, K)
+        d, blob = w12mod.encode(w, w12mod.LAYOUT_NK)
+        items.append((d, w12mod.upload(blob, dev), x))
+        refs.append(oracle.gemm(*oracle.encode(w, oracle.LAYOUT_NK), x))
+    for rep in range(2):  # the workspace is reused by the second call
+        ys = _batched(w12mod, dev, items, M)
+        for (K, N), y, (y_ref, s_ref) in zip(shapes, ys, refs):
+            check_gemm(y, y_ref, s_ref, what=f"batched K={K} N={N} M={M}")
+
+
+@pytest.mark.parametrize("M", [1, 4])
+def test_gemm_batched_full_layer(dev, w12mod, oracle, M):
+    """The layer's six linears in one launch, full size, sampled columns."""
+    rng = synth.streams(1, len(synth.LAYER_SHAPES) + 8)
+    items, ws_ = [], []
+    for i, (name, K, N) in enumerate(synth.LAYER_SHAPES):
+        w = synth.weights(rng[i], K, N)
+        x = synth.activations(rng[len(synth.LAYER_SHAPES) + i], M, K)
+        d, blob = w12mod.encode(w, w12mod.LAYOUT_NK)
+        items.append((d, w12mod.upload(blob, dev), x))
+        ws_.append(w)
+    ys = _batched(w12mod, dev, items, M)
+    for i, (name, K, N) in enumerate(synth.LAYER_SHAPES):
+        ns = np.unique(np.r_[np.random.default_rng(i).integers(0, N, 20), [0, N - 1]])
+        y_ref, s_ref = oracle.gemm(*oracle.encode(ws_[i][ns], oracle.LAYOUT_NK), items[i][2])
+        check_gemm(ys[i][:, ns], y_ref, s_ref, what=f"batched {name} M={M}")
+
+
+def test_gemm_batched_argument_errors(dev, w12mod):
+    import torch
+    w = np.full((16, 256), 0x3F80, dtype=np.uint16)
+    d, blob = w12mod.encode(w, w12mod.LAYOUT_NK)
+    b = w12mod.upload(blob, dev)
+    x = torch.zeros((1, 256), dtype=torch.int16, device=dev)
+    y = torch.empty((1, 16), dtype=torch.float32, device=dev)
+    assert w12mod.gemm_batched_workspace_size([d] * 9, 1) == 0  # more than W12_MAX_BATCH
+    need = w12mod.gemm_batched_workspace_size([d, d], 1)
+    with pytest.raises(w12mod.W12Error) as e:
+        w12mod.gemm_batched([d, d], [b, b], [x, x], [y, y], w12mod.workspace(256, dev)[:64])
+    assert e.value.status == w12mod.ERR_WORKSPACE
+    w12mod.gemm_batched([d, d], [b, b], [x, x], [y, y], w12mod.workspace(need, dev))
