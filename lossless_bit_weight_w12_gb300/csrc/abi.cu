@@ -100,7 +100,14 @@ void finish_ws_layout(GemmPlan *p, int64_t M, int64_t N, bool fused) {
 
 // GEMV: stream-K over units of one stage (gemv_cols_per_tile() columns x
 // gemv_stage_k() k); every CTA gets the same number of units.
+// The GEMV kernel's index arithmetic is 32-bit.
+bool gemv_fits_32bit(const w12_desc *d) {
+    const int64_t lim = int64_t(1) << 31;
+    return d->K < lim && d->N < lim && d->K / 8 * d->N < lim && d->G < lim;
+}
+
 int plan_gemv(const w12_desc *d, int64_t M, const Device &dv, GemmPlan *p) {
+    if (!gemv_fits_32bit(d)) return W12_ERR_SHAPE;
     const int variant = M <= 1 ? 0 : M <= 2 ? 1 : 2;
     const int64_t cpt = gemv_cols_per_tile(), sk = gemv_stage_k();
     int occ = 0;
@@ -112,6 +119,7 @@ int plan_gemv(const w12_desc *d, int64_t M, const Device &dv, GemmPlan *p) {
     p->steps = ceil_div(d->K, sk);
     p->NB = ceil_div(d->N, cpt);
     p->U = p->NB * p->steps;
+    if (p->U >= (int64_t(1) << 31)) return W12_ERR_SHAPE;
     p->grid = int(std::min<int64_t>(int64_t(dv.sms) * occ, p->U));
     p->cols_per_tile = cpt;
     p->nks = 1;
@@ -346,6 +354,7 @@ int plan_batch(const w12_desc *d, int count, int64_t M, BatchPlan *bp) {
         if (cached_occupancy(dv, bp->variant, 0, &occ) != W12_OK || occ < 1) return W12_ERR_CUDA;
         const int64_t cpt = gemv_cols_per_tile(), sk = gemv_stage_k();
         for (int i = 0; i < count; ++i) {
+            if (!gemv_fits_32bit(&d[i])) return W12_ERR_SHAPE;
             bp->steps[i] = ceil_div(d[i].K, sk);
             bp->NB[i] = ceil_div(d[i].N, cpt);
             bp->ubase[i] = bp->U;
@@ -355,6 +364,7 @@ int plan_batch(const w12_desc *d, int count, int64_t M, BatchPlan *bp) {
             bp->partial[i] = off;
             off += round256(uint64_t(bp->steps[i] * bp->NB[i]) * uint64_t(M) * uint64_t(cpt) * 4u);
         }
+        if (bp->U >= (int64_t(1) << 31)) return W12_ERR_SHAPE;
         bp->grid = int(std::min<int64_t>(int64_t(dv.sms) * occ, std::max<int64_t>(bp->U, 1)));
     } else {
         for (int i = 0; i < count; ++i) {
@@ -415,7 +425,7 @@ extern "C" int w12_gemm_batched(const w12_desc *d, const void *const *blobs, con
     b.M = int(M);
     b.y_dtype = y_dtype;
     b.err = reinterpret_cast<int *>(w);
-    b.U = bp.U;
+    b.U = int32_t(bp.U);
     for (int i = 0; i < count; ++i) {
         const uint8_t *bl = static_cast<const uint8_t *>(blobs[i]);
         GemvOne &g = b.g[i];
@@ -424,14 +434,14 @@ extern "C" int w12_gemm_batched(const w12_desc *d, const void *const *blobs, con
         g.E = reinterpret_cast<const uint32_t *>(bl + d[i].off_e);
         g.meta = reinterpret_cast<const uint32_t *>(bl + d[i].off_meta);
         g.esc = reinterpret_cast<const uint16_t *>(bl + d[i].off_esc);
-        g.n_esc = d[i].n_esc;
-        g.K = d[i].K;
-        g.N = d[i].N;
-        g.KW = d[i].K / 8;
-        g.KG = d[i].K / kGroup;
-        g.steps = bp.steps[i];
-        g.NB = bp.NB[i];
-        g.ubase = bp.ubase[i];
+        g.n_esc = uint32_t(d[i].n_esc);
+        g.K = int32_t(d[i].K);
+        g.N = int32_t(d[i].N);
+        g.KW = int32_t(d[i].K / 8);
+        g.KG = int32_t(d[i].K / kGroup);
+        g.steps = int32_t(bp.steps[i]);
+        g.NB = int32_t(bp.NB[i]);
+        g.ubase = int32_t(bp.ubase[i]);
         g.x = xs[i];
         g.y = ys[i];
         g.partial = reinterpret_cast<float *>(w + bp.partial[i]);

@@ -39,7 +39,7 @@ constexpr int kRowBytes = 32 * 16;             // one 16-byte chunk per lane
 template <int MT>
 struct GemvCfg {
     static constexpr int kStages = MT == 1 ? 4 : 3;
-    static constexpr int kMinBlocks = MT == 4 ? 1 : 2;
+    static constexpr int kMinBlocks = MT == 1 ? 2 : 1;
     static constexpr int kSmem = kWarps * kStages * kRows * kRowBytes;
 };
 
@@ -83,10 +83,10 @@ struct Log2<1> {
 };
 
 // Unit cursor over the concatenated units of the batch: GEMM gi, column
-// tile nb, k step ks.  Advanced by increments (no division in the loop).
+// tile nb, k step ks.  Advanced by increments (no division in the loop);
+// all index arithmetic in the loop is 32-bit.
 struct Cur {
-    int gi;
-    int64_t nb, ks;
+    int gi, nb, ks;
 };
 
 __device__ __forceinline__ void cur_next(const GemvBatch &b, Cur &c) {
@@ -99,10 +99,10 @@ __device__ __forceinline__ void cur_next(const GemvBatch &b, Cur &c) {
     }
 }
 
-__device__ __forceinline__ Cur cur_at(const GemvBatch &b, int64_t u) {
+__device__ __forceinline__ Cur cur_at(const GemvBatch &b, int u) {
     Cur c{0, 0, 0};
     while (c.gi + 1 < b.count && u >= b.g[c.gi + 1].ubase) ++c.gi;
-    const int64_t local = u - b.g[c.gi].ubase;
+    const int local = u - b.g[c.gi].ubase;
     c.nb = local / b.g[c.gi].steps;
     c.ks = local % b.g[c.gi].steps;
     return c;
@@ -116,26 +116,31 @@ __global__ void __launch_bounds__(kThreads, GemvCfg<MT>::kMinBlocks) gemv_kernel
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t my = smem_addr(smem) + uint32_t(warp * S * kRows * kRowBytes + lane * 16);
     const uint64_t pol = l2_evict_first_policy();
-    int64_t u0, u1;
-    tile_range(b.U, u0, u1);
+    int u0, u1;
+    {
+        const int G = int(gridDim.x), c = int(blockIdx.x);
+        const int per = b.U / G, rem = b.U % G;
+        u0 = c * per + (c < rem ? c : rem);
+        u1 = u0 + per + (c < rem ? 1 : 0);
+    }
     if (u0 >= u1) return;
     const int M = b.M;
 
     // Start the copies of the unit at c into slot s (this lane's chunks only).
     auto issue = [&](const Cur &c, int s) {
         const GemvOne &g = b.g[c.gi];
-        const int64_t kl = c.ks * kStageK + 32 * lane;
+        const int kl = c.ks * kStageK + 32 * lane;
         if (kl >= g.K) return;
         const uint32_t slot = my + uint32_t(s * kRows * kRowBytes);
 #pragma unroll
         for (int j = 0; j < kCW; ++j) {
-            const int64_t n = c.nb * kCols + warp * kCW + j;
+            const int n = c.nb * kCols + warp * kCW + j;
             if (n < g.N) {
-                const int64_t wo = n * g.KW + (kl >> 3);
+                const uint32_t wo = uint32_t(n) * uint32_t(g.KW) + uint32_t(kl >> 3);
                 cp_async16_stream(slot + (3 * j + 0) * kRowBytes, g.H + wo, pol);
                 cp_async16_stream(slot + (3 * j + 1) * kRowBytes, g.L + wo, pol);
                 cp_async16_stream(slot + (3 * j + 2) * kRowBytes, g.E + wo, pol);
-                const int64_t gg = n * g.KG + (kl >> 7);
+                const uint32_t gg = uint32_t(n) * uint32_t(g.KG) + uint32_t(kl >> 7);
                 cp_async4(slot + 6 * kRowBytes + 8 * j, g.meta + gg);
                 cp_async4(slot + 6 * kRowBytes + 8 * j + 4, g.meta + gg + 1);
             }
@@ -144,13 +149,14 @@ __global__ void __launch_bounds__(kThreads, GemvCfg<MT>::kMinBlocks) gemv_kernel
     // This lane's 32 activations of the unit at c for every token (zeros past K or M).
     auto load_x = [&](const Cur &c, uint4 (&xv)[MT][4]) {
         const GemvOne &g = b.g[c.gi];
-        const int64_t kl = c.ks * kStageK + 32 * lane;
+        const int kl = c.ks * kStageK + 32 * lane;
 #pragma unroll
         for (int m = 0; m < MT; ++m)
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-                xv[m][q] = (kl < g.K && m < M) ? ldg_v4(g.x + int64_t(m) * g.K + kl + 8 * q)
-                                               : make_uint4(0u, 0u, 0u, 0u);
+                xv[m][q] = (kl < g.K && m < M)
+                               ? ldg_v4(g.x + (uint32_t(m) * uint32_t(g.K) + uint32_t(kl + 8 * q)))
+                               : make_uint4(0u, 0u, 0u, 0u);
     };
 
     const Cur c0 = cur_at(b, u0);
@@ -170,12 +176,12 @@ __global__ void __launch_bounds__(kThreads, GemvCfg<MT>::kMinBlocks) gemv_kernel
 
     Cur cc = c0;  // compute cursor
     uint32_t slot_i = S - 1, slot_c = 0;
-    for (int64_t u = u0; u < u1;) {
+    for (int u = u0; u < u1;) {
         const int gi = cc.gi;
         const GemvOne &g = b.g[gi];
-        const int64_t nb = cc.nb, first = g.ubase + nb * g.steps;
-        const int64_t ua = u, ub = min(u1, first + g.steps);
-        const int64_t col0 = nb * kCols;
+        const int nb = cc.nb, first = g.ubase + nb * g.steps;
+        const int ua = u, ub = min(u1, first + g.steps);
+        const int col0 = nb * kCols;
 
         float acc[kCW][MT][2];
 #pragma unroll
@@ -201,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, GemvCfg<MT>::kMinBlocks) gemv_kernel
                 cur_next(b, cx);
             }
 
-            const int64_t kl = cc.ks * kStageK + 32 * lane;
+            const int kl = cc.ks * kStageK + 32 * lane;
             cur_next(b, cc);
             if (kl < g.K) {
                 const uint32_t slot = my + slot_c * uint32_t(kRows * kRowBytes);
@@ -246,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, GemvCfg<MT>::kMinBlocks) gemv_kernel
                 if (whole)
                     store_out(g.y, b.y_dtype, g.N, m, col0 + c, v[0]);
                 else
-                    g.partial[((ua - g.ubase) * M + m) * kCols + c] = v[0];
+                    g.partial[(uint32_t(ua - g.ubase) * uint32_t(M) + uint32_t(m)) * kCols + c] = v[0];
             }
         }
         if (!whole)
@@ -301,20 +307,20 @@ int launch_gemv(const GemmPlan &p, const GemmArgs &a, void *stream) {
     b.M = a.M;
     b.y_dtype = a.y_dtype;
     b.err = a.err;
-    b.U = p.U;
+    b.U = int32_t(p.U);
     GemvOne &g = b.g[0];
     g.H = a.H;
     g.L = a.L;
     g.E = a.E;
     g.meta = a.meta;
     g.esc = a.esc;
-    g.n_esc = a.n_esc;
-    g.K = a.K;
-    g.N = a.N;
-    g.KW = a.KW;
-    g.KG = a.KG;
-    g.steps = p.steps;
-    g.NB = p.NB;
+    g.n_esc = uint32_t(a.n_esc);
+    g.K = int32_t(a.K);
+    g.N = int32_t(a.N);
+    g.KW = int32_t(a.KW);
+    g.KG = int32_t(a.KG);
+    g.steps = int32_t(p.steps);
+    g.NB = int32_t(p.NB);
     g.ubase = 0;
     g.x = a.x;
     g.y = a.y;

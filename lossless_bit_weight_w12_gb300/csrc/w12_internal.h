@@ -75,9 +75,11 @@ constexpr int kMaxBatch = W12_MAX_BATCH;
 struct GemvOne {
     const uint32_t *H, *L, *E, *meta;
     const uint16_t *esc;
-    uint64_t n_esc;
-    int64_t K, N, KW, KG;
-    int64_t steps, NB, ubase;  // units per column tile, column tiles, first unit of this GEMM
+    uint32_t n_esc;
+    // 32-bit on purpose: the kernel's index arithmetic stays 32-bit (the
+    // planner guarantees K*N/8, G and the unit counts stay below 2^31)
+    int32_t K, N, KW, KG;
+    int32_t steps, NB, ubase;  // units per column tile, column tiles, first unit of this GEMM
     const uint16_t *x;         // [M][K]
     void *y;                   // [M][N]
     float *partial;            // [NB * steps][M][cols] stream-K partial slots
@@ -87,7 +89,7 @@ struct GemvBatch {
     GemvOne g[kMaxBatch];
     int count, M, y_dtype;
     int *err;
-    int64_t U;  // total units
+    int32_t U;  // total units
 };
 int launch_gemv_batch(const GemvBatch &b, int variant, int grid, void *stream);
 
