@@ -126,24 +126,41 @@ __global__ void __launch_bounds__(kThreads, GemvCfg<MT>::kMinBlocks) gemv_kernel
     if (u0 >= u1) return;
     const int M = b.M;
 
-    // Start the copies of the unit at c into slot s (this lane's chunks only).
+    // Start the copies of the unit at c into slot s.  Planes: this lane's
+    // 16-byte chunks.  Meta: when K % 1024 == 0 a column's 9 words (groups
+    // g0..g0+8, g0 a multiple of 8) lie in one aligned 48-byte window (inside
+    // the meta section and its padding), copied as three 16-byte chunks by
+    // three lanes into the warp-shared meta row; otherwise every lane copies
+    // the two words of its own group for each column into its private chunk.
     auto issue = [&](const Cur &c, int s) {
         const GemvOne &g = b.g[c.gi];
-        const int kl = c.ks * kStageK + 32 * lane;
-        if (kl >= g.K) return;
+        const int kst = c.ks * kStageK;
+        const int kl = kst + 32 * lane;
         const uint32_t slot = my + uint32_t(s * kRows * kRowBytes);
+        const bool fast_meta = (g.KG & 7) == 0;
+        if (kl < g.K) {
 #pragma unroll
-        for (int j = 0; j < kCW; ++j) {
-            const int n = c.nb * kCols + warp * kCW + j;
-            if (n < g.N) {
-                const uint32_t wo = uint32_t(n) * uint32_t(g.KW) + uint32_t(kl >> 3);
-                cp_async16_stream(slot + (3 * j + 0) * kRowBytes, g.H + wo, pol);
-                cp_async16_stream(slot + (3 * j + 1) * kRowBytes, g.L + wo, pol);
-                cp_async16_stream(slot + (3 * j + 2) * kRowBytes, g.E + wo, pol);
-                const uint32_t gg = uint32_t(n) * uint32_t(g.KG) + uint32_t(kl >> 7);
-                cp_async4(slot + 6 * kRowBytes + 8 * j, g.meta + gg);
-                cp_async4(slot + 6 * kRowBytes + 8 * j + 4, g.meta + gg + 1);
+            for (int j = 0; j < kCW; ++j) {
+                const int n = c.nb * kCols + warp * kCW + j;
+                if (n < g.N) {
+                    const uint32_t wo = uint32_t(n) * uint32_t(g.KW) + uint32_t(kl >> 3);
+                    cp_async16_stream(slot + (3 * j + 0) * kRowBytes, g.H + wo, pol);
+                    cp_async16_stream(slot + (3 * j + 1) * kRowBytes, g.L + wo, pol);
+                    cp_async16_stream(slot + (3 * j + 2) * kRowBytes, g.E + wo, pol);
+                    if (!fast_meta) {
+                        const uint32_t gg = uint32_t(n) * uint32_t(g.KG) + uint32_t(kl >> 7);
+                        cp_async4(slot + 6 * kRowBytes + 8 * j, g.meta + gg);
+                        cp_async4(slot + 6 * kRowBytes + 8 * j + 4, g.meta + gg + 1);
+                    }
+                }
             }
+        }
+        if (fast_meta && lane < 3 * kCW) {
+            const int j = lane / 3, q = lane % 3;
+            const int n = c.nb * kCols + warp * kCW + j;
+            if (n < g.N)
+                cp_async16(slot - uint32_t(lane * 16) + 6 * kRowBytes + j * 64 + q * 16,
+                           g.meta + (uint32_t(n) * uint32_t(g.KG) + uint32_t(kst >> 7) + 4u * q));
         }
     };
     // This lane's 32 activations of the unit at c for every token (zeros past K or M).
@@ -169,11 +186,6 @@ __global__ void __launch_bounds__(kThreads, GemvCfg<MT>::kMinBlocks) gemv_kernel
         }
         cp_async_commit();
     }
-    Cur cx = c0;  // activation prefetch cursor
-    uint4 xnext[MT][4];
-    load_x(cx, xnext);
-    cur_next(b, cx);
-
     Cur cc = c0;  // compute cursor
     uint32_t slot_i = S - 1, slot_c = 0;
     for (int u = u0; u < u1;) {
@@ -196,17 +208,10 @@ __global__ void __launch_bounds__(kThreads, GemvCfg<MT>::kMinBlocks) gemv_kernel
             }
             slot_i = (slot_i + 1 == uint32_t(S)) ? 0u : slot_i + 1;
             cp_async_commit();
-            cp_async_wait<S - 1>();  // this lane's copies of unit u have landed
+            cp_async_wait<S - 1>();  // this lane's copies of unit u have landed ...
+            __syncwarp();            // ... and so have the meta words other lanes copied
             uint4 xv[MT][4];
-#pragma unroll
-            for (int m = 0; m < MT; ++m)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) xv[m][q] = xnext[m][q];
-            if (u + 1 < u1) {
-                load_x(cx, xnext);
-                cur_next(b, cx);
-            }
-
+            load_x(cc, xv);          // L1-resident: every warp of the CTA reads the same slice
             const int kl = cc.ks * kStageK + 32 * lane;
             cur_next(b, cc);
             if (kl < g.K) {
@@ -217,8 +222,16 @@ __global__ void __launch_bounds__(kThreads, GemvCfg<MT>::kMinBlocks) gemv_kernel
                         const uint4 h = lds128(slot + (3 * j + 0) * kRowBytes);
                         const uint4 l = lds128(slot + (3 * j + 1) * kRowBytes);
                         const uint4 e = lds128(slot + (3 * j + 2) * kRowBytes);
-                        const uint32_t m0 = lds32(slot + 6 * kRowBytes + 8 * j);
-                        const uint32_t m1 = lds32(slot + 6 * kRowBytes + 8 * j + 4);
+                        uint32_t m0, m1;
+                        if ((g.KG & 7) == 0) {  // warp-shared 48-byte windows, g0 % 8 == 0
+                            const uint32_t at = slot - uint32_t(lane * 16) + 6 * kRowBytes + j * 64 +
+                                                uint32_t(lane >> 2) * 4u;
+                            m0 = lds32(at);
+                            m1 = lds32(at + 4);
+                        } else {
+                            m0 = lds32(slot + 6 * kRowBytes + 8 * j);
+                            m1 = lds32(slot + 6 * kRowBytes + 8 * j + 4);
+                        }
                         uint32_t w[16];
                         rebuild32(h, l, e, base4(m0), w);
                         if ((m0 >> 8) != (m1 >> 8))
