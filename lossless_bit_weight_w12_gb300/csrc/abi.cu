@@ -55,7 +55,7 @@ int query_device(Device *dv) {
     return W12_OK;
 }
 
-// key: 0..15 GEMV variants, 16.. MMA variants
+// key: 0..15 GEMV variants, 16..31 split-K MMA variants, 32.. stream-K MMA variants
 int cached_occupancy(const Device &dv, int key, size_t smem, int *blocks) {
     {
         std::lock_guard<std::mutex> lock(g_cache_mu);
@@ -66,7 +66,9 @@ int cached_occupancy(const Device &dv, int key, size_t smem, int *blocks) {
             return W12_OK;
         }
     }
-    const int st = key < 16 ? gemv_occupancy(key, blocks) : mma_occupancy(key - 16, smem, blocks);
+    const int st = key < 16   ? gemv_occupancy(key, blocks)
+                   : key < 32 ? mma_occupancy(key - 16, smem, blocks)
+                              : mma_sk_occupancy(key - 32, smem, blocks);
     if (st != W12_OK) return st;
     std::lock_guard<std::mutex> lock(g_cache_mu);
     g_cache[dv.id].occ[{key, smem}] = *blocks;
@@ -245,6 +247,108 @@ size_t verify_ws(int64_t rows, int64_t splits) {
     return kWsHeader + 256 + round256(uint64_t(rows * splits) * 8u) + round256(uint64_t(rows) * 4u);
 }
 
+
+// Workspace layout of a batch: header (error word), then per product its
+// stream-K counters and partial-sum slots.  Both paths are stream-K: the
+// GEMV (M <= 4, units of 16 columns x 1024 k) and the tensor-core kernel
+// (units of 128 columns x 1024 k).
+struct BatchPlan {
+    bool gemv = false;
+    int variant = 0, grid = 0, xchunk = 0;
+    int64_t U = 0;
+    size_t counters[kMaxBatch] = {}, partial[kMaxBatch] = {};
+    int64_t steps[kMaxBatch] = {}, NB[kMaxBatch] = {}, ubase[kMaxBatch] = {};
+    size_t total = 0;
+};
+
+int plan_batch(const w12_desc *d, int count, int64_t M, int path, BatchPlan *bp) {
+    if (!d || count < 1 || count > kMaxBatch || M < 1 || M > W12_MAX_M) return W12_ERR_ARG;
+    for (int i = 0; i < count; ++i) {
+        const int st = check_desc(&d[i]);
+        if (st != W12_OK) return st;
+        if (!gemv_fits_32bit(&d[i])) return W12_ERR_SHAPE;
+    }
+    if (path == W12_PATH_AUTO) path = M <= 1 ? W12_PATH_GEMV : W12_PATH_MMA;
+    if (path == W12_PATH_GEMV && M > 4) return W12_ERR_SHAPE;
+    if (path != W12_PATH_GEMV && path != W12_PATH_MMA) return W12_ERR_ARG;
+    Device dv;
+    if (query_device(&dv) != W12_OK) return W12_ERR_CUDA;
+    bp->gemv = path == W12_PATH_GEMV;
+    int64_t cpt, uk;
+    int occ = 0;
+    if (bp->gemv) {
+        bp->variant = M <= 1 ? 0 : M <= 2 ? 1 : 2;
+        if (cached_occupancy(dv, bp->variant, 0, &occ) != W12_OK || occ < 1) return W12_ERR_CUDA;
+        cpt = gemv_cols_per_tile();
+        uk = gemv_stage_k();
+    } else {
+        int nt = 1, v = 0;
+        while (nt * 8 < M) {
+            nt *= 2;
+            ++v;
+        }
+        bp->variant = v;
+        const int64_t mp = 8 * nt;
+        bp->xchunk = int(std::min<int64_t>(kMmaUnitK, std::max<int64_t>(1, 32768 / mp / kGroup) * kGroup));
+        if (cached_occupancy(dv, 32 + v, size_t(mp * bp->xchunk * 2), &occ) != W12_OK || occ < 1)
+            return W12_ERR_CUDA;
+        cpt = kMmaCols;
+        uk = kMmaUnitK;
+    }
+    size_t off = kWsHeader;
+    for (int i = 0; i < count; ++i) {
+        bp->steps[i] = ceil_div(d[i].K, uk);
+        bp->NB[i] = ceil_div(d[i].N, cpt);
+        bp->ubase[i] = bp->U;
+        bp->U += bp->steps[i] * bp->NB[i];
+        bp->counters[i] = off;
+        off += round256(4u * uint64_t(std::max<int64_t>(bp->NB[i], 1)));
+        bp->partial[i] = off;
+        off += round256(uint64_t(bp->steps[i] * bp->NB[i]) * uint64_t(M) * uint64_t(cpt) * 4u);
+    }
+    if (bp->U >= (int64_t(1) << 31)) return W12_ERR_SHAPE;
+    bp->grid = int(std::min<int64_t>(int64_t(dv.sms) * occ, std::max<int64_t>(bp->U, 1)));
+    bp->total = off;
+    return W12_OK;
+}
+
+// Launch a planned batch (all K_i, N_i > 0; pointers already checked).
+int run_batch(const w12_desc *d, const void *const *blobs, const uint16_t *const *xs, int64_t M,
+              void *const *ys, int y_dtype, int count, void *ws, const BatchPlan &bp, void *stream) {
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    GemvBatch b;
+    std::memset(&b, 0, sizeof b);
+    b.count = count;
+    b.M = int(M);
+    b.y_dtype = y_dtype;
+    b.err = reinterpret_cast<int *>(w);
+    b.U = int32_t(bp.U);
+    b.xchunk = bp.xchunk;
+    for (int i = 0; i < count; ++i) {
+        const uint8_t *bl = static_cast<const uint8_t *>(blobs[i]);
+        GemvOne &g = b.g[i];
+        g.H = reinterpret_cast<const uint32_t *>(bl + d[i].off_h);
+        g.L = reinterpret_cast<const uint32_t *>(bl + d[i].off_l);
+        g.E = reinterpret_cast<const uint32_t *>(bl + d[i].off_e);
+        g.meta = reinterpret_cast<const uint32_t *>(bl + d[i].off_meta);
+        g.esc = reinterpret_cast<const uint16_t *>(bl + d[i].off_esc);
+        g.n_esc = uint32_t(d[i].n_esc);
+        g.K = int32_t(d[i].K);
+        g.N = int32_t(d[i].N);
+        g.KW = int32_t(d[i].K / 8);
+        g.KG = int32_t(d[i].K / kGroup);
+        g.steps = int32_t(bp.steps[i]);
+        g.NB = int32_t(bp.NB[i]);
+        g.ubase = int32_t(bp.ubase[i]);
+        g.x = xs[i];
+        g.y = ys[i];
+        g.partial = reinterpret_cast<float *>(w + bp.partial[i]);
+        g.counters = reinterpret_cast<uint32_t *>(w + bp.counters[i]);
+    }
+    return bp.gemv ? launch_gemv_batch(b, bp.variant, bp.grid, stream)
+                   : launch_mma_batch(b, bp.variant, bp.grid, stream);
+}
+
 }  // namespace
 
 }  // namespace w12
@@ -282,13 +386,12 @@ extern "C" int w12_decode(const w12_desc *d, const void *blob, uint16_t *w, int 
 
 extern "C" size_t w12_gemm_workspace_size(const w12_desc *d, int64_t M) {
     if (check_desc(d) != W12_OK || M < 1 || M > W12_MAX_M) return 0;
-    GemmPlan p;
-    if (choose_plan(d, M, W12_PATH_AUTO, false, &p) != W12_OK) return 0;
-    // room for any path this M can take, so w12_gemm_ex can switch paths
-    size_t need = p.ws_bytes;
-    GemmPlan q;
-    if (M <= 4 && choose_plan(d, M, W12_PATH_GEMV, false, &q) == W12_OK) need = std::max(need, q.ws_bytes);
-    if (choose_plan(d, M, W12_PATH_MMA, false, &q) == W12_OK) need = std::max(need, q.ws_bytes);
+    // room for either path this M can take, so w12_gemm_ex can switch paths
+    size_t need = 0;
+    BatchPlan bp;
+    if (M <= 4 && plan_batch(d, 1, M, W12_PATH_GEMV, &bp) == W12_OK) need = std::max(need, bp.total);
+    BatchPlan bq;
+    if (plan_batch(d, 1, M, W12_PATH_MMA, &bq) == W12_OK) need = std::max(need, bq.total);
     return need;
 }
 
@@ -310,13 +413,15 @@ extern "C" int w12_gemm_ex(const w12_desc *d, const void *blob, const uint16_t *
     }
     if (!blob || !x) return W12_ERR_ARG;
     if (!aligned(blob, 256) || !aligned(x, 16)) return W12_ERR_ALIGN;
-    GemmPlan p;
-    st = choose_plan(d, M, path, false, &p);
+    BatchPlan bp;
+    st = plan_batch(d, 1, M, path, &bp);
     if (st != W12_OK) return st;
-    if (!ws || ws_bytes < p.ws_bytes) return W12_ERR_WORKSPACE;
+    if (!ws || ws_bytes < bp.total) return W12_ERR_WORKSPACE;
     if (!aligned(ws, 256)) return W12_ERR_ALIGN;
-    const GemmArgs a = make_args(d, blob, x, M, y, y_dtype, ws, p);
-    return launch_plan(p, a, stream);
+    const void *blobs[1] = {blob};
+    const uint16_t *xs[1] = {x};
+    void *ys[1] = {y};
+    return run_batch(d, blobs, xs, M, ys, y_dtype, 1, ws, bp, stream);
 }
 
 extern "C" int w12_gemm(const w12_desc *d, const void *blob, const uint16_t *x, int64_t M, void *y,
@@ -324,68 +429,10 @@ extern "C" int w12_gemm(const w12_desc *d, const void *blob, const uint16_t *x, 
     return w12_gemm_ex(d, blob, x, M, y, y_dtype, ws, ws_bytes, W12_PATH_AUTO, stream);
 }
 
-namespace w12 {
-namespace {
-
-// Workspace layout of a batch: header, then per product its counters and
-// partial slots (GEMV path) or its own w12_gemm workspace (tensor-core path).
-struct BatchPlan {
-    bool gemv = false;
-    int variant = 0, grid = 0;
-    int64_t U = 0;
-    size_t off[kMaxBatch] = {}, bytes[kMaxBatch] = {}, counters[kMaxBatch] = {}, partial[kMaxBatch] = {};
-    int64_t steps[kMaxBatch] = {}, NB[kMaxBatch] = {}, ubase[kMaxBatch] = {};
-    size_t total = 0;
-};
-
-int plan_batch(const w12_desc *d, int count, int64_t M, BatchPlan *bp) {
-    if (!d || count < 1 || count > kMaxBatch || M < 1 || M > W12_MAX_M) return W12_ERR_ARG;
-    for (int i = 0; i < count; ++i) {
-        const int st = check_desc(&d[i]);
-        if (st != W12_OK) return st;
-    }
-    size_t off = kWsHeader;
-    bp->gemv = M <= 4;
-    if (bp->gemv) {
-        Device dv;
-        if (query_device(&dv) != W12_OK) return W12_ERR_CUDA;
-        bp->variant = M <= 1 ? 0 : M <= 2 ? 1 : 2;
-        int occ = 0;
-        if (cached_occupancy(dv, bp->variant, 0, &occ) != W12_OK || occ < 1) return W12_ERR_CUDA;
-        const int64_t cpt = gemv_cols_per_tile(), sk = gemv_stage_k();
-        for (int i = 0; i < count; ++i) {
-            if (!gemv_fits_32bit(&d[i])) return W12_ERR_SHAPE;
-            bp->steps[i] = ceil_div(d[i].K, sk);
-            bp->NB[i] = ceil_div(d[i].N, cpt);
-            bp->ubase[i] = bp->U;
-            bp->U += bp->steps[i] * bp->NB[i];
-            bp->counters[i] = off;
-            off += round256(4u * uint64_t(std::max<int64_t>(bp->NB[i], 1)));
-            bp->partial[i] = off;
-            off += round256(uint64_t(bp->steps[i] * bp->NB[i]) * uint64_t(M) * uint64_t(cpt) * 4u);
-        }
-        if (bp->U >= (int64_t(1) << 31)) return W12_ERR_SHAPE;
-        bp->grid = int(std::min<int64_t>(int64_t(dv.sms) * occ, std::max<int64_t>(bp->U, 1)));
-    } else {
-        for (int i = 0; i < count; ++i) {
-            GemmPlan p;
-            const int st = choose_plan(&d[i], M, W12_PATH_MMA, false, &p);
-            if (st != W12_OK) return st;
-            bp->off[i] = off;
-            bp->bytes[i] = p.ws_bytes;
-            off += round256(p.ws_bytes);
-        }
-    }
-    bp->total = off;
-    return W12_OK;
-}
-
-}  // namespace
-}  // namespace w12
 
 extern "C" size_t w12_gemm_batched_workspace_size(const w12_desc *d, int count, int64_t M) {
     BatchPlan bp;
-    return plan_batch(d, count, M, &bp) == W12_OK ? bp.total : 0;
+    return plan_batch(d, count, M, W12_PATH_AUTO, &bp) == W12_OK ? bp.total : 0;
 }
 
 extern "C" int w12_gemm_batched(const w12_desc *d, const void *const *blobs, const uint16_t *const *xs,
@@ -394,7 +441,7 @@ extern "C" int w12_gemm_batched(const w12_desc *d, const void *const *blobs, con
     if (!blobs || !xs || !ys) return W12_ERR_ARG;
     if (y_dtype != W12_F32 && y_dtype != W12_BF16) return W12_ERR_ARG;
     BatchPlan bp;
-    int st = plan_batch(d, count, M, &bp);
+    int st = plan_batch(d, count, M, W12_PATH_AUTO, &bp);
     if (st != W12_OK) return st;
     for (int i = 0; i < count; ++i) {
         if (d[i].N == 0 || d[i].K == 0) return W12_ERR_SHAPE;  // empty products: use w12_gemm
@@ -404,50 +451,7 @@ extern "C" int w12_gemm_batched(const w12_desc *d, const void *const *blobs, con
     }
     if (!ws || ws_bytes < bp.total) return W12_ERR_WORKSPACE;
     if (!aligned(ws, 256)) return W12_ERR_ALIGN;
-    uint8_t *w = static_cast<uint8_t *>(ws);
-    if (!bp.gemv) {
-        // tensor-core path: the products one after the other, each with its
-        // own part of the workspace (they share the error word at offset 0)
-        for (int i = 0; i < count; ++i) {
-            GemmPlan p;
-            st = choose_plan(&d[i], M, W12_PATH_MMA, false, &p);
-            if (st != W12_OK) return st;
-            GemmArgs a = make_args(&d[i], blobs[i], xs[i], M, ys[i], y_dtype, w + bp.off[i], p);
-            a.err = reinterpret_cast<int *>(w);
-            st = launch_mma(p, a, stream);
-            if (st != W12_OK) return st;
-        }
-        return W12_OK;
-    }
-    GemvBatch b;
-    std::memset(&b, 0, sizeof b);
-    b.count = count;
-    b.M = int(M);
-    b.y_dtype = y_dtype;
-    b.err = reinterpret_cast<int *>(w);
-    b.U = int32_t(bp.U);
-    for (int i = 0; i < count; ++i) {
-        const uint8_t *bl = static_cast<const uint8_t *>(blobs[i]);
-        GemvOne &g = b.g[i];
-        g.H = reinterpret_cast<const uint32_t *>(bl + d[i].off_h);
-        g.L = reinterpret_cast<const uint32_t *>(bl + d[i].off_l);
-        g.E = reinterpret_cast<const uint32_t *>(bl + d[i].off_e);
-        g.meta = reinterpret_cast<const uint32_t *>(bl + d[i].off_meta);
-        g.esc = reinterpret_cast<const uint16_t *>(bl + d[i].off_esc);
-        g.n_esc = uint32_t(d[i].n_esc);
-        g.K = int32_t(d[i].K);
-        g.N = int32_t(d[i].N);
-        g.KW = int32_t(d[i].K / 8);
-        g.KG = int32_t(d[i].K / kGroup);
-        g.steps = int32_t(bp.steps[i]);
-        g.NB = int32_t(bp.NB[i]);
-        g.ubase = int32_t(bp.ubase[i]);
-        g.x = xs[i];
-        g.y = ys[i];
-        g.partial = reinterpret_cast<float *>(w + bp.partial[i]);
-        g.counters = reinterpret_cast<uint32_t *>(w + bp.counters[i]);
-    }
-    return launch_gemv_batch(b, bp.variant, bp.grid, stream);
+    return run_batch(d, blobs, xs, M, ys, y_dtype, count, ws, bp, stream);
 }
 
 extern "C" size_t w12_verify_workspace_size(int64_t R, int64_t T, int64_t V) {

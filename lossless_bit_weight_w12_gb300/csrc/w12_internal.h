@@ -89,9 +89,16 @@ struct GemvBatch {
     GemvOne g[kMaxBatch];
     int count, M, y_dtype;
     int *err;
-    int32_t U;  // total units
+    int32_t U;       // total units
+    int32_t xchunk;  // MMA path: k of x staged in shared memory at a time
 };
 int launch_gemv_batch(const GemvBatch &b, int variant, int grid, void *stream);
+// The same batch description drives the stream-K tensor-core kernel
+// (units of 128 columns x 1024 k; variant = log2(ceil(M/8))).
+int launch_mma_batch(const GemvBatch &b, int variant, int grid, void *stream);
+int mma_sk_occupancy(int variant, size_t smem, int *blocks_per_sm);
+constexpr int kMmaUnitK = 1024;
+constexpr int kMmaCols = 128;
 
 // Launchers (return W12_OK or W12_ERR_CUDA).
 int launch_decode(const w12_desc *d, const void *blob, uint16_t *w, int layout, int *err,
