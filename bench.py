@@ -527,9 +527,9 @@ def run_kernel_only(args):
     y = torch.empty((args.m, N), dtype=torch.float32, device=dev)
     ws = w12.workspace(w12.gemm_workspace_size(d, args.m), dev)
     for _ in range(args.warmup):
-        w12.gemm(d, blob_d, x, y, ws)
-    t = time_steps(torch, lambda: w12.gemm(d, blob_d, x, y, ws), args.steps, lambda: None)
-    print(json.dumps({"kernel_only": name, "K": K, "N": N, "M": args.m,
+        w12.gemm(d, blob_d, x, y, ws, path=args.path)
+    t = time_steps(torch, lambda: w12.gemm(d, blob_d, x, y, ws, path=args.path), args.steps, lambda: None)
+    print(json.dumps({"kernel_only": name, "K": K, "N": N, "M": args.m, "path": args.path,
                       "us": 1e6 * t / args.steps,
                       "gbs": synth.weight_bytes_w12(K, N) * args.steps / t / 1e9}))
 
@@ -544,6 +544,8 @@ def main():
     ap.add_argument("--no-verify", dest="verify", action="store_false")
     ap.add_argument("--kernel-only", default=None, help="time one layer GEMM by name (for ncu)")
     ap.add_argument("--m", type=int, default=1, help="tokens for --kernel-only")
+    ap.add_argument("--path", type=int, default=0,
+                    help="--kernel-only: 0 auto, 1 GEMV, 2 mma.sync, 3 tcgen05")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

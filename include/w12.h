@@ -66,6 +66,7 @@ extern "C" {
 #define W12_PATH_AUTO 0
 #define W12_PATH_GEMV 1 /* CUDA-core FFMA GEMV with warp-shuffle reduction, M <= 4 */
 #define W12_PATH_MMA 2  /* tensor-core mma tiles, M <= 128                        */
+#define W12_PATH_TC 3   /* tcgen05 tiles, accumulator in tensor memory, M <= 128   */
 
 #define W12_MAX_M 128
 
@@ -181,25 +182,33 @@ int w12_gemm_ex(const w12_desc *d, const void *blob_dev, const uint16_t *x_dev, 
 
 #define W12_MAX_BATCH 8
 
-/* Bytes of workspace w12_gemm_batched needs for these matrices and M (0 on
- * invalid arguments). */
+/* Bytes of workspace w12_gemm_batched (and w12_gemm_batched_ex, on any path
+ * that serves this M) needs for these matrices and M (0 on invalid
+ * arguments). */
 size_t w12_gemm_batched_workspace_size(const w12_desc *descs, int count, int64_t M);
 
 /*
  * count independent products y_i = x_i . W_i (1 <= count <= W12_MAX_BATCH,
- * every K_i, N_i > 0) with one M, e.g. the linears of a decoder layer.  With
- * M <= 4 all of them run in ONE launch of the GEMV kernel: its work units of
- * all products are split evenly over the GPU, so small products (a layer's
- * k and v) neither run alone on a part of the SMs nor pay their own launch
- * and tail.  With larger M the products run one after the other on the
- * tensor-core path.  descs, blobs_dev, x_dev, y_dev are host arrays of count
- * entries (device pointers in the last three), with the layouts and
- * alignments of w12_gemm.  Errors: as w12_gemm; W12_ERR_SHAPE for an empty
- * product.
+ * every K_i, N_i > 0) with one M, e.g. the linears of a decoder layer, in ONE
+ * kernel launch: the work units of all products (stream-K units of columns x
+ * 1024 k) are split evenly over the GPU, so small products (a layer's k and
+ * v) neither run alone on a part of the SMs nor pay their own launch and
+ * tail.  descs, blobs_dev, x_dev, y_dev are host arrays of count entries
+ * (device pointers in the last three), with the layouts and alignments of
+ * w12_gemm.  The bits of the results depend only on the descriptors, M, the
+ * path and the GPU's SM count (the units' split over the CTAs fixes where
+ * fp32 partial sums are cut), so repeated calls give identical results.
+ * Errors: as w12_gemm; W12_ERR_SHAPE for an empty product.
  */
 int w12_gemm_batched(const w12_desc *descs, const void *const *blobs_dev,
                      const uint16_t *const *x_dev, int64_t M, void *const *y_dev, int y_dtype,
                      int count, void *ws_dev, size_t ws_bytes, void *stream);
+
+/* w12_gemm_batched with an explicit path (W12_PATH_*); W12_ERR_SHAPE if the
+ * path does not serve this M. */
+int w12_gemm_batched_ex(const w12_desc *descs, const void *const *blobs_dev,
+                        const uint16_t *const *x_dev, int64_t M, void *const *y_dev, int y_dtype,
+                        int count, void *ws_dev, size_t ws_bytes, int path, void *stream);
 
 /* Bytes of workspace w12_verify_greedy needs (>= 256). */
 size_t w12_verify_workspace_size(int64_t R, int64_t T, int64_t V);

@@ -55,7 +55,8 @@ int query_device(Device *dv) {
     return W12_OK;
 }
 
-// key: 0..15 GEMV variants, 16..31 split-K MMA variants, 32.. stream-K MMA variants
+// key: 0..15 GEMV variants, 16..31 split-K MMA variants, 32..47 stream-K MMA
+// variants, 48.. tcgen05 variants
 int cached_occupancy(const Device &dv, int key, size_t smem, int *blocks) {
     {
         std::lock_guard<std::mutex> lock(g_cache_mu);
@@ -68,7 +69,8 @@ int cached_occupancy(const Device &dv, int key, size_t smem, int *blocks) {
     }
     const int st = key < 16   ? gemv_occupancy(key, blocks)
                    : key < 32 ? mma_occupancy(key - 16, smem, blocks)
-                              : mma_sk_occupancy(key - 32, smem, blocks);
+                   : key < 48 ? mma_sk_occupancy(key - 32, smem, blocks)
+                              : tc_occupancy(key - 48, blocks);
     if (st != W12_OK) return st;
     std::lock_guard<std::mutex> lock(g_cache_mu);
     g_cache[dv.id].occ[{key, smem}] = *blocks;
@@ -249,11 +251,11 @@ size_t verify_ws(int64_t rows, int64_t splits) {
 
 
 // Workspace layout of a batch: header (error word), then per product its
-// stream-K counters and partial-sum slots.  Both paths are stream-K: the
-// GEMV (M <= 4, units of 16 columns x 1024 k) and the tensor-core kernel
-// (units of 128 columns x 1024 k).
+// stream-K counters and partial-sum slots.  All paths are stream-K: the
+// GEMV (M <= 4, units of 16 columns x 1024 k) and the two tensor-core
+// kernels, mma.sync and tcgen05 (units of 128 columns x 1024 k).
 struct BatchPlan {
-    bool gemv = false;
+    int path = W12_PATH_GEMV;
     int variant = 0, grid = 0, xchunk = 0;
     int64_t U = 0;
     size_t counters[kMaxBatch] = {}, partial[kMaxBatch] = {};
@@ -270,13 +272,20 @@ int plan_batch(const w12_desc *d, int count, int64_t M, int path, BatchPlan *bp)
     }
     if (path == W12_PATH_AUTO) path = M <= 1 ? W12_PATH_GEMV : W12_PATH_MMA;
     if (path == W12_PATH_GEMV && M > 4) return W12_ERR_SHAPE;
-    if (path != W12_PATH_GEMV && path != W12_PATH_MMA) return W12_ERR_ARG;
+    if (path != W12_PATH_GEMV && path != W12_PATH_MMA && path != W12_PATH_TC) return W12_ERR_ARG;
     Device dv;
     if (query_device(&dv) != W12_OK) return W12_ERR_CUDA;
-    bp->gemv = path == W12_PATH_GEMV;
+    bp->path = path;
     int64_t cpt, uk;
     int occ = 0;
-    if (bp->gemv) {
+    if (path == W12_PATH_TC) {
+        int v = 0;
+        while ((16 << v) < M) ++v;
+        bp->variant = v;
+        if (cached_occupancy(dv, 48 + v, 0, &occ) != W12_OK || occ < 1) return W12_ERR_CUDA;
+        cpt = kMmaCols;
+        uk = kMmaUnitK;
+    } else if (path == W12_PATH_GEMV) {
         bp->variant = M <= 1 ? 0 : M <= 2 ? 1 : 2;
         if (cached_occupancy(dv, bp->variant, 0, &occ) != W12_OK || occ < 1) return W12_ERR_CUDA;
         cpt = gemv_cols_per_tile();
@@ -345,8 +354,12 @@ int run_batch(const w12_desc *d, const void *const *blobs, const uint16_t *const
         g.partial = reinterpret_cast<float *>(w + bp.partial[i]);
         g.counters = reinterpret_cast<uint32_t *>(w + bp.counters[i]);
     }
-    return bp.gemv ? launch_gemv_batch(b, bp.variant, bp.grid, stream)
-                   : launch_mma_batch(b, bp.variant, bp.grid, stream);
+    switch (bp.path) {
+        case W12_PATH_GEMV: return launch_gemv_batch(b, bp.variant, bp.grid, stream);
+        case W12_PATH_MMA: return launch_mma_batch(b, bp.variant, bp.grid, stream);
+        case W12_PATH_TC: return launch_tc_batch(b, bp.variant, bp.grid, stream);
+    }
+    return W12_ERR_ARG;
 }
 
 }  // namespace
@@ -387,12 +400,7 @@ extern "C" int w12_decode(const w12_desc *d, const void *blob, uint16_t *w, int 
 extern "C" size_t w12_gemm_workspace_size(const w12_desc *d, int64_t M) {
     if (check_desc(d) != W12_OK || M < 1 || M > W12_MAX_M) return 0;
     // room for either path this M can take, so w12_gemm_ex can switch paths
-    size_t need = 0;
-    BatchPlan bp;
-    if (M <= 4 && plan_batch(d, 1, M, W12_PATH_GEMV, &bp) == W12_OK) need = std::max(need, bp.total);
-    BatchPlan bq;
-    if (plan_batch(d, 1, M, W12_PATH_MMA, &bq) == W12_OK) need = std::max(need, bq.total);
-    return need;
+    return w12_gemm_batched_workspace_size(d, 1, M);
 }
 
 extern "C" int w12_gemm_ex(const w12_desc *d, const void *blob, const uint16_t *x, int64_t M,
@@ -402,7 +410,7 @@ extern "C" int w12_gemm_ex(const w12_desc *d, const void *blob, const uint16_t *
     if (st != W12_OK) return st;
     if (M < 1 || M > W12_MAX_M) return W12_ERR_SHAPE;
     if (y_dtype != W12_F32 && y_dtype != W12_BF16) return W12_ERR_ARG;
-    if (path < W12_PATH_AUTO || path > W12_PATH_MMA) return W12_ERR_ARG;
+    if (path < W12_PATH_AUTO || path > W12_PATH_TC) return W12_ERR_ARG;
     if (d->N == 0) return W12_OK;
     if (!y) return W12_ERR_ARG;
     if (!aligned(y, y_dtype == W12_F32 ? 4 : 2)) return W12_ERR_ALIGN;
@@ -431,17 +439,24 @@ extern "C" int w12_gemm(const w12_desc *d, const void *blob, const uint16_t *x, 
 
 
 extern "C" size_t w12_gemm_batched_workspace_size(const w12_desc *d, int count, int64_t M) {
-    BatchPlan bp;
-    return plan_batch(d, count, M, W12_PATH_AUTO, &bp) == W12_OK ? bp.total : 0;
+    // room for every path this M can take, so the _ex call can switch paths
+    size_t need = 0;
+    for (int path = W12_PATH_GEMV; path <= W12_PATH_TC; ++path) {
+        if (path == W12_PATH_GEMV && M > 4) continue;
+        BatchPlan bp;
+        if (plan_batch(d, count, M, path, &bp) == W12_OK) need = std::max(need, bp.total);
+    }
+    return need;
 }
 
-extern "C" int w12_gemm_batched(const w12_desc *d, const void *const *blobs, const uint16_t *const *xs,
-                                int64_t M, void *const *ys, int y_dtype, int count, void *ws,
-                                size_t ws_bytes, void *stream) {
+extern "C" int w12_gemm_batched_ex(const w12_desc *d, const void *const *blobs, const uint16_t *const *xs,
+                                   int64_t M, void *const *ys, int y_dtype, int count, void *ws,
+                                   size_t ws_bytes, int path, void *stream) {
     if (!blobs || !xs || !ys) return W12_ERR_ARG;
     if (y_dtype != W12_F32 && y_dtype != W12_BF16) return W12_ERR_ARG;
+    if (path < W12_PATH_AUTO || path > W12_PATH_TC) return W12_ERR_ARG;
     BatchPlan bp;
-    int st = plan_batch(d, count, M, W12_PATH_AUTO, &bp);
+    int st = plan_batch(d, count, M, path, &bp);
     if (st != W12_OK) return st;
     for (int i = 0; i < count; ++i) {
         if (d[i].N == 0 || d[i].K == 0) return W12_ERR_SHAPE;  // empty products: use w12_gemm
@@ -452,6 +467,12 @@ extern "C" int w12_gemm_batched(const w12_desc *d, const void *const *blobs, con
     if (!ws || ws_bytes < bp.total) return W12_ERR_WORKSPACE;
     if (!aligned(ws, 256)) return W12_ERR_ALIGN;
     return run_batch(d, blobs, xs, M, ys, y_dtype, count, ws, bp, stream);
+}
+
+extern "C" int w12_gemm_batched(const w12_desc *d, const void *const *blobs, const uint16_t *const *xs,
+                                int64_t M, void *const *ys, int y_dtype, int count, void *ws,
+                                size_t ws_bytes, void *stream) {
+    return w12_gemm_batched_ex(d, blobs, xs, M, ys, y_dtype, count, ws, ws_bytes, W12_PATH_AUTO, stream);
 }
 
 extern "C" size_t w12_verify_workspace_size(int64_t R, int64_t T, int64_t V) {

@@ -1,7 +1,7 @@
-// gemm_common.cuh -- tile scheduling and the split-K epilogue shared by the
-// W12 GEMM kernels.
+// gemm_common.cuh -- tile scheduling, the split-K epilogue of the fused
+// lm_head kernel and the stream-K fix-up of the batched GEMM kernels.
 //
-// Work is cut into tiles (column block nb, k split kc), tile t = kc*NB + nb.
+// Split-K (fused lm_head): work is cut into tiles (column block nb, k split kc), tile t = kc*NB + nb.
 // CTA c owns the contiguous range of tiles [t0, t1) (balanced to within one
 // tile).  With one split a tile writes y directly.  With several, it writes
 // fp32 partials[kc][m][n], bumps the arrival counter of its column block,
@@ -80,63 +80,81 @@ __device__ __forceinline__ void store_out(void *y, int y_dtype, int64_t N, int64
         static_cast<__nv_bfloat16 *>(y)[m * N + n] = __float2bfloat16_rn(v);
 }
 
-// Stream-K fix-up on explicit buffers (the batched GEMV): same protocol as
-// streamk_fixup below; slots are partial[((nb * steps + ks) * M + m) * cpt + c].
-__device__ __forceinline__ void streamk_fixup_raw(uint32_t *counters, float *partial, int64_t steps,
-                                                  int M, int64_t N, void *y, int y_dtype, int64_t cpt,
-                                                  int64_t nb, int64_t count, int *s_last, int tid,
-                                                  int nthreads) {
+// Balanced partition of U stream-K units over the grid: CTA c takes the
+// units [sk_unit_begin(c), sk_unit_begin(c + 1)).
+__device__ __forceinline__ int sk_unit_begin(int c, int per, int rem) { return c * per + min(c, rem); }
+
+__device__ __forceinline__ int sk_cta_of(int u, int per, int rem) {
+    const int big = rem * (per + 1);
+    return u < big ? u / (per + 1) : rem + (u - big) / per;
+}
+
+// Stream-K fix-up of the batched kernels.  Column tile nb of a product
+// covers the global units [first, first + steps) (the product's units start
+// at ubase); U units are spread over the grid as above.  Every CTA that
+// covered a piece of the tile stored the piece's partial sums (all m < M,
+// n < N) in the slot of the piece's first unit,
+//   partial[((u - ubase) * M + m) * cpt + c],
+// and adds the piece's unit count to counters[nb].  The CTA that brings the
+// count to `steps` sums the pieces' slots in unit order (the same bits on
+// every call), writes y, and sets the counter back to zero.  Slots need no
+// clearing: only slots that were written are read.
+__device__ __forceinline__ void streamk_fixup_raw(uint32_t *counters, const float *partial, int first,
+                                                  int ubase, int steps, int U, int M, int N, void *y,
+                                                  int y_dtype, int cpt, int nb, int count, int *s_last,
+                                                  int tid, int nthreads) {
     __threadfence();
     epi_sync(nthreads);
     if (tid == 0) {
         const uint32_t old = atomicAdd(&counters[nb], uint32_t(count));
-        *s_last = (int64_t(old) + count == steps);
+        *s_last = (int(old) + count == steps);
     }
     epi_sync(nthreads);
     if (*s_last) {
         __threadfence();
-        for (int64_t o = tid; o < cpt * M; o += nthreads) {
-            const int64_t m = o / cpt, c = o % cpt, n = nb * cpt + c;
-            float s = 0.f;
-            for (int64_t ks = 0; ks < steps; ++ks) {
-                float *slot = &partial[((nb * steps + ks) * M + m) * cpt + c];
-                s += __ldcg(slot);
-                *slot = 0.f;
+        const int G = int(gridDim.x), per = U / G, rem = U % G;
+        const int c_first = sk_cta_of(first, per, rem);
+        const int q4 = cpt / 4, total = M * q4;  // float4 groups of a slot
+        const size_t slot_floats = size_t(M) * size_t(cpt);
+        constexpr int kB = 4;  // groups per thread in flight
+        for (int o0 = tid; o0 < total; o0 += kB * nthreads) {
+            float4 acc[kB];
+            for (int c = c_first;; ++c) {
+                const int us = max(first, sk_unit_begin(c, per, rem));
+                if (us >= first + steps) break;
+                const float *slot = partial + size_t(us - ubase) * slot_floats;
+                float4 v[kB];
+#pragma unroll
+                for (int j = 0; j < kB; ++j) {
+                    const int o = o0 + j * nthreads;
+                    v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (o < total)
+                        v[j] = __ldcg(reinterpret_cast<const float4 *>(slot + size_t(o / q4) * cpt) + o % q4);
+                }
+#pragma unroll
+                for (int j = 0; j < kB; ++j) {
+                    if (c == c_first) {
+                        acc[j] = v[j];
+                    } else {
+                        acc[j].x += v[j].x;
+                        acc[j].y += v[j].y;
+                        acc[j].z += v[j].z;
+                        acc[j].w += v[j].w;
+                    }
+                }
             }
-            if (n < N) store_out(y, y_dtype, N, m, n, s);
+#pragma unroll
+            for (int j = 0; j < kB; ++j) {
+                const int o = o0 + j * nthreads;
+                if (o >= total) break;
+                const int m = o / q4, n0 = nb * cpt + 4 * (o % q4);
+                const float r[4] = {acc[j].x, acc[j].y, acc[j].z, acc[j].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (n0 + e < N) store_out(y, y_dtype, N, m, n0 + e, r[e]);
+            }
         }
         if (tid == 0) counters[nb] = 0u;
-    }
-    epi_sync(nthreads);
-}
-
-// Stream-K fix-up of column tile nb after a CTA covered `count` of its
-// `steps` stages and stored its partial sums in slot (nb, first stage).  The
-// CTA that completes the tile sums the slots in stage order (deterministic),
-// writes y, and zeroes the slots and the counter for the next call.
-__device__ __forceinline__ void streamk_fixup(const GemmArgs &a, int64_t nb, int64_t count,
-                                              int *s_last, int tid, int nthreads) {
-    __threadfence();
-    epi_sync(nthreads);
-    if (tid == 0) {
-        const uint32_t old = atomicAdd(&a.counters[nb], uint32_t(count));
-        *s_last = (int64_t(old) + count == a.steps);
-    }
-    epi_sync(nthreads);
-    if (*s_last) {
-        __threadfence();
-        const int64_t cpt = a.cols_per_tile;
-        for (int64_t o = tid; o < cpt * a.M; o += nthreads) {
-            const int64_t m = o / cpt, c = o % cpt, n = nb * cpt + c;
-            float s = 0.f;
-            for (int64_t ks = 0; ks < a.steps; ++ks) {
-                float *slot = &a.partial[((nb * a.steps + ks) * a.M + m) * cpt + c];
-                s += __ldcg(slot);
-                *slot = 0.f;
-            }
-            if (n < a.N) store_y(a, m, n, s);
-        }
-        if (tid == 0) a.counters[nb] = 0u;
     }
     epi_sync(nthreads);
 }

@@ -269,8 +269,8 @@ __global__ void __launch_bounds__(kThreads, GemvCfg<MT>::kMinBlocks) gemv_kernel
             }
         }
         if (!whole)
-            streamk_fixup_raw(g.counters, g.partial, g.steps, M, g.N, g.y, b.y_dtype, kCols, nb,
-                              ub - ua, &s_last, threadIdx.x, kThreads);
+            streamk_fixup_raw(g.counters, g.partial, first, g.ubase, g.steps, b.U, M, g.N, g.y, b.y_dtype, kCols,
+                              nb, ub - ua, &s_last, threadIdx.x, kThreads);
     }
     cp_async_wait<0>();
 }

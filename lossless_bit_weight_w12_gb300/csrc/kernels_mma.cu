@@ -236,8 +236,8 @@ __global__ void __launch_bounds__(kThreads, NT >= 8 ? 1 : 2) mma_sk_kernel(const
             }
         }
         if (!whole)
-            streamk_fixup_raw(g.counters, g.partial, g.steps, M, g.N, g.y, b.y_dtype, kColsPerTile, nb,
-                              ub - ua, &s_last, threadIdx.x, kThreads);
+            streamk_fixup_raw(g.counters, g.partial, first, g.ubase, g.steps, b.U, M, g.N, g.y, b.y_dtype, kColsPerTile,
+                              nb, ub - ua, &s_last, threadIdx.x, kThreads);
     }
 }
 

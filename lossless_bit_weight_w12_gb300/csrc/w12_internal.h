@@ -99,6 +99,9 @@ int launch_mma_batch(const GemvBatch &b, int variant, int grid, void *stream);
 int mma_sk_occupancy(int variant, size_t smem, int *blocks_per_sm);
 constexpr int kMmaUnitK = 1024;
 constexpr int kMmaCols = 128;
+// The tcgen05 kernel takes the same batch and units (variant = log2(MP / 16)).
+int launch_tc_batch(const GemvBatch &b, int variant, int grid, void *stream);
+int tc_occupancy(int variant, int *blocks_per_sm);
 
 // Launchers (return W12_OK or W12_ERR_CUDA).
 int launch_decode(const w12_desc *d, const void *blob, uint16_t *w, int layout, int *err,

@@ -22,7 +22,7 @@ ERR_ARG, ERR_SHAPE, ERR_ALIGN, ERR_WORKSPACE, ERR_BLOB = 1, 2, 3, 4, 5
 ERR_TOO_MANY_ESCAPES, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE = 6, 7, 8, 9
 LAYOUT_KN, LAYOUT_NK = 0, 1
 F32, BF16 = 0, 1
-PATH_AUTO, PATH_GEMV, PATH_MMA = 0, 1, 2
+PATH_AUTO, PATH_GEMV, PATH_MMA, PATH_TC = 0, 1, 2, 3
 MAX_M = 128
 
 # every symbol include/w12.h declares
@@ -31,7 +31,7 @@ EXPORTS = (
     "w12_decode", "w12_gemm_workspace_size", "w12_gemm", "w12_gemm_ex",
     "w12_verify_workspace_size", "w12_verify_greedy", "w12_verify_lmhead_workspace_size",
     "w12_verify_greedy_lmhead", "w12_get_device_error", "w12_verify_greedy_noalloc",
-    "w12_gemm_batched_workspace_size", "w12_gemm_batched",
+    "w12_gemm_batched_workspace_size", "w12_gemm_batched", "w12_gemm_batched_ex",
 )
 
 
@@ -109,6 +109,7 @@ def lib():
         L.w12_gemm_batched_workspace_size.restype = SZ
         L.w12_gemm_batched_workspace_size.argtypes = [D, I, I64]
         L.w12_gemm_batched.argtypes = [D, P, P, I64, P, I, I, P, SZ, P]
+        L.w12_gemm_batched_ex.argtypes = [D, P, P, I64, P, I, I, P, SZ, I, P]
         _lib = L
     return _lib
 
@@ -219,9 +220,10 @@ class GemmBatch:
     """Marshalled arguments of one w12_gemm_batched call (built once, reused:
     the pointer arrays stay valid while the tensors live)."""
 
-    def __init__(self, descs, blobs, xs, ys, ws):
+    def __init__(self, descs, blobs, xs, ys, ws, path: int = PATH_AUTO):
         import torch
         n = len(descs)
+        self.path = path
         self.descs = _desc_array(descs)
         self.blobs = (ctypes.c_void_p * n)(*[t.data_ptr() for t in blobs])
         self.xs = (ctypes.c_void_p * n)(*[t.data_ptr() for t in xs])
@@ -233,15 +235,16 @@ class GemmBatch:
         self._keep = (blobs, xs, ys, ws)
 
     def __call__(self, stream=None):
-        _check(lib().w12_gemm_batched(self.descs, self.blobs, self.xs, self.M, self.ys,
-                                      self.y_dtype, self.count, _dptr(self.ws),
-                                      self.ws.numel() * self.ws.element_size(), _stream(stream)),
-               "w12_gemm_batched")
+        _check(lib().w12_gemm_batched_ex(self.descs, self.blobs, self.xs, self.M, self.ys,
+                                         self.y_dtype, self.count, _dptr(self.ws),
+                                         self.ws.numel() * self.ws.element_size(), self.path,
+                                         _stream(stream)),
+               "w12_gemm_batched_ex")
 
 
-def gemm_batched(descs, blobs, xs, ys, ws, stream=None):
-    """ys[i] = xs[i] @ W_i for every i, one launch when M <= 4."""
-    GemmBatch(descs, blobs, xs, ys, ws)(stream)
+def gemm_batched(descs, blobs, xs, ys, ws, path: int = PATH_AUTO, stream=None):
+    """ys[i] = xs[i] @ W_i for every i, in one launch."""
+    GemmBatch(descs, blobs, xs, ys, ws, path)(stream)
 
 
 def verify_workspace_size(R: int, T: int, V: int) -> int:

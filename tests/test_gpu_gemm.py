@@ -31,7 +31,8 @@ def _run(w12mod, dev, d, blob_d, x, path, y_dtype="f32"):
 
 
 def _paths(M):
-    return [1, 2] if M <= 4 else [2]
+    """Every explicit path that serves M: GEMV (M <= 4), mma.sync, tcgen05."""
+    return [1, 2, 3] if M <= 4 else [2, 3]
 
 
 SHAPES = [(128, 1), (128, 7), (384, 33), (1024, 130), (1152, 257), (5120, 96), (6144, 64)]
@@ -113,7 +114,10 @@ def test_gemm_nonfinite(dev, w12mod, oracle):
         check_gemm(y, y_ref, s_ref, what=f"nonfinite path={path}")
 
 
-def test_gemm_deterministic(dev, w12mod):
+@pytest.mark.parametrize("path", [2, 3])
+def test_gemm_deterministic(dev, w12mod, path):
+    """Stream-K partial sums are added in a fixed order: repeated calls give
+    the same bits (K = 17408 spreads every column tile over several CTAs)."""
     import torch
     K, N, M = 17408, 640, 16
     rng = synth.streams(3, 2)
@@ -125,7 +129,7 @@ def test_gemm_deterministic(dev, w12mod):
     ys = []
     for _ in range(3):
         y = torch.empty((M, N), dtype=torch.float32, device=dev)
-        w12mod.gemm(d, blob_d, x, y, ws)
+        w12mod.gemm(d, blob_d, x, y, ws, path=path)
         ys.append(y)
     assert torch.equal(ys[0], ys[1]) and torch.equal(ys[1], ys[2])
 
@@ -141,13 +145,14 @@ def test_gemm_full_layer_sampled(dev, w12mod, oracle, M):
         x = synth.activations(rng[len(synth.LAYER_SHAPES) + i], M, K)
         d, blob = w12mod.encode(w, w12mod.LAYOUT_NK)
         blob_d = w12mod.upload(blob, dev)
-        y = _run(w12mod, dev, d, blob_d, x, 0)
         pick = np.random.default_rng(i)
         ns = np.unique(np.r_[pick.integers(0, N, 22), [0, N - 1]])
         # the oracle encodes and multiplies only the sampled columns
         od, oblob = oracle.encode(w[ns], oracle.LAYOUT_NK)
         y_ref, s_ref = oracle.gemm(od, oblob, x)
-        check_gemm(y[:, ns], y_ref, s_ref, what=f"{name} M={M}")
+        for path in [0] + ([] if M == 1 else [2, 3]):
+            y = _run(w12mod, dev, d, blob_d, x, path)
+            check_gemm(y[:, ns], y_ref, s_ref, what=f"{name} M={M} path={path}")
         del blob_d
 
 
@@ -192,7 +197,7 @@ def test_gemm_k_zero_writes_zeros(dev, w12mod):
     assert torch.count_nonzero(y).item() == 0
 
 
-def _batched(w12mod, dev, items, M, y_dtype="f32"):
+def _batched(w12mod, dev, items, M, y_dtype="f32", path=0):
     """items: list of (desc, blob_dev, x uint16 [M,K]); returns list of fp64 y."""
     import torch
     xs = [to_dev_bits(x, dev) for _, _, x in items]
@@ -200,7 +205,7 @@ def _batched(w12mod, dev, items, M, y_dtype="f32"):
           for d, _, _ in items]
     descs = [d for d, _, _ in items]
     ws = w12mod.workspace(w12mod.gemm_batched_workspace_size(descs, M), dev)
-    w12mod.gemm_batched(descs, [b for _, b, _ in items], xs, ys, ws)
+    w12mod.gemm_batched(descs, [b for _, b, _ in items], xs, ys, ws, path=path)
     torch.cuda.synchronize()
     assert w12mod.get_device_error(ws) == 0
     if y_dtype == "f32":
@@ -208,7 +213,7 @@ def _batched(w12mod, dev, items, M, y_dtype="f32"):
     return [bf16_bits_to_f64(dev_bits_to_np(y)) for y in ys]
 
 
-@pytest.mark.parametrize("M", [1, 2, 3, 4, 16])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 16, 33, 128])
 def test_gemm_batched_mixed_shapes(dev, w12mod, oracle, M):
     """One launch over products of different K and N (ragged tiles and unit
     counts), each checked against the oracle."""
@@ -221,13 +226,30 @@ def test_gemm_batched_mixed_shapes(dev, w12mod, oracle, M):
         d, blob = w12mod.encode(w, w12mod.LAYOUT_NK)
         items.append((d, w12mod.upload(blob, dev), x))
         refs.append(oracle.gemm(*oracle.encode(w, oracle.LAYOUT_NK), x))
-    for rep in range(2):  # the workspace is reused by the second call
-        ys = _batched(w12mod, dev, items, M)
-        for (K, N), y, (y_ref, s_ref) in zip(shapes, ys, refs):
-            check_gemm(y, y_ref, s_ref, what=f"batched K={K} N={N} M={M}")
+    for path in _paths(M):
+        for rep in range(2):  # the workspace is reused by the second call
+            ys = _batched(w12mod, dev, items, M, path=path)
+            for (K, N), y, (y_ref, s_ref) in zip(shapes, ys, refs):
+                check_gemm(y, y_ref, s_ref, what=f"batched K={K} N={N} M={M} path={path}")
 
 
-@pytest.mark.parametrize("M", [1, 4])
+@pytest.mark.parametrize("M,path", [(2, 1), (16, 2), (16, 3), (100, 3)])
+def test_gemm_batched_repeatable(dev, w12mod, M, path):
+    """Repeated batched calls give the same bits: partial sums are combined
+    in unit order, whichever CTA finishes a tile."""
+    shapes = [(5120, 1030), (17408, 300), (384, 33)]
+    rng = synth.streams(4100 + M, 2 * len(shapes))
+    items = []
+    for i, (K, N) in enumerate(shapes):
+        d, blob = w12mod.encode(synth.weights(rng[2 * i], K, N), w12mod.LAYOUT_NK)
+        items.append((d, w12mod.upload(blob, dev), synth.activations(rng[2 * i + 1], M, K)))
+    ya = _batched(w12mod, dev, items, M, path=path)
+    yb = _batched(w12mod, dev, items, M, path=path)
+    for a, bb in zip(ya, yb):
+        assert np.array_equal(a, bb)
+
+
+@pytest.mark.parametrize("M", [1, 4, 16, 128])
 def test_gemm_batched_full_layer(dev, w12mod, oracle, M):
     """The layer's six linears in one launch, full size, sampled columns."""
     rng = synth.streams(1, len(synth.LAYER_SHAPES) + 8)
@@ -238,11 +260,15 @@ def test_gemm_batched_full_layer(dev, w12mod, oracle, M):
         d, blob = w12mod.encode(w, w12mod.LAYOUT_NK)
         items.append((d, w12mod.upload(blob, dev), x))
         ws_.append(w)
-    ys = _batched(w12mod, dev, items, M)
+    refs = []
     for i, (name, K, N) in enumerate(synth.LAYER_SHAPES):
         ns = np.unique(np.r_[np.random.default_rng(i).integers(0, N, 20), [0, N - 1]])
-        y_ref, s_ref = oracle.gemm(*oracle.encode(ws_[i][ns], oracle.LAYOUT_NK), items[i][2])
-        check_gemm(ys[i][:, ns], y_ref, s_ref, what=f"batched {name} M={M}")
+        refs.append((ns, oracle.gemm(*oracle.encode(ws_[i][ns], oracle.LAYOUT_NK), items[i][2])))
+    for path in [0] + _paths(M):
+        ys = _batched(w12mod, dev, items, M, path=path)
+        for i, (name, K, N) in enumerate(synth.LAYER_SHAPES):
+            ns, (y_ref, s_ref) = refs[i]
+            check_gemm(ys[i][:, ns], y_ref, s_ref, what=f"batched {name} M={M} path={path}")
 
 
 def test_gemm_batched_argument_errors(dev, w12mod):
