@@ -346,32 +346,30 @@ def run_w12(args):
     nbytes = _layer_bytes()
 
     # ---- timed region: K steps in one CUDA graph; a step is ONE batched
-    # launch over the six linears (stream-K over all their work units), with
-    # an event pair around it
+    # launch over the six linears (stream-K over all their work units).  No
+    # event nodes inside the graph: each step is exactly one kernel launch,
+    # so the timed region / K is that kernel's mean launch duration (gaps
+    # between launches included).
     descs = [g["desc"] for g in layer]
     blobs = [g["blob"] for g in layer]
     ws_b = w12.workspace(w12.gemm_batched_workspace_size(descs, 1), dev)
     batch = w12.GemmBatch(descs, blobs, x1, ys, ws_b)
 
-    def layer_step(mark=None):
-        done = mark("layer") if mark is not None else None
-        batch()
-        if done is not None:
-            done()
-    gsteps = GraphSteps(torch, layer_step, args.steps)
-    gwarm = GraphSteps(torch, layer_step, args.warmup)
+    gsteps = GraphSteps(torch, lambda mark: batch(), args.steps)
+    gwarm = GraphSteps(torch, lambda mark: batch(), args.warmup)
     gwarm.run(barrier)
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
     dt = gsteps.run(barrier)
     clk = clocks.stop()
-    t_launch = gsteps.per_launch().get("layer")
+    t_launch = dt / args.steps
     if world > 1:
         t = torch.tensor([dt], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         dt = float(t.item())
     value = world * nbytes * args.steps / dt / 1e9
     assert w12.get_device_error(ws_b) == 0
+    del gsteps, gwarm
 
     # ---- per-GEMM view: the six linears as six launches (informational)
     gsep = GraphSteps(torch, lambda mark: run_step(w12, layer, x1, ys, wss, mark), max(3, args.steps // 2))
@@ -382,24 +380,33 @@ def run_w12(args):
     for wsb in wss:
         assert w12.get_device_error(wsb) == 0
 
-    # ---- e2e: through the public API with host buffers, copies inside
-    pin_x = [x.cpu().pin_memory() for x in x1]
-    pin_y = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in ys]
-    xd = [torch.empty_like(x) for x in x1]
-
-    batch_e2e = w12.GemmBatch(descs, blobs, xd, ys, ws_b)
+    # ---- e2e: through the public API with host buffers, copies inside.
+    # The six x live in one pinned host buffer and one device buffer (one
+    # host->device copy per step), the six y in one device buffer (one
+    # device->host copy per step).
+    xsz = [x.numel() for x in x1]
+    ysz = [y.numel() for y in ys]
+    pin_x = torch.cat([x.reshape(-1) for x in x1]).cpu().pin_memory()
+    pin_y = torch.empty(sum(ysz), dtype=torch.float32).pin_memory()
+    xd_all = torch.empty_like(pin_x, device=dev)
+    yd_all = torch.empty(sum(ysz), dtype=torch.float32, device=dev)
+    xd = [v.view(x.shape) for v, x in zip(torch.split(xd_all, xsz), x1)]
+    yd = [v.view(y.shape) for v, y in zip(torch.split(yd_all, ysz), ys)]
+    batch_e2e = w12.GemmBatch(descs, blobs, xd, yd, ws_b)
 
     def e2e_step():
-        for i in range(len(layer)):
-            xd[i].copy_(pin_x[i], non_blocking=True)
+        xd_all.copy_(pin_x, non_blocking=True)
         batch_e2e()
-        for i in range(len(layer)):
-            pin_y[i].copy_(ys[i], non_blocking=True)
+        pin_y.copy_(yd_all, non_blocking=True)
     for _ in range(2):
         e2e_step()
     dt_e2e = time_steps(torch, e2e_step, args.steps, barrier)
-    h2d = sum(x.numel() * 2 for x in x1)
-    d2h = sum(y.numel() * 4 for y in ys)
+    h2d = pin_x.numel() * pin_x.element_size()
+    d2h = pin_y.numel() * pin_y.element_size()
+    batch()
+    torch.cuda.synchronize()
+    for y_ref, y_e2e in zip(ys, yd):
+        assert torch.equal(y_ref, y_e2e), "e2e result differs from the device-resident run"
 
     # ---- sweep over M (same weights; inputs > L2)
     sweep = {}
@@ -440,12 +447,13 @@ def run_w12(args):
     if args.verify:
         verify = bench_lmhead(w12, torch, dev, args, barrier)
 
-    # ---- roofline of the dominant kernel: the step's single batched GEMV launch
+    # ---- roofline of the dominant kernel: the step's single batched launch
     achieved = nbytes / t_launch / 1e9 if t_launch else None
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                 "frac": achieved / hbm_peak if achieved else None,
-                "traffic": traffic_for("gemv_layer_m1"),
-                "kernel": "gemv_kernel<1> over the six layer linears (one launch per step)",
+                "traffic": traffic_for("stream_layer_m1"),
+                "kernel": "stream_kernel<1,2> (TMA-fed mma.sync W12 decode-GEMM) over the six "
+                          "layer linears (one launch per step)",
                 "peak_kind": f"{peak_kind} hbm_gbs (copy)",
                 "algorithmic_bytes_per_launch": nbytes}
 
@@ -469,8 +477,8 @@ def run_w12(args):
         "frac_of_peak": value / world / hbm_peak,
         "per_gemm_us": {k: 1e6 * v for k, v in per_gemm.items()},
         "unbatched_us_per_layer": 1e6 * t_sep,
-        "timing": "K steps replayed from one CUDA graph; a step is one batched launch; "
-                  "per-GEMM times from a separate unbatched graph",
+        "timing": "K steps replayed from one CUDA graph (no event nodes inside); a step is one "
+                  "batched launch; per-GEMM times from a separate unbatched graph with event nodes",
         "e2e": {"value": world * nbytes * args.steps / dt_e2e / 1e9, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps,

@@ -8,6 +8,7 @@
 #include <mutex>
 #include <utility>
 
+#include "stream_common.h"
 #include "w12_internal.h"
 
 namespace w12 {
@@ -55,8 +56,8 @@ int query_device(Device *dv) {
     return W12_OK;
 }
 
-// key: 0..15 GEMV variants, 16..31 split-K MMA variants, 32..47 stream-K MMA
-// variants, 48.. tcgen05 variants
+// key: 0..15 GEMV variants, 16..31 split-K MMA variants (fused lm_head),
+// 48..63 tcgen05 variants, 64.. TMA-fed stream-K variants
 int cached_occupancy(const Device &dv, int key, size_t smem, int *blocks) {
     {
         std::lock_guard<std::mutex> lock(g_cache_mu);
@@ -69,8 +70,8 @@ int cached_occupancy(const Device &dv, int key, size_t smem, int *blocks) {
     }
     const int st = key < 16   ? gemv_occupancy(key, blocks)
                    : key < 32 ? mma_occupancy(key - 16, smem, blocks)
-                   : key < 48 ? mma_sk_occupancy(key - 32, smem, blocks)
-                              : tc_occupancy(key - 48, blocks);
+                   : key < 64 ? tc_occupancy(key - 48, blocks)
+                              : stream_occupancy(key - 64, blocks);
     if (st != W12_OK) return st;
     std::lock_guard<std::mutex> lock(g_cache_mu);
     g_cache[dv.id].occ[{key, smem}] = *blocks;
@@ -251,17 +252,30 @@ size_t verify_ws(int64_t rows, int64_t splits) {
 
 
 // Workspace layout of a batch: header (error word), then per product its
-// stream-K counters and partial-sum slots.  All paths are stream-K: the
-// GEMV (M <= 4, units of 16 columns x 1024 k) and the two tensor-core
-// kernels, mma.sync and tcgen05 (units of 128 columns x 1024 k).
+// stream-K counters, then the partial sums.  All paths are stream-K: the
+// GEMV (M <= 4, units of 16 columns x 1024 k, a partial slot per unit), the
+// TMA-fed mma.sync kernel (units of 128 columns x one 128-k group, two
+// partial slots per CTA) and the tcgen05 kernel (units of 128 columns x
+// 1024 k, a partial slot per unit).
 struct BatchPlan {
     int path = W12_PATH_GEMV;
     int variant = 0, grid = 0, xchunk = 0;
     int64_t U = 0;
     size_t counters[kMaxBatch] = {}, partial[kMaxBatch] = {};
     int64_t steps[kMaxBatch] = {}, NB[kMaxBatch] = {}, ubase[kMaxBatch] = {};
+    size_t stream_partial = 0;  // MMA path: [grid][2][M][128] floats
     size_t total = 0;
 };
+
+// TMA-fed mma.sync kernel variant for M: NT = tokens padded to 8 .. 128 in
+// powers of two; two CTAs per SM up to 32 tokens (measured faster on the
+// 27B-class layer: 89 vs 104 us at M = 1, 97 vs 108 at 16, 110 vs 125 at
+// 32), one CTA with the deepest ring beyond.
+int stream_variant_for(int64_t M) {
+    int l = 0;
+    while ((8 << l) < M) ++l;
+    return l <= 2 ? 2 * l + 1 : 2 * l;
+}
 
 int plan_batch(const w12_desc *d, int count, int64_t M, int path, BatchPlan *bp) {
     if (!d || count < 1 || count > kMaxBatch || M < 1 || M > W12_MAX_M) return W12_ERR_ARG;
@@ -270,7 +284,7 @@ int plan_batch(const w12_desc *d, int count, int64_t M, int path, BatchPlan *bp)
         if (st != W12_OK) return st;
         if (!gemv_fits_32bit(&d[i])) return W12_ERR_SHAPE;
     }
-    if (path == W12_PATH_AUTO) path = M <= 1 ? W12_PATH_GEMV : W12_PATH_MMA;
+    if (path == W12_PATH_AUTO) path = W12_PATH_MMA;
     if (path == W12_PATH_GEMV && M > 4) return W12_ERR_SHAPE;
     if (path != W12_PATH_GEMV && path != W12_PATH_MMA && path != W12_PATH_TC) return W12_ERR_ARG;
     Device dv;
@@ -291,19 +305,12 @@ int plan_batch(const w12_desc *d, int count, int64_t M, int path, BatchPlan *bp)
         cpt = gemv_cols_per_tile();
         uk = gemv_stage_k();
     } else {
-        int nt = 1, v = 0;
-        while (nt * 8 < M) {
-            nt *= 2;
-            ++v;
-        }
-        bp->variant = v;
-        const int64_t mp = 8 * nt;
-        bp->xchunk = int(std::min<int64_t>(kMmaUnitK, std::max<int64_t>(1, 32768 / mp / kGroup) * kGroup));
-        if (cached_occupancy(dv, 32 + v, size_t(mp * bp->xchunk * 2), &occ) != W12_OK || occ < 1)
-            return W12_ERR_CUDA;
+        bp->variant = stream_variant_for(M);
+        if (cached_occupancy(dv, 64 + bp->variant, 0, &occ) != W12_OK || occ < 1) return W12_ERR_CUDA;
         cpt = kMmaCols;
-        uk = kMmaUnitK;
+        uk = kGroup;
     }
+    const bool per_unit_slots = path != W12_PATH_MMA;
     size_t off = kWsHeader;
     for (int i = 0; i < count; ++i) {
         bp->steps[i] = ceil_div(d[i].K, uk);
@@ -313,17 +320,55 @@ int plan_batch(const w12_desc *d, int count, int64_t M, int path, BatchPlan *bp)
         bp->counters[i] = off;
         off += round256(4u * uint64_t(std::max<int64_t>(bp->NB[i], 1)));
         bp->partial[i] = off;
-        off += round256(uint64_t(bp->steps[i] * bp->NB[i]) * uint64_t(M) * uint64_t(cpt) * 4u);
+        if (per_unit_slots)
+            off += round256(uint64_t(bp->steps[i] * bp->NB[i]) * uint64_t(M) * uint64_t(cpt) * 4u);
     }
     if (bp->U >= (int64_t(1) << 31)) return W12_ERR_SHAPE;
     bp->grid = int(std::min<int64_t>(int64_t(dv.sms) * occ, std::max<int64_t>(bp->U, 1)));
+    if (!per_unit_slots) {
+        bp->stream_partial = off;
+        off += round256(uint64_t(bp->grid) * 2u * uint64_t(M) * uint64_t(cpt) * 4u);
+    }
     bp->total = off;
     return W12_OK;
+}
+
+// The TMA-fed mma.sync path: one tensor map per plane and one for x per product.
+int run_stream_batch(const w12_desc *d, const void *const *blobs, const uint16_t *const *xs, int64_t M,
+                     void *const *ys, int y_dtype, int count, void *ws, const BatchPlan &bp, void *stream) {
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    StreamBatch b;
+    std::memset(&b, 0, sizeof b);
+    b.count = count;
+    b.M = int(M);
+    b.y_dtype = y_dtype;
+    b.err = reinterpret_cast<int *>(w);
+    b.U = int32_t(bp.U);
+    b.partial = reinterpret_cast<float *>(w + bp.stream_partial);
+    const int MP = 8 << (bp.variant / 2);
+    for (int i = 0; i < count; ++i) {
+        const uint8_t *bl = static_cast<const uint8_t *>(blobs[i]);
+        StreamOne &g = b.g[i];
+        const int st = stream_make_maps(g, d[i], blobs[i], xs[i], int(M), MP);
+        if (st != W12_OK) return st;
+        g.meta = reinterpret_cast<const uint32_t *>(bl + d[i].off_meta);
+        g.esc = reinterpret_cast<const uint16_t *>(bl + d[i].off_esc);
+        g.y = ys[i];
+        g.counters = reinterpret_cast<uint32_t *>(w + bp.counters[i]);
+        g.n_esc = uint32_t(d[i].n_esc);
+        g.K = int32_t(d[i].K);
+        g.N = int32_t(d[i].N);
+        g.KG = int32_t(d[i].K / kGroup);
+        g.NB = int32_t(bp.NB[i]);
+        g.ubase = int32_t(bp.ubase[i]);
+    }
+    return launch_stream_batch(b, bp.variant, bp.grid, stream);
 }
 
 // Launch a planned batch (all K_i, N_i > 0; pointers already checked).
 int run_batch(const w12_desc *d, const void *const *blobs, const uint16_t *const *xs, int64_t M,
               void *const *ys, int y_dtype, int count, void *ws, const BatchPlan &bp, void *stream) {
+    if (bp.path == W12_PATH_MMA) return run_stream_batch(d, blobs, xs, M, ys, y_dtype, count, ws, bp, stream);
     uint8_t *w = static_cast<uint8_t *>(ws);
     GemvBatch b;
     std::memset(&b, 0, sizeof b);
@@ -356,7 +401,6 @@ int run_batch(const w12_desc *d, const void *const *blobs, const uint16_t *const
     }
     switch (bp.path) {
         case W12_PATH_GEMV: return launch_gemv_batch(b, bp.variant, bp.grid, stream);
-        case W12_PATH_MMA: return launch_mma_batch(b, bp.variant, bp.grid, stream);
         case W12_PATH_TC: return launch_tc_batch(b, bp.variant, bp.grid, stream);
     }
     return W12_ERR_ARG;

@@ -97,150 +97,6 @@ __device__ __forceinline__ void tile_argmax(const GemmArgs &a, const float (&acc
     }
 }
 
-// ---------------------------------------------------------------------------
-// Stream-K, batch-native variant for plain products (no fused epilogue).
-// Work is cut into units of 128 columns x 1024 k; every CTA takes the same
-// number of consecutive units across the whole batch, and a column tile cut
-// by a CTA boundary is finished by the deterministic partial-sum fix-up.
-// x is staged per unit (in xchunk pieces when M is large).
-// ---------------------------------------------------------------------------
-constexpr int kUnitK = 1024;
-
-struct SkCur {
-    int gi, nb, ks;
-};
-
-__device__ __forceinline__ void sk_next(const GemvBatch &b, SkCur &c) {
-    if (++c.ks == b.g[c.gi].steps) {
-        c.ks = 0;
-        if (++c.nb == b.g[c.gi].NB) {
-            c.nb = 0;
-            ++c.gi;
-        }
-    }
-}
-
-__device__ __forceinline__ SkCur sk_at(const GemvBatch &b, int u) {
-    SkCur c{0, 0, 0};
-    while (c.gi + 1 < b.count && u >= b.g[c.gi + 1].ubase) ++c.gi;
-    const int local = u - b.g[c.gi].ubase;
-    c.nb = local / b.g[c.gi].steps;
-    c.ks = local % b.g[c.gi].steps;
-    return c;
-}
-
-__device__ __forceinline__ void load_a_one(const GemvOne &g, int nrow0, int k, int t, AFrag &f) {
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        const int n = nrow0 + 8 * r;
-        if (n < g.N) {
-            const uint32_t wo = uint32_t(n) * uint32_t(g.KW) + uint32_t((k + 32 * t) >> 3);
-            f.h[r] = ldg_stream(g.H + wo);
-            f.l[r] = ldg_stream(g.L + wo);
-            f.e[r] = ldg_stream(g.E + wo);
-            const uint32_t gg = uint32_t(n) * uint32_t(g.KG) + uint32_t(k >> 7);
-            f.m0[r] = ldg_u32(g.meta + gg);
-            f.m1[r] = ldg_u32(g.meta + gg + 1);
-        } else {
-            f.h[r] = f.l[r] = f.e[r] = make_uint4(0u, 0u, 0u, 0u);
-            f.m0[r] = f.m1[r] = 0u;
-        }
-    }
-}
-
-template <int NT>
-__global__ void __launch_bounds__(kThreads, NT >= 8 ? 1 : 2) mma_sk_kernel(const GemvBatch b) {
-    extern __shared__ __align__(16) unsigned char xs[];
-    __shared__ int s_last;
-    constexpr int MP = NT * 8;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g8 = lane >> 2, t = lane & 3;
-    const int xchunk = b.xchunk, pitch = xchunk * 2;
-    const int M = b.M;
-    int u0, u1;
-    {
-        const int G = int(gridDim.x), c = int(blockIdx.x);
-        const int per = b.U / G, rem = b.U % G;
-        u0 = c * per + (c < rem ? c : rem);
-        u1 = u0 + per + (c < rem ? 1 : 0);
-    }
-    if (u0 >= u1) return;
-    SkCur cc = sk_at(b, u0);
-    for (int u = u0; u < u1;) {
-        const GemvOne &g = b.g[cc.gi];
-        const int nb = cc.nb, first = g.ubase + nb * g.steps;
-        const int ua = u, ub = min(u1, first + g.steps);
-        const int nrow0 = nb * kColsPerTile + warp * 16 + g8;
-
-        float acc[NT][4];
-#pragma unroll
-        for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-
-        for (; u < ub; ++u) {
-            const int kst = cc.ks * kUnitK, kend = min(g.K, kst + kUnitK);
-            sk_next(b, cc);
-            AFrag cur, nxt;
-            load_a_one(g, nrow0, kst, t, cur);
-            for (int xb = kst; xb < kend; xb += xchunk) {
-                const int xe = min(kend, xb + xchunk);
-                const int nchunks = (xe - xb) / 8;
-                __syncthreads();  // the previous piece of x is no longer read
-                for (int i = threadIdx.x; i < MP * nchunks; i += kThreads) {
-                    const int r = i / nchunks, c = i % nchunks;
-                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                    if (r < M) v = ldg_v4(g.x + (uint32_t(r) * uint32_t(g.K) + uint32_t(xb + 8 * c)));
-                    *reinterpret_cast<uint4 *>(xs + x_chunk_offset(r, c, pitch)) = v;
-                }
-                __syncthreads();
-                for (int k = xb; k < xe; k += 128) {
-                    if (k + 128 < kend) load_a_one(g, nrow0, k + 128, t, nxt);
-                    uint32_t wa[16], wb[16];
-                    rebuild32(cur.h[0], cur.l[0], cur.e[0], base4(cur.m0[0]), wa);
-                    rebuild32(cur.h[1], cur.l[1], cur.e[1], base4(cur.m0[1]), wb);
-                    if ((cur.m0[0] >> 8) != (cur.m1[0] >> 8))
-                        patch_escapes(wa, cur.m0[0], cur.m1[0], uint32_t(32 * t), g.esc, g.n_esc, b.err);
-                    if ((cur.m0[1] >> 8) != (cur.m1[1] >> 8))
-                        patch_escapes(wb, cur.m0[1], cur.m1[1], uint32_t(32 * t), g.esc, g.n_esc, b.err);
-                    const int cbase = (k - xb) / 8 + 4 * t;
-#pragma unroll
-                    for (int sp = 0; sp < 4; ++sp) {
-#pragma unroll
-                        for (int j = 0; j < NT; ++j) {
-                            const uint4 bx = *reinterpret_cast<const uint4 *>(
-                                xs + x_chunk_offset(8 * j + g8, cbase + sp, pitch));
-                            mma_bf16(acc[j], wa[4 * sp], wb[4 * sp], wa[4 * sp + 1], wb[4 * sp + 1], bx.x, bx.y);
-                            mma_bf16(acc[j], wa[4 * sp + 2], wb[4 * sp + 2], wa[4 * sp + 3], wb[4 * sp + 3],
-                                     bx.z, bx.w);
-                        }
-                    }
-                    cur = nxt;
-                }
-            }
-        }
-
-        // C fragment: acc[j][0..1] = (row g8, tokens 8j+2t, +1), [2..3] = row g8+8.
-        const bool whole = (ua == first) && (ub == first + g.steps);
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int n = nrow0 + 8 * (q >> 1);
-                const int m = 8 * j + 2 * t + (q & 1);
-                if (n < g.N && m < M) {
-                    if (whole)
-                        store_out(g.y, b.y_dtype, g.N, m, n, acc[j][q]);
-                    else
-                        g.partial[(uint32_t(ua - g.ubase) * uint32_t(M) + uint32_t(m)) * kColsPerTile +
-                                  uint32_t(n - nb * kColsPerTile)] = acc[j][q];
-                }
-            }
-        }
-        if (!whole)
-            streamk_fixup_raw(g.counters, g.partial, first, g.ubase, g.steps, b.U, M, g.N, g.y, b.y_dtype, kColsPerTile,
-                              nb, ub - ua, &s_last, threadIdx.x, kThreads);
-    }
-}
-
 template <int NT, bool FUSED>
 __global__ void __launch_bounds__(kThreads, NT >= 8 ? 1 : 2) mma_kernel(const GemmArgs a) {
     extern __shared__ __align__(16) unsigned char xs[];
@@ -375,50 +231,7 @@ int occ_t(int *blocks, size_t smem) {
 }
 
 
-template <int NT>
-int launch_sk_t(const GemvBatch &b, int grid, cudaStream_t s) {
-    const size_t smem = size_t(NT) * 8 * size_t(b.xchunk) * 2;
-    if (smem > size_t(kMaxXSmem)) return W12_ERR_ARG;
-    mma_sk_kernel<NT><<<unsigned(grid), kThreads, smem, s>>>(b);
-    return cudaGetLastError() == cudaSuccess ? W12_OK : W12_ERR_CUDA;
-}
-
-template <int NT>
-int occ_sk_t(int *blocks, size_t smem) {
-    if (cudaFuncSetAttribute(mma_sk_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kMaxXSmem) != cudaSuccess)
-        return W12_ERR_CUDA;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, mma_sk_kernel<NT>, kThreads, smem) ==
-                   cudaSuccess
-               ? W12_OK
-               : W12_ERR_CUDA;
-}
-
 }  // namespace
-
-int launch_mma_batch(const GemvBatch &b, int variant, int grid, void *stream) {
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    switch (variant) {
-        case 0: return launch_sk_t<1>(b, grid, s);
-        case 1: return launch_sk_t<2>(b, grid, s);
-        case 2: return launch_sk_t<4>(b, grid, s);
-        case 3: return launch_sk_t<8>(b, grid, s);
-        case 4: return launch_sk_t<16>(b, grid, s);
-    }
-    return W12_ERR_ARG;
-}
-
-int mma_sk_occupancy(int variant, size_t smem, int *blocks) {
-    switch (variant) {
-        case 0: return occ_sk_t<1>(blocks, smem);
-        case 1: return occ_sk_t<2>(blocks, smem);
-        case 2: return occ_sk_t<4>(blocks, smem);
-        case 3: return occ_sk_t<8>(blocks, smem);
-        case 4: return occ_sk_t<16>(blocks, smem);
-    }
-    return W12_ERR_ARG;
-}
-
 
 // variant v: NT = 1 << v, i.e. tokens padded to 8, 16, 32, 64 or 128.
 int launch_mma(const GemmPlan &p, const GemmArgs &a, void *stream) {

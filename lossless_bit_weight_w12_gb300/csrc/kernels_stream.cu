@@ -1,0 +1,551 @@
+// kernels_stream.cu -- W12 decode-GEMM for skinny M (1 <= M <= 128) on
+// mma.sync tensor tiles, fed by the Tensor Memory Accelerator.
+//
+// A decode or verification step reads every weight once (SpecPilot summary,
+// airadar.tv English edition, first paragraph), so this kernel is a weight
+// stream first: one warp of each CTA only issues copies, eight warps only
+// rebuild and multiply, and the two meet in a ring of shared-memory stages.
+//
+//  - Work: units of one 128-k group of a 128-column tile, over every product
+//    of the batch (stream-K): CTA c takes a balanced contiguous range of
+//    units, so the busiest CTA does at most one group more than the
+//    average.  A tile cut by a CTA boundary is finished by a deterministic
+//    fix-up (partial sums added in CTA order by the CTA that completes it).
+//  - Producer warp: per unit, three 2-D tensor copies (the H, L and E plane
+//    boxes: 128 columns x 64 bytes) and one 3-D tensor copy of x (every
+//    token's 128 activations of the group, 128-byte swizzle, rows past M
+//    zero-filled), all completing on the stage's "full" barrier; 4-byte
+//    asynchronous copies of each column's meta[g], meta[g + 1] arrive on
+//    the same barrier.  At the start of every tile piece it prefetches the
+//    piece's escape entries (one contiguous range of the escape list) into
+//    L1, so the rare patch-up does not wait on HBM.
+//  - Compute warps (swap-AB, mma.m16n8k16: weights are operand A, tokens
+//    operand B): warp w owns columns 16w .. 16w + 15 of the tile; lane
+//    (g, t) rebuilds columns 16w + g and 16w + g + 8 for k = 32t .. 32t + 31
+//    of the group straight into A-fragment registers ("reconstructing bit by
+//    bit in GEMM registers", same page, "Reasons" bullet 2), patches escapes
+//    and reads the matching B fragments from the swizzled x box.  A and B
+//    agree on that k order, so no shuffle is needed.  After its last read of
+//    a stage each warp arrives on the stage's "empty" barrier.
+//  - Shared-memory reads are conflict-free: plane rows are 64 bytes (the
+//    two columns of a quarter-warp fill one 128-byte line); in the x box a
+//    token's row pair (2 r, 2 r + 1) under the 128-byte swizzle sends the 8
+//    lanes of a quarter-warp to 8 different 16-byte bank groups.
+// Every mbarrier wait is bounded (async_common.cuh): after a timeout the
+// error word says W12_ERR_TIMEOUT and all roles run to the end without
+// waiting, so the CTA still reaches its named barriers and exits.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <unordered_map>
+
+#include "async_common.cuh"
+#include "gemm_common.cuh"
+#include "stream_common.h"
+
+namespace w12 {
+
+namespace {
+
+constexpr int kCW = 8;                    // compute warps
+constexpr int kCT = kCW * 32;             // compute threads
+constexpr int kST = kCT + 32;             // + one producer warp
+constexpr int kTileN = 128;               // columns per tile
+constexpr int kPlaneBytes = kTileN * 64;  // one plane box: 128 columns x 128 k
+constexpr int kMetaBytes = kTileN * 8;    // meta[g], meta[g + 1] per column
+constexpr int kEscPrefetchLines = 64;     // escape lines prefetched per tile piece (8 KB)
+
+// Stage layout (bytes from the stage start, stages 1024-byte aligned):
+// x box (MP tokens x 2 halves x 128 bytes), H, L, E boxes, meta pairs.
+template <int NT>
+struct SCfg {
+    static constexpr int MP = 8 * NT;
+    static constexpr int kX = MP * 256;
+    static constexpr int kH = kX, kL = kX + kPlaneBytes, kE = kX + 2 * kPlaneBytes;
+    static constexpr int kMeta = kX + 3 * kPlaneBytes;
+    static constexpr int kStage = (kX + 3 * kPlaneBytes + kMetaBytes + 1023) / 1024 * 1024;
+    static constexpr uint32_t kTx = uint32_t(kX + 3 * kPlaneBytes);  // TMA bytes per stage
+};
+
+// Ring depth for NT and CTAs per SM: as many stages as fit in the 227 KB a
+// CTA may use (or half of it for two CTAs per SM), at most 8.
+constexpr int kSmemPerSm = 227 * 1024;
+template <int NT, int MINB>
+struct SRing {
+    static constexpr int kAvail = kSmemPerSm / MINB - 1024 - 2048;  // alignment slack, static smem
+    static constexpr int kFit = kAvail / SCfg<NT>::kStage;
+    static constexpr int S = kFit > 8 ? 8 : kFit;
+    static constexpr size_t kDynSmem = size_t(S) * SCfg<NT>::kStage + 1024;
+};
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+    uint2 r;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(addr));
+    return r;
+}
+
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar,
+                                       uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2,
+                                       uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// Arrive on `bar` once every earlier cp.async of this thread has landed
+// (counts as one of the barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l1(const void *p) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
+// Bounded wait that ignores the abort flag (used only to let copies that
+// are already in flight land before the CTA exits after a timeout).
+__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity) {
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > kWaitLimitNs) return;
+        __nanosleep(64);
+    }
+}
+
+// Unit cursor: product gi, column tile nb, group kg.
+struct SCur {
+    int gi, nb, kg;
+};
+
+__device__ __forceinline__ SCur s_at(const StreamBatch &b, int u) {
+    SCur c{0, 0, 0};
+    while (c.gi + 1 < b.count && u >= b.g[c.gi + 1].ubase) ++c.gi;
+    const int local = u - b.g[c.gi].ubase;
+    c.nb = local / b.g[c.gi].KG;
+    c.kg = local % b.g[c.gi].KG;
+    return c;
+}
+
+__device__ __forceinline__ void s_next_tile(const StreamBatch &b, SCur &c) {
+    c.kg = 0;
+    if (++c.nb == b.g[c.gi].NB) {
+        c.nb = 0;
+        ++c.gi;
+    }
+}
+
+__device__ __forceinline__ void s_next(const StreamBatch &b, SCur &c) {
+    if (++c.kg == b.g[c.gi].KG) s_next_tile(b, c);
+}
+
+// Stream-K fix-up.  A tile (one product, 128 columns) covers the units
+// [first, first + KG); CTA c's piece of it is stored in partial slot
+// (c, 0) if the piece starts at c's first unit, else (c, 1) (only a CTA's
+// first and last pieces can be split).  Each piece adds its unit count to
+// counters[nb]; the CTA that completes the count sums the pieces' slots in
+// CTA order (the same bits on every call), writes y and resets the counter.
+__device__ __forceinline__ void stream_fixup(const StreamBatch &b, const StreamOne &g, int first, int nb,
+                                             int count, int *s_last, int tid) {
+    __threadfence();
+    named_sync(kCT);
+    if (tid == 0) {
+        const uint32_t old = atomicAdd(&g.counters[nb], uint32_t(count));
+        *s_last = (int(old) + count == g.KG);
+    }
+    named_sync(kCT);
+    if (*s_last) {
+        __threadfence();
+        const int G = int(gridDim.x), per = b.U / G, rem = b.U % G;
+        const int c_first = sk_cta_of(first, per, rem), c_last = sk_cta_of(first + g.KG - 1, per, rem);
+        const int M = b.M;
+        const size_t slot_floats = size_t(M) * kTileN;
+        for (int o = tid; o < M * (kTileN / 4); o += kCT) {
+            const int m = o / (kTileN / 4), c4 = o % (kTileN / 4);
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int c = c_first; c <= c_last; ++c) {
+                const int slot = sk_unit_begin(c, per, rem) >= first ? 0 : 1;
+                const float4 v = __ldcg(reinterpret_cast<const float4 *>(
+                    b.partial + (size_t(c) * 2 + slot) * slot_floats + size_t(m) * kTileN) + c4);
+                if (c == c_first) {
+                    acc = v;
+                } else {
+                    acc.x += v.x;
+                    acc.y += v.y;
+                    acc.z += v.z;
+                    acc.w += v.w;
+                }
+            }
+            const int n0 = nb * kTileN + 4 * c4;
+            const float r[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (n0 + e < g.N) store_out(g.y, b.y_dtype, g.N, m, n0 + e, r[e]);
+        }
+        if (tid == 0) g.counters[nb] = 0u;
+    }
+    named_sync(kCT);  // s_last is reused by the next piece
+}
+
+template <int NT, int MINB>
+__global__ void __launch_bounds__(kST, MINB) stream_kernel(const __grid_constant__ StreamBatch b) {
+    using C = SCfg<NT>;
+    constexpr int S = SRing<NT, MINB>::S;
+    extern __shared__ unsigned char smem_dyn[];
+    __shared__ __align__(8) uint64_t full[S], empty[S];
+    __shared__ int s_abort, s_last;
+    const uint32_t base = (smem_addr(smem_dyn) + 1023u) & ~1023u;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int u0, u1;
+    {
+        const int G = int(gridDim.x), c = int(blockIdx.x);
+        const int per = b.U / G, rem = b.U % G;
+        u0 = sk_unit_begin(c, per, rem);
+        u1 = u0 + per + (c < rem ? 1 : 0);
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 32 + 1);  // 32 meta-copy arrivals + the expect_tx arrival
+            mbar_init(&empty[s], kCW);
+        }
+        s_abort = 0;
+        mbar_fence_init();
+    }
+    __syncthreads();
+    if (u0 >= u1) return;
+
+    if (warp == kCW) {
+        // ------------------------------------------------------------ producer
+        const uint64_t pol = l2_evict_first_policy();
+        SCur c = s_at(b, u0);
+        int s = 0, issued = 0;
+        uint32_t ph = 0;
+        for (int u = u0; u < u1; ++u) {
+            const StreamOne &g = b.g[c.gi];
+            if (issued >= S && !mbar_wait(&empty[s], ph ^ 1u, &s_abort, b.err)) break;
+            if (u == u0 || c.kg == 0) {
+                // escape entries of this tile piece: groups [kga, kgb) of
+                // columns n0 .. nl, one contiguous range of the list
+                const int first = g.ubase + c.nb * g.KG;
+                const int kgb = min(u1, first + g.KG) - first;
+                const int n0 = c.nb * kTileN, nl = min(g.N, n0 + kTileN) - 1;
+                uint32_t lo = 0, hi = 0;
+                if (lane == 0) {
+                    lo = ldg_u32(g.meta + (uint32_t(n0) * uint32_t(g.KG) + uint32_t(c.kg))) >> 8;
+                    hi = ldg_u32(g.meta + (uint32_t(nl) * uint32_t(g.KG) + uint32_t(kgb))) >> 8;
+                }
+                lo = __shfl_sync(0xFFFFFFFFu, lo, 0);
+                hi = min(__shfl_sync(0xFFFFFFFFu, hi, 0), g.n_esc);
+                if (lo < hi) {
+                    const uintptr_t a0 = reinterpret_cast<uintptr_t>(g.esc + lo) & ~uintptr_t(127);
+                    const uintptr_t a1 = reinterpret_cast<uintptr_t>(g.esc + hi);
+                    for (int q = lane; q < kEscPrefetchLines; q += 32) {
+                        const uintptr_t a = a0 + uintptr_t(q) * 128u;
+                        if (a < a1) prefetch_l1(reinterpret_cast<const void *>(a));
+                    }
+                }
+            }
+            const uint32_t st = base + uint32_t(s) * C::kStage;
+#pragma unroll
+            for (int q = 0; q < kTileN / 32; ++q) {
+                const int row = lane + 32 * q, n = c.nb * kTileN + row;
+                if (n < g.N) {
+                    const uint32_t gi = uint32_t(n) * uint32_t(g.KG) + uint32_t(c.kg);
+                    cp_async4(st + C::kMeta + uint32_t(row) * 8u, g.meta + gi);
+                    cp_async4(st + C::kMeta + uint32_t(row) * 8u + 4u, g.meta + gi + 1);
+                }
+            }
+            cp_async_mbar_arrive_noinc(&full[s]);
+            if (lane == 0) {
+                mbar_expect_tx(&full[s], C::kTx);
+                tma_2d(st + C::kH, &g.th, c.kg * 16, c.nb * kTileN, &full[s], pol);
+                tma_2d(st + C::kL, &g.tl, c.kg * 16, c.nb * kTileN, &full[s], pol);
+                tma_2d(st + C::kE, &g.te, c.kg * 16, c.nb * kTileN, &full[s], pol);
+                tma_3d(st, &g.tx, 0, 2 * c.kg, 0, &full[s]);
+            }
+            s_next(b, c);
+            ++issued;
+            if (++s == S) {
+                s = 0;
+                ph ^= 1u;
+            }
+        }
+        cp_async_wait<0>();
+        if (s_abort) {
+            // let the tensor copies already issued land before the CTA exits
+            for (int k = 0; k < S && k < issued; ++k) {
+                if (--s < 0) {
+                    s = S - 1;
+                    ph ^= 1u;
+                }
+                mbar_drain(&full[s], ph);
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- compute
+    const int g8 = lane >> 2, t = lane & 3;
+    const int ra = 16 * warp + g8;                       // tile column of fragment row g8
+    const uint32_t pa = uint32_t(ra * 64 + 16 * t);      // this lane's 16 bytes of row ra
+    const uint32_t pb = pa + 8u * 64u;                   // ... of row ra + 8
+    const uint32_t ma = uint32_t(ra * 8), mb = ma + 64u;
+    // x box: token r, half h at row 2r + h (128 bytes), 16-byte chunk c
+    // stored at c ^ (row & 7).  Lane t reads half t >> 1, chunks
+    // 4 (t & 1) + sp, sp = 0..3; token 8j + g8 adds j * 2048 bytes.
+    const int xr = 2 * g8 + (t >> 1);
+    const uint32_t xb0 = uint32_t(xr * 128) + (uint32_t((4 * (t & 1)) ^ (xr & 7)) << 4);
+    const int M = b.M;
+    SCur c = s_at(b, u0);
+    int s = 0;
+    uint32_t ph = 0;
+    for (int u = u0; u < u1;) {
+        const StreamOne &g = b.g[c.gi];
+        const int nb = c.nb, first = g.ubase + nb * g.KG;
+        const int ua = u, ub = min(u1, first + g.KG);
+        const int na = nb * kTileN + ra, nbb = na + 8;
+        const bool va = na < g.N, vb = nbb < g.N;
+
+        float acc[NT][4];
+#pragma unroll
+        for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+
+        for (; u < ub; ++u) {
+            mbar_wait(&full[s], ph, &s_abort, b.err);
+            const uint32_t st = base + uint32_t(s) * C::kStage;
+            const uint4 ha = lds128(st + C::kH + pa), la = lds128(st + C::kL + pa), ea = lds128(st + C::kE + pa);
+            const uint4 hb = lds128(st + C::kH + pb), lb = lds128(st + C::kL + pb), eb = lds128(st + C::kE + pb);
+            const uint2 mA = lds64(st + C::kMeta + ma), mB = lds64(st + C::kMeta + mb);
+            uint32_t wa[16], wb[16];
+            rebuild32(ha, la, ea, base4(mA.x), wa);
+            rebuild32(hb, lb, eb, base4(mB.x), wb);
+            if (va && (mA.x >> 8) != (mA.y >> 8))
+                patch_escapes(wa, mA.x, mA.y, uint32_t(32 * t), g.esc, g.n_esc, b.err);
+            if (vb && (mB.x >> 8) != (mB.y >> 8))
+                patch_escapes(wb, mB.x, mB.y, uint32_t(32 * t), g.esc, g.n_esc, b.err);
+#pragma unroll
+            for (int sp = 0; sp < 4; ++sp) {
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    const uint4 bx = lds128(st + uint32_t(j * 2048) + (xb0 ^ uint32_t(sp << 4)));
+                    mma_bf16(acc[j], wa[4 * sp], wb[4 * sp], wa[4 * sp + 1], wb[4 * sp + 1], bx.x, bx.y);
+                    mma_bf16(acc[j], wa[4 * sp + 2], wb[4 * sp + 2], wa[4 * sp + 3], wb[4 * sp + 3], bx.z, bx.w);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+            if (++s == S) {
+                s = 0;
+                ph ^= 1u;
+            }
+        }
+
+        // C fragment: acc[j][0..1] = (row g8, tokens 8j + 2t, +1), [2..3] = row g8 + 8.
+        if (ua == first && ub == first + g.KG) {
+#pragma unroll
+            for (int j = 0; j < NT; ++j)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int n = q < 2 ? na : nbb;
+                    const int m = 8 * j + 2 * t + (q & 1);
+                    if (n < g.N && m < M) store_out(g.y, b.y_dtype, g.N, m, n, acc[j][q]);
+                }
+        } else {
+            const int slot = ua == u0 ? 0 : 1;
+            float *P = b.partial + (size_t(blockIdx.x) * 2 + slot) * size_t(M) * kTileN;
+#pragma unroll
+            for (int j = 0; j < NT; ++j)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int m = 8 * j + 2 * t + (q & 1);
+                    if (m < M) P[m * kTileN + (q < 2 ? ra : ra + 8)] = acc[j][q];
+                }
+            stream_fixup(b, g, first, nb, ub - ua, &s_last, threadIdx.x);
+        }
+        s_next_tile(b, c);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, looked up once through the runtime (the
+// library does not link libcuda directly).
+EncodeTiledFn encoder() {
+    static const EncodeTiledFn fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<EncodeTiledFn>(nullptr);
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// A plane section as [N][K/8] 32-bit words; box 16 words x 128 columns.
+int plane_map(CUtensorMap *m, const void *plane, int64_t K, int64_t N) {
+    const cuuint64_t dims[2] = {cuuint64_t(K / 8), cuuint64_t(N)};
+    const cuuint64_t strides[1] = {cuuint64_t(K / 2)};
+    const cuuint32_t box[2] = {16, kTileN};
+    const cuuint32_t es[2] = {1, 1};
+    return encoder()(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(plane), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+               ? W12_OK
+               : W12_ERR_CUDA;
+}
+
+// x [M][K] bf16 as [M][K/64][64]; box 64 x 2 x MP (one group, every token),
+// 128-byte swizzle, tokens past M read as zeros.
+int x_map(CUtensorMap *m, const uint16_t *x, int64_t K, int M, int MP) {
+    const cuuint64_t dims[3] = {64, cuuint64_t(K / 64), cuuint64_t(M)};
+    const cuuint64_t strides[2] = {128, cuuint64_t(K * 2)};
+    const cuuint32_t box[3] = {64, 2, cuuint32_t(MP)};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return encoder()(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<uint16_t *>(x), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+               ? W12_OK
+               : W12_ERR_CUDA;
+}
+
+template <int NT, int MINB>
+int launch_t(const StreamBatch &b, int grid, cudaStream_t s) {
+    stream_kernel<NT, MINB><<<unsigned(grid), kST, SRing<NT, MINB>::kDynSmem, s>>>(b);
+    return cudaGetLastError() == cudaSuccess ? W12_OK : W12_ERR_CUDA;
+}
+
+template <int NT, int MINB>
+int occ_t(int *blocks) {
+    const size_t smem = SRing<NT, MINB>::kDynSmem;
+    if (cudaFuncSetAttribute(stream_kernel<NT, MINB>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
+        cudaSuccess)
+        return W12_ERR_CUDA;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, stream_kernel<NT, MINB>, kST, smem) ==
+                   cudaSuccess
+               ? W12_OK
+               : W12_ERR_CUDA;
+}
+
+}  // namespace
+
+// v = 2 * log2(NT) + (ctas_per_sm - 1); two CTAs per SM only where the
+// ring still holds three stages.
+int stream_variant_valid(int v) { return v >= 0 && v < kStreamVariants && v != 7 && v != 9; }
+
+int stream_occupancy(int v, int *blocks) {
+    switch (v) {
+        case 0: return occ_t<1, 1>(blocks);
+        case 1: return occ_t<1, 2>(blocks);
+        case 2: return occ_t<2, 1>(blocks);
+        case 3: return occ_t<2, 2>(blocks);
+        case 4: return occ_t<4, 1>(blocks);
+        case 5: return occ_t<4, 2>(blocks);
+        case 6: return occ_t<8, 1>(blocks);
+        case 8: return occ_t<16, 1>(blocks);
+    }
+    return W12_ERR_ARG;
+}
+
+namespace {
+
+// Tensor maps depend only on the address and the shape they describe, so
+// they are encoded once and reused (a batched call of six products would
+// otherwise spend tens of microseconds of host time in the encoder).
+struct MapKey {
+    uintptr_t ptr;
+    int64_t a, b, c;
+    bool operator==(const MapKey &o) const { return ptr == o.ptr && a == o.a && b == o.b && c == o.c; }
+};
+struct MapKeyHash {
+    size_t operator()(const MapKey &k) const {
+        uint64_t h = k.ptr * 0x9E3779B97F4A7C15ull;
+        h ^= uint64_t(k.a) + 0x632BE59BD9B4E019ull + (h << 6) + (h >> 2);
+        h ^= uint64_t(k.b) + 0x8CB92BA72F3D8DD7ull + (h << 6) + (h >> 2);
+        h ^= uint64_t(k.c) + 0x7F4A7C159E3779B9ull + (h << 6) + (h >> 2);
+        return size_t(h);
+    }
+};
+std::mutex g_map_mu;
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
+constexpr size_t kMaxCachedMaps = 4096;
+
+template <class Make>
+int cached_map(CUtensorMap *out, const MapKey &key, Make make) {
+    {
+        std::lock_guard<std::mutex> lock(g_map_mu);
+        auto it = g_maps.find(key);
+        if (it != g_maps.end()) {
+            *out = it->second;
+            return W12_OK;
+        }
+    }
+    const int st = make(out);
+    if (st != W12_OK) return st;
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    if (g_maps.size() >= kMaxCachedMaps) g_maps.clear();
+    g_maps.emplace(key, *out);
+    return W12_OK;
+}
+
+}  // namespace
+
+int stream_make_maps(StreamOne &g, const w12_desc &d, const void *blob, const uint16_t *x, int M, int MP) {
+    if (!encoder()) return W12_ERR_CUDA;
+    const uint8_t *bl = static_cast<const uint8_t *>(blob);
+    const int64_t K = d.K, N = d.N;
+    CUtensorMap *maps[3] = {&g.th, &g.tl, &g.te};
+    const uint64_t offs[3] = {d.off_h, d.off_l, d.off_e};
+    for (int p = 0; p < 3; ++p) {
+        const void *plane = bl + offs[p];
+        const int st = cached_map(maps[p], MapKey{reinterpret_cast<uintptr_t>(plane), K, N, -1},
+                                  [&](CUtensorMap *m) { return plane_map(m, plane, K, N); });
+        if (st != W12_OK) return st;
+    }
+    return cached_map(&g.tx, MapKey{reinterpret_cast<uintptr_t>(x), K, M, MP},
+                      [&](CUtensorMap *m) { return x_map(m, x, K, M, MP); });
+}
+
+// The dynamic shared-memory limit is raised by stream_occupancy(), which the
+// planner runs (once per device and variant) before the first launch.
+int launch_stream_batch(const StreamBatch &b, int v, int grid, void *stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    switch (v) {
+        case 0: return launch_t<1, 1>(b, grid, s);
+        case 1: return launch_t<1, 2>(b, grid, s);
+        case 2: return launch_t<2, 1>(b, grid, s);
+        case 3: return launch_t<2, 2>(b, grid, s);
+        case 4: return launch_t<4, 1>(b, grid, s);
+        case 5: return launch_t<4, 2>(b, grid, s);
+        case 6: return launch_t<8, 1>(b, grid, s);
+        case 8: return launch_t<16, 1>(b, grid, s);
+    }
+    return W12_ERR_ARG;
+}
+
+}  // namespace w12

@@ -1,0 +1,53 @@
+// stream_common.h -- argument block of the TMA-fed stream-K decode-GEMM
+// (kernels_stream.cu).  Included by CUDA translation units only (it needs
+// cuda.h for CUtensorMap).
+#pragma once
+
+#include <cuda.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "w12_internal.h"
+
+namespace w12 {
+
+// One product y = x . W of a batch.  The tensor maps describe, for the
+// Tensor Memory Accelerator, the three plane sections as 2-D arrays of
+// 32-bit words [N columns][K/8 words] (box 16 words x 128 columns: one
+// 128-k group of a 128-column tile) and x as a 3-D array
+// [M tokens][K/64][64] bf16 (box 64 x 2 x MP: one group for every token,
+// rows past M read as zeros, 128-byte swizzle).
+struct StreamOne {
+    CUtensorMap th, tl, te, tx;
+    const uint32_t *meta;  // G + 1 words
+    const uint16_t *esc;   // n_esc entries
+    void *y;               // [M][N]
+    uint32_t *counters;    // [NB] stream-K arrival counters (zero between calls)
+    uint32_t n_esc;
+    int32_t K, N, KG, NB;  // KG = K / 128 groups per column, NB = column tiles
+    int32_t ubase;         // first unit of this product
+};
+
+// A batch: units are (product, 128-column tile, 128-k group), concatenated
+// in that order; CTA c takes a balanced contiguous range of them.
+struct StreamBatch {
+    StreamOne g[kMaxBatch];
+    float *partial;  // [grid][2][M][128] partial sums of split tiles
+    int *err;        // workspace word 0
+    int count, M, y_dtype;
+    int32_t U;       // total units
+};
+
+// Kernel variants: v = 2 * log2(NT) + (ctas_per_sm - 1), NT = ceil(M / 8)
+// rounded up to a power of two (1..16).
+constexpr int kStreamVariants = 10;
+int stream_variant_valid(int v);
+int stream_occupancy(int v, int *blocks_per_sm);
+// Fills the tensor maps of b.g[i] from the blob and x pointers; returns
+// W12_ERR_CUDA if the driver's tensor-map encoder is unavailable or rejects
+// a map.
+int stream_make_maps(StreamOne &g, const w12_desc &d, const void *blob, const uint16_t *x, int M, int MP);
+int launch_stream_batch(const StreamBatch &b, int variant, int grid, void *stream);
+
+}  // namespace w12

@@ -93,10 +93,6 @@ struct GemvBatch {
     int32_t xchunk;  // MMA path: k of x staged in shared memory at a time
 };
 int launch_gemv_batch(const GemvBatch &b, int variant, int grid, void *stream);
-// The same batch description drives the stream-K tensor-core kernel
-// (units of 128 columns x 1024 k; variant = log2(ceil(M/8))).
-int launch_mma_batch(const GemvBatch &b, int variant, int grid, void *stream);
-int mma_sk_occupancy(int variant, size_t smem, int *blocks_per_sm);
 constexpr int kMmaUnitK = 1024;
 constexpr int kMmaCols = 128;
 // The tcgen05 kernel takes the same batch and units (variant = log2(MP / 16)).
