@@ -520,12 +520,26 @@ def bench_lmhead(w12, torch, dev, args, barrier):
 
 
 def run_kernel_only(args):
-    """One layer GEMM (by name) at M = args.m, eager launches: the case the
-    ncu captures under profiles/ are taken on."""
+    """One GEMM of the layer (by name), or the whole layer as one batched
+    launch ("layer"), at M = args.m with eager launches: the cases the ncu
+    captures under profiles/ are taken on."""
     import torch
     from lossless_bit_weight_w12_gb300 import build_lib, w12
     build_lib.build()
     dev = torch.device("cuda", 0)
+    if args.kernel_only == "layer":
+        layer, xs = build_layer(w12, dev, seed=1, M_list=(args.m,))
+        descs = [g["desc"] for g in layer]
+        ys = [torch.empty((args.m, g["N"]), dtype=torch.float32, device=dev) for g in layer]
+        ws = w12.workspace(w12.gemm_batched_workspace_size(descs, args.m), dev)
+        b = w12.GemmBatch(descs, [g["blob"] for g in layer], xs[args.m], ys, ws, args.path)
+        for _ in range(args.warmup):
+            b()
+        t = time_steps(torch, b, args.steps, lambda: None)
+        assert w12.get_device_error(ws) == 0
+        print(json.dumps({"kernel_only": "layer", "M": args.m, "path": args.path, "us": 1e6 * t / args.steps,
+                          "gbs": _layer_bytes() * args.steps / t / 1e9}))
+        return
     i, (name, K, N) = next((i, t) for i, t in enumerate(synth.LAYER_SHAPES) if t[0] == args.kernel_only)
     rng = synth.streams(1, len(synth.LAYER_SHAPES) + 8)
     d, blob = w12.encode(synth.weights(rng[i], K, N), w12.LAYOUT_NK)
@@ -550,7 +564,7 @@ def main():
     ap.add_argument("--impl", default="w12", choices=["w12", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-verify", dest="verify", action="store_false")
-    ap.add_argument("--kernel-only", default=None, help="time one layer GEMM by name (for ncu)")
+    ap.add_argument("--kernel-only", default=None, help="time one layer GEMM by name, or \"layer\" for the batched layer (for ncu)")
     ap.add_argument("--m", type=int, default=1, help="tokens for --kernel-only")
     ap.add_argument("--path", type=int, default=0,
                     help="--kernel-only: 0 auto, 1 GEMV, 2 mma.sync, 3 tcgen05")

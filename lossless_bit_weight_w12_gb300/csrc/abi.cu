@@ -56,8 +56,8 @@ int query_device(Device *dv) {
     return W12_OK;
 }
 
-// key: 0..15 GEMV variants, 16..31 split-K MMA variants (fused lm_head),
-// 48..63 tcgen05 variants, 64.. TMA-fed stream-K variants
+// key: 0..15 GEMV variants, 48..63 tcgen05 variants, 64..79 TMA-fed
+// stream-K variants, 80.. the same with the fused lm_head verify
 int cached_occupancy(const Device &dv, int key, size_t smem, int *blocks) {
     {
         std::lock_guard<std::mutex> lock(g_cache_mu);
@@ -69,168 +69,19 @@ int cached_occupancy(const Device &dv, int key, size_t smem, int *blocks) {
         }
     }
     const int st = key < 16   ? gemv_occupancy(key, blocks)
-                   : key < 32 ? mma_occupancy(key - 16, smem, blocks)
                    : key < 64 ? tc_occupancy(key - 48, blocks)
-                              : stream_occupancy(key - 64, blocks);
+                   : key < 80 ? stream_occupancy(key - 64, blocks)
+                              : stream_fused_occupancy(key - 80, blocks);
     if (st != W12_OK) return st;
     std::lock_guard<std::mutex> lock(g_cache_mu);
     g_cache[dv.id].occ[{key, smem}] = *blocks;
     return W12_OK;
 }
 
-// Makespan model: tiles are dealt out in contiguous balanced ranges, so the
-// busiest CTA runs ceil(T / grid) tiles of `tile_work` weights each.  A small
-// per-split charge prefers fewer splits among equal makespans.
-double makespan(int64_t T, int64_t grid, double tile_work, int nks, int64_t N, int64_t M,
-                int64_t K) {
-    const double rounds = double(ceil_div(T, grid));
-    const double split_bytes = nks > 1 ? double(nks) * double(N) * double(M) * 8.0 : 0.0;
-    const double per_cta_split = split_bytes / double(grid) / 1.5;  // in weight-equivalents
-    (void)K;
-    return rounds * tile_work + per_cta_split + 1e-3 * nks * tile_work;
-}
-
-void finish_ws_layout(GemmPlan *p, int64_t M, int64_t N, bool fused) {
-    size_t off = kWsHeader;
-    p->off_counters = off;
-    off += round256(4u * uint64_t(std::max<int64_t>(p->NB, 1)));
-    p->off_partial = off;
-    if (p->nks > 1) off += round256(uint64_t(p->nks) * uint64_t(M) * uint64_t(N) * 4u);
-    p->off_best = off;
-    if (fused) off += round256(uint64_t(p->grid) * uint64_t(M) * 8u);
-    p->off_gbuf = off;
-    if (fused) off += round256(uint64_t(M) * 4u);
-    p->ws_bytes = off;
-}
-
-// GEMV: stream-K over units of one stage (gemv_cols_per_tile() columns x
-// gemv_stage_k() k); every CTA gets the same number of units.
-// The GEMV kernel's index arithmetic is 32-bit.
+// The batched kernels' index arithmetic is 32-bit.
 bool gemv_fits_32bit(const w12_desc *d) {
     const int64_t lim = int64_t(1) << 31;
     return d->K < lim && d->N < lim && d->K / 8 * d->N < lim && d->G < lim;
-}
-
-int plan_gemv(const w12_desc *d, int64_t M, const Device &dv, GemmPlan *p) {
-    if (!gemv_fits_32bit(d)) return W12_ERR_SHAPE;
-    const int variant = M <= 1 ? 0 : M <= 2 ? 1 : 2;
-    const int64_t cpt = gemv_cols_per_tile(), sk = gemv_stage_k();
-    int occ = 0;
-    if (cached_occupancy(dv, variant, 0, &occ) != W12_OK) return W12_ERR_CUDA;
-    if (occ < 1) return W12_ERR_CUDA;
-    std::memset(p, 0, sizeof *p);
-    p->path = W12_PATH_GEMV;
-    p->variant = variant;
-    p->steps = ceil_div(d->K, sk);
-    p->NB = ceil_div(d->N, cpt);
-    p->U = p->NB * p->steps;
-    if (p->U >= (int64_t(1) << 31)) return W12_ERR_SHAPE;
-    p->grid = int(std::min<int64_t>(int64_t(dv.sms) * occ, p->U));
-    p->cols_per_tile = cpt;
-    p->nks = 1;
-    p->kchunk = sk;
-    size_t off = kWsHeader;
-    p->off_counters = off;
-    off += round256(4u * uint64_t(p->NB));
-    p->off_partial = off;
-    off += round256(uint64_t(p->U) * uint64_t(M) * uint64_t(cpt) * 4u);
-    p->off_best = p->off_gbuf = off;
-    p->ws_bytes = off;
-    return W12_OK;
-}
-
-int plan_mma(const w12_desc *d, int64_t M, const Device &dv, bool fused, GemmPlan *p) {
-    int nt = 1, v = 0;
-    while (nt * 8 < M) {
-        nt *= 2;
-        ++v;
-    }
-    const int64_t mp = 8 * nt;
-    const int64_t groups = d->K / kGroup;
-    const int64_t xmax = std::max<int64_t>(1, 32768 / mp / kGroup) * kGroup;  // 64 KB of x
-    const int64_t NB = ceil_div(d->N, 128);
-    double best = 1e300;
-    bool found = false;
-    for (int64_t nks = 1; nks <= (fused ? 1 : groups); ++nks) {
-        const int64_t cg = ceil_div(groups, nks);
-        const int64_t eff = ceil_div(groups, cg);
-        if (eff != nks) continue;
-        const int64_t kchunk = cg * kGroup;
-        const int64_t xchunk = std::min(kchunk, xmax);
-        int occ = 0;
-        if (cached_occupancy(dv, 16 + v, size_t(mp * xchunk * 2), &occ) != W12_OK) return W12_ERR_CUDA;
-        if (occ < 1) continue;
-        const int64_t grid = int64_t(dv.sms) * occ;
-        const int64_t T = NB * eff;
-        const double work = 128.0 * double(kchunk);
-        const double c = makespan(T, grid, work, int(eff), d->N, M, d->K);
-        if (c < best) {
-            best = c;
-            found = true;
-            p->path = W12_PATH_MMA;
-            p->variant = v;
-            p->grid = int(fused ? grid : std::min<int64_t>(grid, T));
-            p->NB = NB;
-            p->cols_per_tile = 128;
-            p->nks = int(eff);
-            p->kchunk = kchunk;
-            p->xchunk = xchunk;
-        }
-    }
-    if (!found) return W12_ERR_CUDA;
-    finish_ws_layout(p, M, d->N, fused);
-    return W12_OK;
-}
-
-GemmArgs make_args(const w12_desc *d, const void *blob, const uint16_t *x, int64_t M, void *y,
-                   int y_dtype, void *ws, const GemmPlan &p) {
-    const uint8_t *b = static_cast<const uint8_t *>(blob);
-    uint8_t *w = static_cast<uint8_t *>(ws);
-    GemmArgs a;
-    std::memset(&a, 0, sizeof a);
-    a.H = reinterpret_cast<const uint32_t *>(b + d->off_h);
-    a.L = reinterpret_cast<const uint32_t *>(b + d->off_l);
-    a.E = reinterpret_cast<const uint32_t *>(b + d->off_e);
-    a.meta = reinterpret_cast<const uint32_t *>(b + d->off_meta);
-    a.esc = reinterpret_cast<const uint16_t *>(b + d->off_esc);
-    a.n_esc = d->n_esc;
-    a.K = d->K;
-    a.N = d->N;
-    a.KW = d->K / 8;
-    a.KG = d->K / kGroup;
-    a.x = x;
-    a.M = int(M);
-    a.y = y;
-    a.y_dtype = y_dtype;
-    a.partial = reinterpret_cast<float *>(w + p.off_partial);
-    a.counters = reinterpret_cast<uint32_t *>(w + p.off_counters);
-    a.err = reinterpret_cast<int *>(w);
-    a.NB = p.NB;
-    a.cols_per_tile = p.cols_per_tile;
-    a.nks = p.nks;
-    a.kchunk = p.kchunk;
-    a.xchunk = p.xchunk;
-    a.T = p.path == W12_PATH_GEMV ? p.U : p.NB * p.nks;
-    a.U = p.U;
-    a.steps = p.steps;
-    return a;
-}
-
-int choose_plan(const w12_desc *d, int64_t M, int path, bool fused, GemmPlan *p) {
-    std::memset(p, 0, sizeof *p);
-    Device dv;
-    if (query_device(&dv) != W12_OK) return W12_ERR_CUDA;
-    if (path == W12_PATH_AUTO) path = (M == 1 && !fused) ? W12_PATH_GEMV : W12_PATH_MMA;
-    if (path == W12_PATH_GEMV) {
-        if (M > 4 || fused) return W12_ERR_SHAPE;
-        return plan_gemv(d, M, dv, p);
-    }
-    if (path == W12_PATH_MMA) return plan_mma(d, M, dv, fused, p);
-    return W12_ERR_ARG;
-}
-
-int launch_plan(const GemmPlan &p, const GemmArgs &a, void *stream) {
-    return p.path == W12_PATH_GEMV ? launch_gemv(p, a, stream) : launch_mma(p, a, stream);
 }
 
 int verify_plan(int64_t rows, int64_t V, int *grid, int64_t *splits, int64_t *chunk) {
@@ -334,11 +185,10 @@ int plan_batch(const w12_desc *d, int count, int64_t M, int path, BatchPlan *bp)
 }
 
 // The TMA-fed mma.sync path: one tensor map per plane and one for x per product.
-int run_stream_batch(const w12_desc *d, const void *const *blobs, const uint16_t *const *xs, int64_t M,
-                     void *const *ys, int y_dtype, int count, void *ws, const BatchPlan &bp, void *stream) {
+int fill_stream_batch(const w12_desc *d, const void *const *blobs, const uint16_t *const *xs, int64_t M,
+                      void *const *ys, int y_dtype, int count, void *ws, const BatchPlan &bp, StreamBatch *out) {
     uint8_t *w = static_cast<uint8_t *>(ws);
-    StreamBatch b;
-    std::memset(&b, 0, sizeof b);
+    StreamBatch &b = *out;
     b.count = count;
     b.M = int(M);
     b.y_dtype = y_dtype;
@@ -362,6 +212,15 @@ int run_stream_batch(const w12_desc *d, const void *const *blobs, const uint16_t
         g.NB = int32_t(bp.NB[i]);
         g.ubase = int32_t(bp.ubase[i]);
     }
+    return W12_OK;
+}
+
+int run_stream_batch(const w12_desc *d, const void *const *blobs, const uint16_t *const *xs, int64_t M,
+                     void *const *ys, int y_dtype, int count, void *ws, const BatchPlan &bp, void *stream) {
+    StreamBatch b;
+    std::memset(&b, 0, sizeof b);
+    const int st = fill_stream_batch(d, blobs, xs, M, ys, y_dtype, count, ws, bp, &b);
+    if (st != W12_OK) return st;
     return launch_stream_batch(b, bp.variant, bp.grid, stream);
 }
 
@@ -404,6 +263,35 @@ int run_batch(const w12_desc *d, const void *const *blobs, const uint16_t *const
         case W12_PATH_TC: return launch_tc_batch(b, bp.variant, bp.grid, stream);
     }
     return W12_ERR_ARG;
+}
+
+// Fused lm_head + verify: the stream-K plan of the one product, then the
+// per-CTA argmax keys, the CTA arrival counter and the greedy tokens.
+struct FusedPlan {
+    BatchPlan bp;
+    size_t off_best = 0, off_done = 0, off_gbuf = 0, total = 0;
+};
+
+int plan_fused(const w12_desc *d, int64_t M, FusedPlan *fp) {
+    BatchPlan &bp = fp->bp;
+    int st = plan_batch(d, 1, M, W12_PATH_MMA, &bp);
+    if (st != W12_OK) return st;
+    Device dv;
+    if (query_device(&dv) != W12_OK) return W12_ERR_CUDA;
+    bp.variant = stream_variant_for(M) & ~1;  // one CTA per SM
+    int occ = 0;
+    if (cached_occupancy(dv, 80 + bp.variant, 0, &occ) != W12_OK || occ < 1) return W12_ERR_CUDA;
+    bp.grid = int(std::min<int64_t>(int64_t(dv.sms) * occ, bp.U));
+    size_t off = bp.stream_partial;
+    off += round256(uint64_t(bp.grid) * 2u * uint64_t(M) * uint64_t(kMmaCols) * 4u);
+    fp->off_best = off;
+    off += round256(uint64_t(bp.grid) * uint64_t(M) * 8u);
+    fp->off_done = off;
+    off += 256;
+    fp->off_gbuf = off;
+    off += round256(uint64_t(M) * 4u);
+    fp->total = off;
+    return W12_OK;
 }
 
 }  // namespace
@@ -558,10 +446,10 @@ extern "C" int w12_verify_greedy(const void *logits, int dtype, int64_t R, int64
 }
 
 extern "C" size_t w12_verify_lmhead_workspace_size(const w12_desc *d, int64_t R, int64_t T) {
-    if (check_desc(d) != W12_OK || R < 1 || T < 1 || R * T > W12_MAX_M) return 0;
-    GemmPlan p;
-    if (choose_plan(d, R * T, W12_PATH_MMA, true, &p) != W12_OK) return 0;
-    return p.ws_bytes;
+    if (check_desc(d) != W12_OK || R < 1 || T < 1 || R * T > W12_MAX_M || d->N < 1 || d->K < kGroup) return 0;
+    FusedPlan fp;
+    if (plan_fused(d, R * T, &fp) != W12_OK) return 0;
+    return fp.total;
 }
 
 extern "C" int w12_verify_greedy_lmhead(const uint16_t *hidden, const w12_desc *d,
@@ -572,28 +460,35 @@ extern "C" int w12_verify_greedy_lmhead(const uint16_t *hidden, const w12_desc *
     int st = check_desc(d);
     if (st != W12_OK) return st;
     if (R < 1 || T < 1 || R * T > W12_MAX_M || d->N < 1 || d->K < kGroup) return W12_ERR_SHAPE;
+    if (!gemv_fits_32bit(d)) return W12_ERR_SHAPE;
     if (!hidden || !blob || !accept_len || !next_tok || (T > 1 && !draft)) return W12_ERR_ARG;
     if (!aligned(blob, 256) || !aligned(hidden, 16) || !aligned(accept_len, 4) ||
         !aligned(next_tok, 4) || (draft && !aligned(draft, 4)) ||
         (logits_out && !aligned(logits_out, 4)))
         return W12_ERR_ALIGN;
     const int64_t M = R * T;
-    GemmPlan p;
-    st = choose_plan(d, M, W12_PATH_MMA, true, &p);
+    FusedPlan fp;
+    st = plan_fused(d, M, &fp);
     if (st != W12_OK) return st;
-    if (!ws || ws_bytes < p.ws_bytes) return W12_ERR_WORKSPACE;
+    if (!ws || ws_bytes < fp.total) return W12_ERR_WORKSPACE;
     if (!aligned(ws, 256)) return W12_ERR_ALIGN;
-    GemmArgs a = make_args(d, blob, hidden, M, nullptr, W12_F32, ws, p);
     uint8_t *w = static_cast<uint8_t *>(ws);
-    a.row_best = reinterpret_cast<unsigned long long *>(w + p.off_best);
-    a.gbuf = reinterpret_cast<int32_t *>(w + p.off_gbuf);
-    a.logits_out = logits_out;
-    a.vR = R;
-    a.vT = T;
-    a.draft = draft;
-    a.accept_len = accept_len;
-    a.next_tok = next_tok;
-    return launch_mma(p, a, stream);
+    StreamBatch b;
+    std::memset(&b, 0, sizeof b);
+    const void *blobs[1] = {blob};
+    const uint16_t *xs[1] = {hidden};
+    void *ys[1] = {logits_out};
+    st = fill_stream_batch(d, blobs, xs, M, ys, W12_F32, 1, ws, fp.bp, &b);
+    if (st != W12_OK) return st;
+    b.row_best = reinterpret_cast<unsigned long long *>(w + fp.off_best);
+    b.done = reinterpret_cast<uint32_t *>(w + fp.off_done);
+    b.gbuf = reinterpret_cast<int32_t *>(w + fp.off_gbuf);
+    b.draft = draft;
+    b.accept_len = accept_len;
+    b.next_tok = next_tok;
+    b.vR = int(R);
+    b.vT = int(T);
+    return launch_stream_fused(b, fp.bp.variant, fp.bp.grid, stream);
 }
 
 extern "C" int w12_get_device_error(void *ws, int *err_host, void *stream) {

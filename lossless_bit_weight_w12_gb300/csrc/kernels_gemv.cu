@@ -313,35 +313,6 @@ int launch_gemv_batch(const GemvBatch &b, int variant, int grid, void *stream) {
     return W12_ERR_ARG;
 }
 
-// A single GEMM is a batch of one.
-int launch_gemv(const GemmPlan &p, const GemmArgs &a, void *stream) {
-    GemvBatch b;
-    b.count = 1;
-    b.M = a.M;
-    b.y_dtype = a.y_dtype;
-    b.err = a.err;
-    b.U = int32_t(p.U);
-    GemvOne &g = b.g[0];
-    g.H = a.H;
-    g.L = a.L;
-    g.E = a.E;
-    g.meta = a.meta;
-    g.esc = a.esc;
-    g.n_esc = uint32_t(a.n_esc);
-    g.K = int32_t(a.K);
-    g.N = int32_t(a.N);
-    g.KW = int32_t(a.KW);
-    g.KG = int32_t(a.KG);
-    g.steps = int32_t(p.steps);
-    g.NB = int32_t(p.NB);
-    g.ubase = 0;
-    g.x = a.x;
-    g.y = a.y;
-    g.partial = a.partial;
-    g.counters = a.counters;
-    return launch_gemv_batch(b, p.variant, p.grid, stream);
-}
-
 int gemv_occupancy(int variant, int *blocks) {
     switch (variant) {
         case 0: return occ_t<1>(blocks);

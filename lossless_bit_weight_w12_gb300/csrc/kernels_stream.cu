@@ -43,6 +43,7 @@
 #include "async_common.cuh"
 #include "gemm_common.cuh"
 #include "stream_common.h"
+#include "verify_common.cuh"
 
 namespace w12 {
 
@@ -55,6 +56,7 @@ constexpr int kTileN = 128;               // columns per tile
 constexpr int kPlaneBytes = kTileN * 64;  // one plane box: 128 columns x 128 k
 constexpr int kMetaBytes = kTileN * 8;    // meta[g], meta[g + 1] per column
 constexpr int kEscPrefetchLines = 64;     // escape lines prefetched per tile piece (8 KB)
+constexpr int kMaxM = W12_MAX_M;
 
 // Stage layout (bytes from the stage start, stages 1024-byte aligned):
 // x box (MP tokens x 2 halves x 128 bytes), H, L, E boxes, meta pairs.
@@ -164,8 +166,9 @@ __device__ __forceinline__ void s_next(const StreamBatch &b, SCur &c) {
 // first and last pieces can be split).  Each piece adds its unit count to
 // counters[nb]; the CTA that completes the count sums the pieces' slots in
 // CTA order (the same bits on every call), writes y and resets the counter.
+template <bool FUSED>
 __device__ __forceinline__ void stream_fixup(const StreamBatch &b, const StreamOne &g, int first, int nb,
-                                             int count, int *s_last, int tid) {
+                                             int count, int *s_last, int tid, unsigned long long *s_best) {
     __threadfence();
     named_sync(kCT);
     if (tid == 0) {
@@ -197,22 +200,58 @@ __device__ __forceinline__ void stream_fixup(const StreamBatch &b, const StreamO
             }
             const int n0 = nb * kTileN + 4 * c4;
             const float r[4] = {acc.x, acc.y, acc.z, acc.w};
+            unsigned long long best = 0ull;
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (n0 + e < g.N) store_out(g.y, b.y_dtype, g.N, m, n0 + e, r[e]);
+            for (int e = 0; e < 4; ++e) {
+                if (n0 + e >= g.N) continue;
+                if (!FUSED || g.y) store_out(g.y, b.y_dtype, g.N, m, n0 + e, r[e]);
+                if (FUSED) {
+                    const unsigned long long k = pack_key(r[e], uint32_t(n0 + e));
+                    best = k > best ? k : best;
+                }
+            }
+            if (FUSED && best != 0ull) atomicMax(&s_best[m], best);
         }
         if (tid == 0) g.counters[nb] = 0u;
     }
     named_sync(kCT);  // s_last is reused by the next piece
 }
 
-template <int NT, int MINB>
+// Best (value, lowest index) key per token over the columns a warp holds in
+// its C fragments, folded into the CTA's running maximum s_best (shared).
+template <int NT>
+__device__ __forceinline__ void frag_argmax(const float (&acc)[NT][4], int na, int nbb, int N, int M, int t,
+                                            int lane, unsigned long long *s_best) {
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int m = 8 * j + 2 * t + q;
+            unsigned long long best = 0ull;
+            if (na < N) best = pack_key(acc[j][q], uint32_t(na));
+            if (nbb < N) {
+                const unsigned long long k2 = pack_key(acc[j][q + 2], uint32_t(nbb));
+                best = k2 > best ? k2 : best;
+            }
+            // lanes with the same t hold the same tokens; they differ in lane bits 2..4
+#pragma unroll
+            for (int off = 4; off <= 16; off <<= 1) {
+                const unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, best, off);
+                best = o > best ? o : best;
+            }
+            if ((lane & 28) == 0 && m < M && best != 0ull) atomicMax(&s_best[m], best);
+        }
+    }
+}
+
+template <int NT, int MINB, bool FUSED>
 __global__ void __launch_bounds__(kST, MINB) stream_kernel(const __grid_constant__ StreamBatch b) {
     using C = SCfg<NT>;
     constexpr int S = SRing<NT, MINB>::S;
     extern __shared__ unsigned char smem_dyn[];
     __shared__ __align__(8) uint64_t full[S], empty[S];
     __shared__ int s_abort, s_last;
+    __shared__ unsigned long long s_best[FUSED ? kMaxM : 1];
     const uint32_t base = (smem_addr(smem_dyn) + 1023u) & ~1023u;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int u0, u1;
@@ -230,10 +269,13 @@ __global__ void __launch_bounds__(kST, MINB) stream_kernel(const __grid_constant
         s_abort = 0;
         mbar_fence_init();
     }
+    if (FUSED)
+        for (int m = threadIdx.x; m < kMaxM; m += kST) s_best[m] = 0ull;
     __syncthreads();
-    if (u0 >= u1) return;
+    if (!FUSED && u0 >= u1) return;
 
     if (warp == kCW) {
+        if (u0 >= u1) return;
         // ------------------------------------------------------------ producer
         const uint64_t pol = l2_evict_first_policy();
         SCur c = s_at(b, u0);
@@ -361,14 +403,17 @@ __global__ void __launch_bounds__(kST, MINB) stream_kernel(const __grid_constant
 
         // C fragment: acc[j][0..1] = (row g8, tokens 8j + 2t, +1), [2..3] = row g8 + 8.
         if (ua == first && ub == first + g.KG) {
+            if (!FUSED || g.y) {
 #pragma unroll
-            for (int j = 0; j < NT; ++j)
+                for (int j = 0; j < NT; ++j)
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int n = q < 2 ? na : nbb;
-                    const int m = 8 * j + 2 * t + (q & 1);
-                    if (n < g.N && m < M) store_out(g.y, b.y_dtype, g.N, m, n, acc[j][q]);
-                }
+                    for (int q = 0; q < 4; ++q) {
+                        const int n = q < 2 ? na : nbb;
+                        const int m = 8 * j + 2 * t + (q & 1);
+                        if (n < g.N && m < M) store_out(g.y, b.y_dtype, g.N, m, n, acc[j][q]);
+                    }
+            }
+            if (FUSED) frag_argmax<NT>(acc, na, nbb, g.N, M, t, lane, s_best);
         } else {
             const int slot = ua == u0 ? 0 : 1;
             float *P = b.partial + (size_t(blockIdx.x) * 2 + slot) * size_t(M) * kTileN;
@@ -379,9 +424,27 @@ __global__ void __launch_bounds__(kST, MINB) stream_kernel(const __grid_constant
                     const int m = 8 * j + 2 * t + (q & 1);
                     if (m < M) P[m * kTileN + (q < 2 ? ra : ra + 8)] = acc[j][q];
                 }
-            stream_fixup(b, g, first, nb, ub - ua, &s_last, threadIdx.x);
+            stream_fixup<FUSED>(b, g, first, nb, ub - ua, &s_last, threadIdx.x, s_best);
         }
         s_next_tile(b, c);
+    }
+
+    if (FUSED) {
+        // publish this CTA's per-token best; the last CTA to arrive folds
+        // them and runs the acceptance rule
+        const int tid = threadIdx.x;
+        named_sync(kCT);
+        for (int m = tid; m < M; m += kCT) b.row_best[size_t(blockIdx.x) * M + m] = s_best[m];
+        __threadfence();
+        named_sync(kCT);
+        if (tid == 0) s_last = (atomicAdd(b.done, 1u) == gridDim.x - 1);
+        named_sync(kCT);
+        if (s_last) {
+            __threadfence();
+            verify_from_keys(b.row_best, int64_t(gridDim.x), M, b.vR, b.vT, b.draft, b.accept_len, b.next_tok,
+                             b.gbuf, tid, kCT);
+            if (tid == 0) *b.done = 0u;
+        }
     }
 }
 
@@ -434,19 +497,19 @@ int x_map(CUtensorMap *m, const uint16_t *x, int64_t K, int M, int MP) {
                : W12_ERR_CUDA;
 }
 
-template <int NT, int MINB>
+template <int NT, int MINB, bool FUSED = false>
 int launch_t(const StreamBatch &b, int grid, cudaStream_t s) {
-    stream_kernel<NT, MINB><<<unsigned(grid), kST, SRing<NT, MINB>::kDynSmem, s>>>(b);
+    stream_kernel<NT, MINB, FUSED><<<unsigned(grid), kST, SRing<NT, MINB>::kDynSmem, s>>>(b);
     return cudaGetLastError() == cudaSuccess ? W12_OK : W12_ERR_CUDA;
 }
 
-template <int NT, int MINB>
+template <int NT, int MINB, bool FUSED = false>
 int occ_t(int *blocks) {
     const size_t smem = SRing<NT, MINB>::kDynSmem;
-    if (cudaFuncSetAttribute(stream_kernel<NT, MINB>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(stream_kernel<NT, MINB, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(smem)) != cudaSuccess)
         return W12_ERR_CUDA;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, stream_kernel<NT, MINB>, kST, smem) ==
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, stream_kernel<NT, MINB, FUSED>, kST, smem) ==
                    cudaSuccess
                ? W12_OK
                : W12_ERR_CUDA;
@@ -531,8 +594,38 @@ int stream_make_maps(StreamOne &g, const w12_desc &d, const void *blob, const ui
                       [&](CUtensorMap *m) { return x_map(m, x, K, M, MP); });
 }
 
-// The dynamic shared-memory limit is raised by stream_occupancy(), which the
-// planner runs (once per device and variant) before the first launch.
+int stream_fused_occupancy(int v, int *blocks) {
+    switch (v) {
+        case 0: return occ_t<1, 1, true>(blocks);
+        case 1: return occ_t<1, 2, true>(blocks);
+        case 2: return occ_t<2, 1, true>(blocks);
+        case 3: return occ_t<2, 2, true>(blocks);
+        case 4: return occ_t<4, 1, true>(blocks);
+        case 5: return occ_t<4, 2, true>(blocks);
+        case 6: return occ_t<8, 1, true>(blocks);
+        case 8: return occ_t<16, 1, true>(blocks);
+    }
+    return W12_ERR_ARG;
+}
+
+int launch_stream_fused(const StreamBatch &b, int v, int grid, void *stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    switch (v) {
+        case 0: return launch_t<1, 1, true>(b, grid, s);
+        case 1: return launch_t<1, 2, true>(b, grid, s);
+        case 2: return launch_t<2, 1, true>(b, grid, s);
+        case 3: return launch_t<2, 2, true>(b, grid, s);
+        case 4: return launch_t<4, 1, true>(b, grid, s);
+        case 5: return launch_t<4, 2, true>(b, grid, s);
+        case 6: return launch_t<8, 1, true>(b, grid, s);
+        case 8: return launch_t<16, 1, true>(b, grid, s);
+    }
+    return W12_ERR_ARG;
+}
+
+// The dynamic shared-memory limit is raised by stream_occupancy() (or
+// stream_fused_occupancy()), which the planner runs once per device and
+// variant before the first launch.
 int launch_stream_batch(const StreamBatch &b, int v, int grid, void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     switch (v) {

@@ -37,6 +37,14 @@ struct StreamBatch {
     int *err;        // workspace word 0
     int count, M, y_dtype;
     int32_t U;       // total units
+    // Fused greedy verify (lm_head; count == 1, y = the optional fp32
+    // logits copy or NULL): per-CTA best (value, index) keys of each row, a
+    // CTA arrival counter, and the acceptance rule's inputs and outputs.
+    unsigned long long *row_best;  // [grid][M]
+    uint32_t *done;                // zero between calls
+    const int32_t *draft;          // [vR][vT - 1]
+    int32_t *accept_len, *next_tok, *gbuf;
+    int vR, vT;
 };
 
 // Kernel variants: v = 2 * log2(NT) + (ctas_per_sm - 1), NT = ceil(M / 8)
@@ -49,5 +57,8 @@ int stream_occupancy(int v, int *blocks_per_sm);
 // a map.
 int stream_make_maps(StreamOne &g, const w12_desc &d, const void *blob, const uint16_t *x, int M, int MP);
 int launch_stream_batch(const StreamBatch &b, int variant, int grid, void *stream);
+// The fused lm_head + greedy verify variants (same v).
+int stream_fused_occupancy(int v, int *blocks_per_sm);
+int launch_stream_fused(const StreamBatch &b, int variant, int grid, void *stream);
 
 }  // namespace w12

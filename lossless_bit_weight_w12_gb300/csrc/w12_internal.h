@@ -22,53 +22,6 @@ void layout_v1(int64_t K, int64_t N, uint64_t n_esc, w12_desc *d);
 // code, counters start at byte 256, the fp32 partials after them.
 constexpr size_t kWsHeader = 256;
 
-// Kernel argument block for the GEMM paths (plain pointers, device side).
-struct GemmArgs {
-    const uint32_t *H, *L, *E;  // plane words, column-major, K/8 words per column
-    const uint32_t *meta;       // G + 1 words
-    const uint16_t *esc;        // n_esc entries
-    uint64_t n_esc;
-    int64_t K, N, KW, KG;       // KW = K/8, KG = K/128
-    const uint16_t *x;          // [M][K] bf16
-    int M;
-    void *y;                    // [M][N]
-    int y_dtype;                // W12_F32 / W12_BF16
-    float *partial;             // [nks][M][N] when nks > 1
-    uint32_t *counters;         // [NB] arrival counters when nks > 1
-    int *err;                   // workspace word 0
-    int64_t NB;                 // column tiles
-    int64_t cols_per_tile;
-    int nks;                    // k splits
-    int64_t kchunk;             // k per split (multiple of 128)
-    int64_t T;                  // NB * nks tiles
-    int64_t xchunk;             // k staged in shared memory at a time (MMA path)
-    // stream-K (GEMV path): U units of one stage each, `steps` units per tile;
-    // partial[((nb * steps + ks) * M + m) * cols_per_tile + c] zero between calls
-    int64_t U, steps;
-    // fused argmax + acceptance epilogue (lm_head verify); row_best NULL otherwise
-    unsigned long long *row_best;  // [grid][M] per-CTA best keys
-    float *logits_out;             // optional [M][N] copy of the fp32 logits
-    int64_t vR, vT;                // draft blocks: M = vR * vT
-    const int32_t *draft;          // [vR][vT-1]
-    int32_t *accept_len, *next_tok;
-    int32_t *gbuf;                 // [M] greedy tokens (scratch)
-};
-
-struct GemmPlan {
-    int path;        // W12_PATH_GEMV / W12_PATH_MMA
-    int variant;     // kernel template selector
-    int grid;
-    int64_t NB, cols_per_tile;
-    int nks;
-    int64_t kchunk, xchunk;
-    int64_t U, steps;  // stream-K (GEMV): units and units per tile
-    size_t ws_bytes;
-    // workspace offsets (bytes from the workspace start)
-    size_t off_counters, off_partial, off_best, off_gbuf;
-};
-
-int plan_gemm(const w12_desc *d, int64_t M, int path, int fused_argmax, GemmPlan *p);
-
 // Batched GEMV: up to kMaxBatch independent GEMMs with the same M in one
 // launch; stream-K runs over the concatenation of their units.
 constexpr int kMaxBatch = W12_MAX_BATCH;
@@ -102,12 +55,9 @@ int tc_occupancy(int variant, int *blocks_per_sm);
 // Launchers (return W12_OK or W12_ERR_CUDA).
 int launch_decode(const w12_desc *d, const void *blob, uint16_t *w, int layout, int *err,
                   void *stream);
-int launch_gemv(const GemmPlan &p, const GemmArgs &a, void *stream);
-int launch_mma(const GemmPlan &p, const GemmArgs &a, void *stream);
 int gemv_occupancy(int variant, int *blocks_per_sm);
 int gemv_cols_per_tile();
 int gemv_stage_k();
-int mma_occupancy(int variant, size_t smem, int *blocks_per_sm);
 int device_sm_count(int *sms);
 
 struct VerifyArgs {
