@@ -62,11 +62,15 @@ extern "C" {
 #define W12_F32 0
 #define W12_BF16 1
 
-/* GEMM paths (w12_gemm_ex). */
+/* GEMM paths (w12_gemm_ex, w12_gemm_batched_ex).  All three stream the
+ * weights with stream-K over the whole GPU.  W12_PATH_AUTO takes the mma.sync
+ * path for M <= 32 and the tcgen05 path above (the faster of the two on
+ * GB300 at each M). */
 #define W12_PATH_AUTO 0
-#define W12_PATH_GEMV 1 /* CUDA-core FFMA GEMV with warp-shuffle reduction, M <= 4 */
-#define W12_PATH_MMA 2  /* tensor-core mma tiles, M <= 128                        */
-#define W12_PATH_TC 3   /* tcgen05 tiles, accumulator in tensor memory, M <= 128   */
+#define W12_PATH_GEMV 1 /* CUDA-core bf16 FMA GEMV with warp-shuffle reduction, M <= 4   */
+#define W12_PATH_MMA 2  /* mma.sync tiles fed by tensor copies (TMA), M <= 128          */
+#define W12_PATH_TC 3   /* tcgen05: weights rebuilt into tensor memory, fp32 accumulator
+                           in tensor memory, M <= 128                                    */
 
 #define W12_MAX_M 128
 

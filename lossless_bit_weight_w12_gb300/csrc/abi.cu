@@ -104,13 +104,12 @@ size_t verify_ws(int64_t rows, int64_t splits) {
 
 // Workspace layout of a batch: header (error word), then per product its
 // stream-K counters, then the partial sums.  All paths are stream-K: the
-// GEMV (M <= 4, units of 16 columns x 1024 k, a partial slot per unit), the
-// TMA-fed mma.sync kernel (units of 128 columns x one 128-k group, two
-// partial slots per CTA) and the tcgen05 kernel (units of 128 columns x
-// 1024 k, a partial slot per unit).
+// GEMV (M <= 4, units of 16 columns x 1024 k, a partial slot per unit) and
+// the TMA-fed mma.sync and tcgen05 kernels (units of 128 columns x one
+// 128-k group, two partial slots per CTA).
 struct BatchPlan {
     int path = W12_PATH_GEMV;
-    int variant = 0, grid = 0, xchunk = 0;
+    int variant = 0, grid = 0;
     int64_t U = 0;
     size_t counters[kMaxBatch] = {}, partial[kMaxBatch] = {};
     int64_t steps[kMaxBatch] = {}, NB[kMaxBatch] = {}, ubase[kMaxBatch] = {};
@@ -135,7 +134,11 @@ int plan_batch(const w12_desc *d, int count, int64_t M, int path, BatchPlan *bp)
         if (st != W12_OK) return st;
         if (!gemv_fits_32bit(&d[i])) return W12_ERR_SHAPE;
     }
-    if (path == W12_PATH_AUTO) path = W12_PATH_MMA;
+    // Measured on the 27B-class layer (GB300, us per layer, mma.sync /
+    // tcgen05): M = 16: 94 / 120, 32: 108 / 121, 64: 161 / 125,
+    // 128: 242 / 161.  The GEMV path (M <= 4) is slower than mma.sync at
+    // M = 1 (110 vs 89) and is only taken when asked for.
+    if (path == W12_PATH_AUTO) path = M <= 32 ? W12_PATH_MMA : W12_PATH_TC;
     if (path == W12_PATH_GEMV && M > 4) return W12_ERR_SHAPE;
     if (path != W12_PATH_GEMV && path != W12_PATH_MMA && path != W12_PATH_TC) return W12_ERR_ARG;
     Device dv;
@@ -149,7 +152,7 @@ int plan_batch(const w12_desc *d, int count, int64_t M, int path, BatchPlan *bp)
         bp->variant = v;
         if (cached_occupancy(dv, 48 + v, 0, &occ) != W12_OK || occ < 1) return W12_ERR_CUDA;
         cpt = kMmaCols;
-        uk = kMmaUnitK;
+        uk = kGroup;
     } else if (path == W12_PATH_GEMV) {
         bp->variant = M <= 1 ? 0 : M <= 2 ? 1 : 2;
         if (cached_occupancy(dv, bp->variant, 0, &occ) != W12_OK || occ < 1) return W12_ERR_CUDA;
@@ -161,7 +164,7 @@ int plan_batch(const w12_desc *d, int count, int64_t M, int path, BatchPlan *bp)
         cpt = kMmaCols;
         uk = kGroup;
     }
-    const bool per_unit_slots = path != W12_PATH_MMA;
+    const bool per_unit_slots = path == W12_PATH_GEMV;
     size_t off = kWsHeader;
     for (int i = 0; i < count; ++i) {
         bp->steps[i] = ceil_div(d[i].K, uk);
@@ -195,11 +198,12 @@ int fill_stream_batch(const w12_desc *d, const void *const *blobs, const uint16_
     b.err = reinterpret_cast<int *>(w);
     b.U = int32_t(bp.U);
     b.partial = reinterpret_cast<float *>(w + bp.stream_partial);
-    const int MP = 8 << (bp.variant / 2);
+    const bool tc = bp.path == W12_PATH_TC;
+    const int MP = tc ? (16 << bp.variant) : (8 << (bp.variant / 2));
     for (int i = 0; i < count; ++i) {
         const uint8_t *bl = static_cast<const uint8_t *>(blobs[i]);
         StreamOne &g = b.g[i];
-        const int st = stream_make_maps(g, d[i], blobs[i], xs[i], int(M), MP);
+        const int st = stream_make_maps(g, d[i], blobs[i], xs[i], int(M), MP, tc);
         if (st != W12_OK) return st;
         g.meta = reinterpret_cast<const uint32_t *>(bl + d[i].off_meta);
         g.esc = reinterpret_cast<const uint16_t *>(bl + d[i].off_esc);
@@ -221,13 +225,14 @@ int run_stream_batch(const w12_desc *d, const void *const *blobs, const uint16_t
     std::memset(&b, 0, sizeof b);
     const int st = fill_stream_batch(d, blobs, xs, M, ys, y_dtype, count, ws, bp, &b);
     if (st != W12_OK) return st;
-    return launch_stream_batch(b, bp.variant, bp.grid, stream);
+    return bp.path == W12_PATH_TC ? launch_tc_batch(b, bp.variant, bp.grid, stream)
+                                  : launch_stream_batch(b, bp.variant, bp.grid, stream);
 }
 
 // Launch a planned batch (all K_i, N_i > 0; pointers already checked).
 int run_batch(const w12_desc *d, const void *const *blobs, const uint16_t *const *xs, int64_t M,
               void *const *ys, int y_dtype, int count, void *ws, const BatchPlan &bp, void *stream) {
-    if (bp.path == W12_PATH_MMA) return run_stream_batch(d, blobs, xs, M, ys, y_dtype, count, ws, bp, stream);
+    if (bp.path != W12_PATH_GEMV) return run_stream_batch(d, blobs, xs, M, ys, y_dtype, count, ws, bp, stream);
     uint8_t *w = static_cast<uint8_t *>(ws);
     GemvBatch b;
     std::memset(&b, 0, sizeof b);
@@ -236,7 +241,6 @@ int run_batch(const w12_desc *d, const void *const *blobs, const uint16_t *const
     b.y_dtype = y_dtype;
     b.err = reinterpret_cast<int *>(w);
     b.U = int32_t(bp.U);
-    b.xchunk = bp.xchunk;
     for (int i = 0; i < count; ++i) {
         const uint8_t *bl = static_cast<const uint8_t *>(blobs[i]);
         GemvOne &g = b.g[i];
@@ -258,11 +262,7 @@ int run_batch(const w12_desc *d, const void *const *blobs, const uint16_t *const
         g.partial = reinterpret_cast<float *>(w + bp.partial[i]);
         g.counters = reinterpret_cast<uint32_t *>(w + bp.counters[i]);
     }
-    switch (bp.path) {
-        case W12_PATH_GEMV: return launch_gemv_batch(b, bp.variant, bp.grid, stream);
-        case W12_PATH_TC: return launch_tc_batch(b, bp.variant, bp.grid, stream);
-    }
-    return W12_ERR_ARG;
+    return launch_gemv_batch(b, bp.variant, bp.grid, stream);
 }
 
 // Fused lm_head + verify: the stream-K plan of the one product, then the
@@ -278,7 +278,7 @@ int plan_fused(const w12_desc *d, int64_t M, FusedPlan *fp) {
     if (st != W12_OK) return st;
     Device dv;
     if (query_device(&dv) != W12_OK) return W12_ERR_CUDA;
-    bp.variant = stream_variant_for(M) & ~1;  // one CTA per SM
+    bp.variant = stream_variant_for(M);
     int occ = 0;
     if (cached_occupancy(dv, 80 + bp.variant, 0, &occ) != W12_OK || occ < 1) return W12_ERR_CUDA;
     bp.grid = int(std::min<int64_t>(int64_t(dv.sms) * occ, bp.U));

@@ -43,6 +43,7 @@
 #include "async_common.cuh"
 #include "gemm_common.cuh"
 #include "stream_common.h"
+#include "stream_device.cuh"
 #include "verify_common.cuh"
 
 namespace w12 {
@@ -52,10 +53,6 @@ namespace {
 constexpr int kCW = 8;                    // compute warps
 constexpr int kCT = kCW * 32;             // compute threads
 constexpr int kST = kCT + 32;             // + one producer warp
-constexpr int kTileN = 128;               // columns per tile
-constexpr int kPlaneBytes = kTileN * 64;  // one plane box: 128 columns x 128 k
-constexpr int kMetaBytes = kTileN * 8;    // meta[g], meta[g + 1] per column
-constexpr int kEscPrefetchLines = 64;     // escape lines prefetched per tile piece (8 KB)
 constexpr int kMaxM = W12_MAX_M;
 
 // Stage layout (bytes from the stage start, stages 1024-byte aligned):
@@ -88,133 +85,6 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1
         "{%8,%9}, {%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint2 lds64(uint32_t addr) {
-    uint2 r;
-    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(addr));
-    return r;
-}
-
-__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar,
-                                       uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_addr(bar)), "l"(policy)
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2,
-                                       uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
-        : "memory");
-}
-
-// Arrive on `bar` once every earlier cp.async of this thread has landed
-// (counts as one of the barrier's expected arrivals).
-__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t *bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
-__device__ __forceinline__ void prefetch_l1(const void *p) {
-    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
-}
-
-// Bounded wait that ignores the abort flag (used only to let copies that
-// are already in flight land before the CTA exits after a timeout).
-__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity) {
-    const uint64_t t0 = global_timer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (global_timer_ns() - t0 > kWaitLimitNs) return;
-        __nanosleep(64);
-    }
-}
-
-// Unit cursor: product gi, column tile nb, group kg.
-struct SCur {
-    int gi, nb, kg;
-};
-
-__device__ __forceinline__ SCur s_at(const StreamBatch &b, int u) {
-    SCur c{0, 0, 0};
-    while (c.gi + 1 < b.count && u >= b.g[c.gi + 1].ubase) ++c.gi;
-    const int local = u - b.g[c.gi].ubase;
-    c.nb = local / b.g[c.gi].KG;
-    c.kg = local % b.g[c.gi].KG;
-    return c;
-}
-
-__device__ __forceinline__ void s_next_tile(const StreamBatch &b, SCur &c) {
-    c.kg = 0;
-    if (++c.nb == b.g[c.gi].NB) {
-        c.nb = 0;
-        ++c.gi;
-    }
-}
-
-__device__ __forceinline__ void s_next(const StreamBatch &b, SCur &c) {
-    if (++c.kg == b.g[c.gi].KG) s_next_tile(b, c);
-}
-
-// Stream-K fix-up.  A tile (one product, 128 columns) covers the units
-// [first, first + KG); CTA c's piece of it is stored in partial slot
-// (c, 0) if the piece starts at c's first unit, else (c, 1) (only a CTA's
-// first and last pieces can be split).  Each piece adds its unit count to
-// counters[nb]; the CTA that completes the count sums the pieces' slots in
-// CTA order (the same bits on every call), writes y and resets the counter.
-template <bool FUSED>
-__device__ __forceinline__ void stream_fixup(const StreamBatch &b, const StreamOne &g, int first, int nb,
-                                             int count, int *s_last, int tid, unsigned long long *s_best) {
-    __threadfence();
-    named_sync(kCT);
-    if (tid == 0) {
-        const uint32_t old = atomicAdd(&g.counters[nb], uint32_t(count));
-        *s_last = (int(old) + count == g.KG);
-    }
-    named_sync(kCT);
-    if (*s_last) {
-        __threadfence();
-        const int G = int(gridDim.x), per = b.U / G, rem = b.U % G;
-        const int c_first = sk_cta_of(first, per, rem), c_last = sk_cta_of(first + g.KG - 1, per, rem);
-        const int M = b.M;
-        const size_t slot_floats = size_t(M) * kTileN;
-        for (int o = tid; o < M * (kTileN / 4); o += kCT) {
-            const int m = o / (kTileN / 4), c4 = o % (kTileN / 4);
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int c = c_first; c <= c_last; ++c) {
-                const int slot = sk_unit_begin(c, per, rem) >= first ? 0 : 1;
-                const float4 v = __ldcg(reinterpret_cast<const float4 *>(
-                    b.partial + (size_t(c) * 2 + slot) * slot_floats + size_t(m) * kTileN) + c4);
-                if (c == c_first) {
-                    acc = v;
-                } else {
-                    acc.x += v.x;
-                    acc.y += v.y;
-                    acc.z += v.z;
-                    acc.w += v.w;
-                }
-            }
-            const int n0 = nb * kTileN + 4 * c4;
-            const float r[4] = {acc.x, acc.y, acc.z, acc.w};
-            unsigned long long best = 0ull;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                if (n0 + e >= g.N) continue;
-                if (!FUSED || g.y) store_out(g.y, b.y_dtype, g.N, m, n0 + e, r[e]);
-                if (FUSED) {
-                    const unsigned long long k = pack_key(r[e], uint32_t(n0 + e));
-                    best = k > best ? k : best;
-                }
-            }
-            if (FUSED && best != 0ull) atomicMax(&s_best[m], best);
-        }
-        if (tid == 0) g.counters[nb] = 0u;
-    }
-    named_sync(kCT);  // s_last is reused by the next piece
 }
 
 // Best (value, lowest index) key per token over the columns a warp holds in
@@ -276,72 +146,7 @@ __global__ void __launch_bounds__(kST, MINB) stream_kernel(const __grid_constant
 
     if (warp == kCW) {
         if (u0 >= u1) return;
-        // ------------------------------------------------------------ producer
-        const uint64_t pol = l2_evict_first_policy();
-        SCur c = s_at(b, u0);
-        int s = 0, issued = 0;
-        uint32_t ph = 0;
-        for (int u = u0; u < u1; ++u) {
-            const StreamOne &g = b.g[c.gi];
-            if (issued >= S && !mbar_wait(&empty[s], ph ^ 1u, &s_abort, b.err)) break;
-            if (u == u0 || c.kg == 0) {
-                // escape entries of this tile piece: groups [kga, kgb) of
-                // columns n0 .. nl, one contiguous range of the list
-                const int first = g.ubase + c.nb * g.KG;
-                const int kgb = min(u1, first + g.KG) - first;
-                const int n0 = c.nb * kTileN, nl = min(g.N, n0 + kTileN) - 1;
-                uint32_t lo = 0, hi = 0;
-                if (lane == 0) {
-                    lo = ldg_u32(g.meta + (uint32_t(n0) * uint32_t(g.KG) + uint32_t(c.kg))) >> 8;
-                    hi = ldg_u32(g.meta + (uint32_t(nl) * uint32_t(g.KG) + uint32_t(kgb))) >> 8;
-                }
-                lo = __shfl_sync(0xFFFFFFFFu, lo, 0);
-                hi = min(__shfl_sync(0xFFFFFFFFu, hi, 0), g.n_esc);
-                if (lo < hi) {
-                    const uintptr_t a0 = reinterpret_cast<uintptr_t>(g.esc + lo) & ~uintptr_t(127);
-                    const uintptr_t a1 = reinterpret_cast<uintptr_t>(g.esc + hi);
-                    for (int q = lane; q < kEscPrefetchLines; q += 32) {
-                        const uintptr_t a = a0 + uintptr_t(q) * 128u;
-                        if (a < a1) prefetch_l1(reinterpret_cast<const void *>(a));
-                    }
-                }
-            }
-            const uint32_t st = base + uint32_t(s) * C::kStage;
-#pragma unroll
-            for (int q = 0; q < kTileN / 32; ++q) {
-                const int row = lane + 32 * q, n = c.nb * kTileN + row;
-                if (n < g.N) {
-                    const uint32_t gi = uint32_t(n) * uint32_t(g.KG) + uint32_t(c.kg);
-                    cp_async4(st + C::kMeta + uint32_t(row) * 8u, g.meta + gi);
-                    cp_async4(st + C::kMeta + uint32_t(row) * 8u + 4u, g.meta + gi + 1);
-                }
-            }
-            cp_async_mbar_arrive_noinc(&full[s]);
-            if (lane == 0) {
-                mbar_expect_tx(&full[s], C::kTx);
-                tma_2d(st + C::kH, &g.th, c.kg * 16, c.nb * kTileN, &full[s], pol);
-                tma_2d(st + C::kL, &g.tl, c.kg * 16, c.nb * kTileN, &full[s], pol);
-                tma_2d(st + C::kE, &g.te, c.kg * 16, c.nb * kTileN, &full[s], pol);
-                tma_3d(st, &g.tx, 0, 2 * c.kg, 0, &full[s]);
-            }
-            s_next(b, c);
-            ++issued;
-            if (++s == S) {
-                s = 0;
-                ph ^= 1u;
-            }
-        }
-        cp_async_wait<0>();
-        if (s_abort) {
-            // let the tensor copies already issued land before the CTA exits
-            for (int k = 0; k < S && k < issued; ++k) {
-                if (--s < 0) {
-                    s = S - 1;
-                    ph ^= 1u;
-                }
-                mbar_drain(&full[s], ph);
-            }
-        }
+        stream_producer<S, false>(b, base, C::kStage, C::kX, C::MP, full, empty, &s_abort, u0, u1, lane);
         return;
     }
 
@@ -424,7 +229,7 @@ __global__ void __launch_bounds__(kST, MINB) stream_kernel(const __grid_constant
                     const int m = 8 * j + 2 * t + (q & 1);
                     if (m < M) P[m * kTileN + (q < 2 ? ra : ra + 8)] = acc[j][q];
                 }
-            stream_fixup<FUSED>(b, g, first, nb, ub - ua, &s_last, threadIdx.x, s_best);
+            stream_fixup<FUSED>(b, g, first, nb, ub - ua, &s_last, threadIdx.x, kCT, s_best);
         }
         s_next_tile(b, c);
     }
@@ -470,27 +275,42 @@ EncodeTiledFn encoder() {
     return fn;
 }
 
-// A plane section as [N][K/8] 32-bit words; box 16 words x 128 columns.
-int plane_map(CUtensorMap *m, const void *plane, int64_t K, int64_t N) {
+// A plane section as [N][K/8] 32-bit words; box 16 words x 128 columns
+// (64 bytes per row: unswizzled, or with the 64-byte swizzle).
+int plane_map(CUtensorMap *m, const void *plane, int64_t K, int64_t N, bool swizzle64) {
     const cuuint64_t dims[2] = {cuuint64_t(K / 8), cuuint64_t(N)};
     const cuuint64_t strides[1] = {cuuint64_t(K / 2)};
     const cuuint32_t box[2] = {16, kTileN};
     const cuuint32_t es[2] = {1, 1};
     return encoder()(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(plane), dims, strides, box, es,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
                ? W12_OK
                : W12_ERR_CUDA;
 }
 
 // x [M][K] bf16 as [M][K/64][64]; box 64 x 2 x MP (one group, every token),
-// 128-byte swizzle, tokens past M read as zeros.
+// 128-byte swizzle, tokens past M read as zeros (the mma.sync kernel).
 int x_map(CUtensorMap *m, const uint16_t *x, int64_t K, int M, int MP) {
     const cuuint64_t dims[3] = {64, cuuint64_t(K / 64), cuuint64_t(M)};
     const cuuint64_t strides[2] = {128, cuuint64_t(K * 2)};
     const cuuint32_t box[3] = {64, 2, cuuint32_t(MP)};
     const cuuint32_t es[3] = {1, 1, 1};
     return encoder()(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<uint16_t *>(x), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+               ? W12_OK
+               : W12_ERR_CUDA;
+}
+
+// x [M][K] bf16 as a 2-D array; box 64 k x MP tokens, 128-byte swizzle,
+// tokens past M read as zeros (the tcgen05 kernel's B operand).
+int x_map_tc(CUtensorMap *m, const uint16_t *x, int64_t K, int M, int MP) {
+    const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(M)};
+    const cuuint64_t strides[1] = {cuuint64_t(K * 2)};
+    const cuuint32_t box[2] = {64, cuuint32_t(MP)};
+    const cuuint32_t es[2] = {1, 1};
+    return encoder()(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t *>(x), dims, strides, box, es,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
                ? W12_OK
@@ -578,7 +398,8 @@ int cached_map(CUtensorMap *out, const MapKey &key, Make make) {
 
 }  // namespace
 
-int stream_make_maps(StreamOne &g, const w12_desc &d, const void *blob, const uint16_t *x, int M, int MP) {
+int stream_make_maps(StreamOne &g, const w12_desc &d, const void *blob, const uint16_t *x, int M, int MP,
+                     bool tc) {
     if (!encoder()) return W12_ERR_CUDA;
     const uint8_t *bl = static_cast<const uint8_t *>(blob);
     const int64_t K = d.K, N = d.N;
@@ -586,10 +407,13 @@ int stream_make_maps(StreamOne &g, const w12_desc &d, const void *blob, const ui
     const uint64_t offs[3] = {d.off_h, d.off_l, d.off_e};
     for (int p = 0; p < 3; ++p) {
         const void *plane = bl + offs[p];
-        const int st = cached_map(maps[p], MapKey{reinterpret_cast<uintptr_t>(plane), K, N, -1},
-                                  [&](CUtensorMap *m) { return plane_map(m, plane, K, N); });
+        const int st = cached_map(maps[p], MapKey{reinterpret_cast<uintptr_t>(plane), K, N, tc ? -2 : -1},
+                                  [&](CUtensorMap *m) { return plane_map(m, plane, K, N, tc); });
         if (st != W12_OK) return st;
     }
+    if (tc)
+        return cached_map(&g.tx, MapKey{reinterpret_cast<uintptr_t>(x), K, M, -MP},
+                          [&](CUtensorMap *m) { return x_map_tc(m, x, K, M, MP); });
     return cached_map(&g.tx, MapKey{reinterpret_cast<uintptr_t>(x), K, M, MP},
                       [&](CUtensorMap *m) { return x_map(m, x, K, M, MP); });
 }

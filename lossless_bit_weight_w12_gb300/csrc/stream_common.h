@@ -52,13 +52,20 @@ struct StreamBatch {
 constexpr int kStreamVariants = 10;
 int stream_variant_valid(int v);
 int stream_occupancy(int v, int *blocks_per_sm);
-// Fills the tensor maps of b.g[i] from the blob and x pointers; returns
-// W12_ERR_CUDA if the driver's tensor-map encoder is unavailable or rejects
-// a map.
-int stream_make_maps(StreamOne &g, const w12_desc &d, const void *blob, const uint16_t *x, int M, int MP);
+// Fills the tensor maps of g from the blob and x pointers, for the mma.sync
+// kernel (tc = false: planes unswizzled, x as one 3-D box) or the tcgen05
+// kernel (tc = true: planes with the 64-byte swizzle, x as 2-D boxes of
+// 64 k x MP tokens with the 128-byte swizzle).  Returns W12_ERR_CUDA if the
+// driver's tensor-map encoder is unavailable or rejects a map.
+int stream_make_maps(StreamOne &g, const w12_desc &d, const void *blob, const uint16_t *x, int M, int MP,
+                     bool tc);
 int launch_stream_batch(const StreamBatch &b, int variant, int grid, void *stream);
 // The fused lm_head + greedy verify variants (same v).
 int stream_fused_occupancy(int v, int *blocks_per_sm);
 int launch_stream_fused(const StreamBatch &b, int variant, int grid, void *stream);
+// The tcgen05 kernel (kernels_tc.cu) over the same batch and units; variant
+// v: MP = 16 << v tokens.
+int launch_tc_batch(const StreamBatch &b, int variant, int grid, void *stream);
+int tc_occupancy(int variant, int *blocks_per_sm);
 
 }  // namespace w12

@@ -43,14 +43,9 @@ struct GemvBatch {
     int count, M, y_dtype;
     int *err;
     int32_t U;       // total units
-    int32_t xchunk;  // MMA path: k of x staged in shared memory at a time
 };
 int launch_gemv_batch(const GemvBatch &b, int variant, int grid, void *stream);
-constexpr int kMmaUnitK = 1024;
-constexpr int kMmaCols = 128;
-// The tcgen05 kernel takes the same batch and units (variant = log2(MP / 16)).
-int launch_tc_batch(const GemvBatch &b, int variant, int grid, void *stream);
-int tc_occupancy(int variant, int *blocks_per_sm);
+constexpr int kMmaCols = 128;  // columns per tile of the tensor-core kernels
 
 // Launchers (return W12_OK or W12_ERR_CUDA).
 int launch_decode(const w12_desc *d, const void *blob, uint16_t *w, int layout, int *err,
