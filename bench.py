@@ -452,8 +452,9 @@ def run_w12(args):
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                 "frac": achieved / hbm_peak if achieved else None,
                 "traffic": traffic_for("stream_layer_m1"),
-                "kernel": "stream_kernel<1,2> (TMA-fed mma.sync W12 decode-GEMM) over the six "
-                          "layer linears (one launch per step)",
+                "kernel": "stream_kernel<1,2,false,1>: the W12 GEMV (bulk-copied unit blocks, "
+                          "CUDA-core bf16 FMA, warp-shuffle reduction) over the six layer linears "
+                          "(one launch per step)",
                 "peak_kind": f"{peak_kind} hbm_gbs (copy)",
                 "algorithmic_bytes_per_launch": nbytes}
 

@@ -40,7 +40,7 @@
 extern "C" {
 #endif
 
-#define W12_FORMAT_VERSION 1
+#define W12_FORMAT_VERSION 2
 
 /* Status codes. */
 #define W12_OK 0
@@ -63,50 +63,69 @@ extern "C" {
 #define W12_BF16 1
 
 /* GEMM paths (w12_gemm_ex, w12_gemm_batched_ex).  All three stream the
- * weights with stream-K over the whole GPU.  W12_PATH_AUTO takes the mma.sync
- * path for M <= 32 and the tcgen05 path above (the faster of the two on
- * GB300 at each M). */
+ * weights' unit blocks with bulk copies (TMA) through a shared-memory ring,
+ * stream-K over the whole GPU; they differ in the contraction.
+ * W12_PATH_AUTO takes the GEMV at M = 1, mma.sync for M <= 32 and tcgen05
+ * above (the fastest on GB300 at each M). */
 #define W12_PATH_AUTO 0
 #define W12_PATH_GEMV 1 /* CUDA-core bf16 FMA GEMV with warp-shuffle reduction, M <= 4   */
-#define W12_PATH_MMA 2  /* mma.sync tiles fed by tensor copies (TMA), M <= 128          */
+#define W12_PATH_MMA 2  /* mma.sync tiles, M <= 128                                     */
 #define W12_PATH_TC 3   /* tcgen05: weights rebuilt into tensor memory, fp32 accumulator
                            in tensor memory, M <= 128                                    */
 
 #define W12_MAX_M 128
 
 /*
- * Descriptor of one encoded K x N matrix (format v1).
+ * Descriptor of one encoded K x N matrix (format v2).
  *
- * Logical format.  A group is 128 consecutive k of one output column n:
- * group g = n*(K/128) + k/128, pos = k % 128.  A bf16 weight has sign s
- * (bit 15), exponent e (bits 14..7) and mantissa m (bits 6..0).  Each group
- * has a base b in [0, 240]: the b whose window [b, b+14] holds the most of
- * the group's exponents, the largest such b on a tie.  A weight's exponent
- * code is c = e - b inside the window and 15 ("escape") outside it.  Escaped
- * weights get a 16-bit entry pos | e << 7 in the escape list, ordered by
- * group then pos.  meta[g] = b | first_escape_index(g) << 8, and
- * meta[G] = n_esc << 8.  Weights k and k^1 (an even k and the next) form a
- * pair; each stores its pair partner's sign.
+ * Logical format.  A group is 128 consecutive k of one output column n
+ * (pos = k % 128).  A bf16 weight has sign s (bit 15), exponent e (bits
+ * 14..7) and mantissa m (bits 6..0).  Each group has a base b in [0, 240]:
+ * the b whose window [b, b+14] holds the most of the group's exponents, the
+ * largest such b on a tie.  A weight's exponent code is c = e - b inside the
+ * window and 15 ("escape") outside it; an escaped weight gets a 16-bit entry
+ * pos | e << 7 in the escape list.  Weights k and k^1 (an even k and the
+ * next) form a pair; each stores its pair partner's sign.
  *
- * Physical format (byte offsets from the blob start; each section starts on
- * a 256-byte boundary; the blob start itself must be 256-byte aligned):
- *   H plane  at off_h:    N*K/2 bytes, nibble = SM'(k) >> 4
- *   L plane  at off_l:    N*K/2 bytes, nibble = SM'(k) & 15
- *   E plane  at off_e:    N*K/2 bytes, nibble = c(k)
- *   meta     at off_meta: (G+1) little-endian uint32
- *   escapes  at off_esc:  n_esc little-endian uint16
- * with SM'(k) = m(k) << 1 | s(k ^ 1).
- * Planes are column-major: column n owns bytes [n*K/2, (n+1)*K/2).  The
- * little-endian 32-bit word at index n*K/8 + k0/8 of a plane covers weights
- * k0..k0+7 of column n; its nibble q (bits 4q..4q+3) holds weight k0+P[q]:
- *   H: P = {4,0,5,1,6,2,7,3}   L: P = {0,5,1,6,2,7,3,4}   E: P = {0,4,1,5,2,6,3,7}
- * total_bytes covers all five sections rounded up to 256.
+ * Physical format: plane-major, 16-byte-aligned tiles.
+ *  - Columns are cut into tiles of 128 (T = ceil(N / 128) tiles; columns
+ *    past N are padding) and k into groups (KG = K / 128).  Unit
+ *    u = t * KG + kg holds group kg of the 128 columns of tile t; the blob
+ *    starts with the U = T * KG unit blocks, each W12_UNIT_BYTES long:
+ *      [0, 8192)      H plane: nibble = SM'(k) >> 4
+ *      [8192, 16384)  L plane: nibble = SM'(k) & 15
+ *      [16384, 24576) E plane: nibble = c(k)
+ *      [24576, 25092) meta: 129 little-endian uint32
+ *      [25092, 25104) zero
+ *    with SM'(k) = m(k) << 1 | s(k ^ 1).
+ *  - In a plane block, column c of the tile owns the 64-byte row
+ *    [64 c, 64 c + 64): four 16-byte chunks, chunk j holding pos
+ *    32 j .. 32 j + 31 as four little-endian 32-bit words (word q: pos
+ *    32 j + 8 q + 0..7).  Logical chunk j is stored at chunk position
+ *    j ^ ((c >> 1) & 3).  Nibble p (bits 4p..4p+3) of a word covering pos
+ *    p0..p0+7 holds the weight p0 + P[p]:
+ *      H: P = {4,0,5,1,6,2,7,3}   L: P = {0,5,1,6,2,7,3,4}   E: P = {0,4,1,5,2,6,3,7}
+ *  - Meta word c < 128 = b | first_escape_index(u, c) << 8; word 128 =
+ *    first_escape_index(u + 1, 0) << 8 (n_esc << 8 for the last unit), so
+ *    column c's escapes in unit u are entries [word c >> 8, word c+1 >> 8).
+ *    Padding columns have b = 0 and no escapes; their plane bytes are 0.
+ *  - The escape list (n_esc uint16 entries, ordered by unit, then column,
+ *    then pos) starts at off_esc, the first 256-byte boundary after the
+ *    units.  total_bytes = off_esc + 2 n_esc rounded up to 256.
+ * Every unit is one contiguous, 16-byte-aligned block (the blob itself must
+ * be 256-byte aligned on the device), so a kernel streams a unit with one
+ * bulk copy.
  */
+#define W12_UNIT_BYTES 25104
 typedef struct w12_desc {
-    uint32_t version; /* W12_FORMAT_VERSION */
-    uint32_t reserved; /* 0 */
-    int64_t K, N, G;
-    uint64_t off_h, off_l, off_e, off_meta, off_esc;
+    uint32_t version;    /* W12_FORMAT_VERSION */
+    uint32_t reserved;   /* 0 */
+    int64_t K, N, G;     /* G = N * K / 128 groups of real columns */
+    uint64_t tiles;      /* T = ceil(N / 128) */
+    uint64_t unit_bytes; /* W12_UNIT_BYTES */
+    uint64_t n_units;    /* U = T * K / 128 */
+    uint64_t off_units;  /* 0 */
+    uint64_t off_esc;
     uint64_t n_esc;
     uint64_t total_bytes;
 } w12_desc;

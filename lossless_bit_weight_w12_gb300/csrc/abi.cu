@@ -26,7 +26,7 @@ int check_desc(const w12_desc *d) {
         return W12_ERR_ARG;
     if (d->n_esc >= kMaxEscapes) return W12_ERR_BLOB;
     w12_desc want;
-    layout_v1(d->K, d->N, d->n_esc, &want);
+    layout_v2(d->K, d->N, d->n_esc, &want);
     if (std::memcmp(&want, d, sizeof want) != 0) return W12_ERR_BLOB;
     if (d->N >= (int64_t(1) << 31)) return W12_ERR_SHAPE;
     return W12_OK;
@@ -56,8 +56,8 @@ int query_device(Device *dv) {
     return W12_OK;
 }
 
-// key: 0..15 GEMV variants, 48..63 tcgen05 variants, 64..79 TMA-fed
-// stream-K variants, 80.. the same with the fused lm_head verify
+// key: 48..63 tcgen05 variants, 64..79 mma.sync stream variants, 80..95
+// the same with the fused lm_head verify, 96.. CUDA-core GEMV variants
 int cached_occupancy(const Device &dv, int key, size_t smem, int *blocks) {
     {
         std::lock_guard<std::mutex> lock(g_cache_mu);
@@ -68,10 +68,10 @@ int cached_occupancy(const Device &dv, int key, size_t smem, int *blocks) {
             return W12_OK;
         }
     }
-    const int st = key < 16   ? gemv_occupancy(key, blocks)
-                   : key < 64 ? tc_occupancy(key - 48, blocks)
+    const int st = key < 64   ? tc_occupancy(key - 48, blocks)
                    : key < 80 ? stream_occupancy(key - 64, blocks)
-                              : stream_fused_occupancy(key - 80, blocks);
+                   : key < 96 ? stream_fused_occupancy(key - 80, blocks)
+                              : stream_gemv_occupancy(key - 96, blocks);
     if (st != W12_OK) return st;
     std::lock_guard<std::mutex> lock(g_cache_mu);
     g_cache[dv.id].occ[{key, smem}] = *blocks;
@@ -103,10 +103,10 @@ size_t verify_ws(int64_t rows, int64_t splits) {
 
 
 // Workspace layout of a batch: header (error word), then per product its
-// stream-K counters, then the partial sums.  All paths are stream-K: the
-// GEMV (M <= 4, units of 16 columns x 1024 k, a partial slot per unit) and
-// the TMA-fed mma.sync and tcgen05 kernels (units of 128 columns x one
-// 128-k group, two partial slots per CTA).
+// stream-K counters, then the partial sums (two slots per CTA).  Every path
+// is the same weight stream (units of 128 columns x one 128-k group, one
+// unit block of the blob each) with different consumers: CUDA-core GEMV
+// (M <= 4), mma.sync, tcgen05.
 struct BatchPlan {
     int path = W12_PATH_GEMV;
     int variant = 0, grid = 0;
@@ -134,11 +134,12 @@ int plan_batch(const w12_desc *d, int count, int64_t M, int path, BatchPlan *bp)
         if (st != W12_OK) return st;
         if (!gemv_fits_32bit(&d[i])) return W12_ERR_SHAPE;
     }
-    // Measured on the 27B-class layer (GB300, us per layer, mma.sync /
-    // tcgen05): M = 16: 94 / 120, 32: 108 / 121, 64: 161 / 125,
-    // 128: 242 / 161.  The GEMV path (M <= 4) is slower than mma.sync at
-    // M = 1 (110 vs 89) and is only taken when asked for.
-    if (path == W12_PATH_AUTO) path = M <= 32 ? W12_PATH_MMA : W12_PATH_TC;
+    // Measured on the 27B-class layer (GB300, us per layer, GEMV / mma.sync
+    // / tcgen05): M = 1: 82.4 / 82.5 / 119, 16: - / 85.7 / 119,
+    // 32: - / 97.4 / 121, 64: - / 154 / 125, 128: - / 232 / 150.  At M = 1
+    // the weight stream is the whole cost and the CUDA-core GEMV does it
+    // with the fewest tensor instructions; tcgen05 takes over above 32.
+    if (path == W12_PATH_AUTO) path = M == 1 ? W12_PATH_GEMV : M <= 32 ? W12_PATH_MMA : W12_PATH_TC;
     if (path == W12_PATH_GEMV && M > 4) return W12_ERR_SHAPE;
     if (path != W12_PATH_GEMV && path != W12_PATH_MMA && path != W12_PATH_TC) return W12_ERR_ARG;
     Device dv;
@@ -155,16 +156,15 @@ int plan_batch(const w12_desc *d, int count, int64_t M, int path, BatchPlan *bp)
         uk = kGroup;
     } else if (path == W12_PATH_GEMV) {
         bp->variant = M <= 1 ? 0 : M <= 2 ? 1 : 2;
-        if (cached_occupancy(dv, bp->variant, 0, &occ) != W12_OK || occ < 1) return W12_ERR_CUDA;
-        cpt = gemv_cols_per_tile();
-        uk = gemv_stage_k();
+        if (cached_occupancy(dv, 96 + bp->variant, 0, &occ) != W12_OK || occ < 1) return W12_ERR_CUDA;
+        cpt = kMmaCols;
+        uk = kGroup;
     } else {
         bp->variant = stream_variant_for(M);
         if (cached_occupancy(dv, 64 + bp->variant, 0, &occ) != W12_OK || occ < 1) return W12_ERR_CUDA;
         cpt = kMmaCols;
         uk = kGroup;
     }
-    const bool per_unit_slots = path == W12_PATH_GEMV;
     size_t off = kWsHeader;
     for (int i = 0; i < count; ++i) {
         bp->steps[i] = ceil_div(d[i].K, uk);
@@ -173,16 +173,11 @@ int plan_batch(const w12_desc *d, int count, int64_t M, int path, BatchPlan *bp)
         bp->U += bp->steps[i] * bp->NB[i];
         bp->counters[i] = off;
         off += round256(4u * uint64_t(std::max<int64_t>(bp->NB[i], 1)));
-        bp->partial[i] = off;
-        if (per_unit_slots)
-            off += round256(uint64_t(bp->steps[i] * bp->NB[i]) * uint64_t(M) * uint64_t(cpt) * 4u);
     }
     if (bp->U >= (int64_t(1) << 31)) return W12_ERR_SHAPE;
     bp->grid = int(std::min<int64_t>(int64_t(dv.sms) * occ, std::max<int64_t>(bp->U, 1)));
-    if (!per_unit_slots) {
-        bp->stream_partial = off;
-        off += round256(uint64_t(bp->grid) * 2u * uint64_t(M) * uint64_t(cpt) * 4u);
-    }
+    bp->stream_partial = off;
+    off += round256(uint64_t(bp->grid) * 2u * uint64_t(M) * uint64_t(cpt) * 4u);
     bp->total = off;
     return W12_OK;
 }
@@ -199,13 +194,13 @@ int fill_stream_batch(const w12_desc *d, const void *const *blobs, const uint16_
     b.U = int32_t(bp.U);
     b.partial = reinterpret_cast<float *>(w + bp.stream_partial);
     const bool tc = bp.path == W12_PATH_TC;
-    const int MP = tc ? (16 << bp.variant) : (8 << (bp.variant / 2));
+    const int MP = tc ? (16 << bp.variant) : bp.path == W12_PATH_GEMV ? 8 : (8 << (bp.variant / 2));
     for (int i = 0; i < count; ++i) {
         const uint8_t *bl = static_cast<const uint8_t *>(blobs[i]);
         StreamOne &g = b.g[i];
-        const int st = stream_make_maps(g, d[i], blobs[i], xs[i], int(M), MP, tc);
+        const int st = stream_make_maps(g, d[i], xs[i], int(M), MP, tc);
         if (st != W12_OK) return st;
-        g.meta = reinterpret_cast<const uint32_t *>(bl + d[i].off_meta);
+        g.units = bl + d[i].off_units;
         g.esc = reinterpret_cast<const uint16_t *>(bl + d[i].off_esc);
         g.y = ys[i];
         g.counters = reinterpret_cast<uint32_t *>(w + bp.counters[i]);
@@ -225,44 +220,17 @@ int run_stream_batch(const w12_desc *d, const void *const *blobs, const uint16_t
     std::memset(&b, 0, sizeof b);
     const int st = fill_stream_batch(d, blobs, xs, M, ys, y_dtype, count, ws, bp, &b);
     if (st != W12_OK) return st;
-    return bp.path == W12_PATH_TC ? launch_tc_batch(b, bp.variant, bp.grid, stream)
-                                  : launch_stream_batch(b, bp.variant, bp.grid, stream);
+    switch (bp.path) {
+        case W12_PATH_TC: return launch_tc_batch(b, bp.variant, bp.grid, stream);
+        case W12_PATH_GEMV: return launch_stream_gemv(b, bp.variant, bp.grid, stream);
+    }
+    return launch_stream_batch(b, bp.variant, bp.grid, stream);
 }
 
 // Launch a planned batch (all K_i, N_i > 0; pointers already checked).
 int run_batch(const w12_desc *d, const void *const *blobs, const uint16_t *const *xs, int64_t M,
               void *const *ys, int y_dtype, int count, void *ws, const BatchPlan &bp, void *stream) {
-    if (bp.path != W12_PATH_GEMV) return run_stream_batch(d, blobs, xs, M, ys, y_dtype, count, ws, bp, stream);
-    uint8_t *w = static_cast<uint8_t *>(ws);
-    GemvBatch b;
-    std::memset(&b, 0, sizeof b);
-    b.count = count;
-    b.M = int(M);
-    b.y_dtype = y_dtype;
-    b.err = reinterpret_cast<int *>(w);
-    b.U = int32_t(bp.U);
-    for (int i = 0; i < count; ++i) {
-        const uint8_t *bl = static_cast<const uint8_t *>(blobs[i]);
-        GemvOne &g = b.g[i];
-        g.H = reinterpret_cast<const uint32_t *>(bl + d[i].off_h);
-        g.L = reinterpret_cast<const uint32_t *>(bl + d[i].off_l);
-        g.E = reinterpret_cast<const uint32_t *>(bl + d[i].off_e);
-        g.meta = reinterpret_cast<const uint32_t *>(bl + d[i].off_meta);
-        g.esc = reinterpret_cast<const uint16_t *>(bl + d[i].off_esc);
-        g.n_esc = uint32_t(d[i].n_esc);
-        g.K = int32_t(d[i].K);
-        g.N = int32_t(d[i].N);
-        g.KW = int32_t(d[i].K / 8);
-        g.KG = int32_t(d[i].K / kGroup);
-        g.steps = int32_t(bp.steps[i]);
-        g.NB = int32_t(bp.NB[i]);
-        g.ubase = int32_t(bp.ubase[i]);
-        g.x = xs[i];
-        g.y = ys[i];
-        g.partial = reinterpret_cast<float *>(w + bp.partial[i]);
-        g.counters = reinterpret_cast<uint32_t *>(w + bp.counters[i]);
-    }
-    return launch_gemv_batch(b, bp.variant, bp.grid, stream);
+    return run_stream_batch(d, blobs, xs, M, ys, y_dtype, count, ws, bp, stream);
 }
 
 // Fused lm_head + verify: the stream-K plan of the one product, then the

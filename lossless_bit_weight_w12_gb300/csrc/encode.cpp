@@ -1,12 +1,13 @@
-// encode.cpp -- host encoder and validator for the W12 v1 blob.
+// encode.cpp -- host encoder and validator for the W12 v2 blob.
 //
 // W12 splits each bf16 weight into three 4-bit planes (SpecPilot summary,
 // airadar.tv English edition, "Reasons" bullet 2): the high and low nibble of
 // the byte (mantissa << 1 | sign of the pair partner), and a 4-bit exponent
 // code relative to a per-group base with an escape list for exponents
-// outside the group window.  The layout is
-// the one documented in include/w12.h.  Groups are independent, so both
-// passes run OpenMP-parallel over groups.
+// outside the group window.  The layout (plane-major units of 128 columns x
+// one 128-k group, each one contiguous block with its meta words) is the one
+// documented in include/w12.h.  Groups are independent: the scan runs
+// OpenMP-parallel over groups, the packing over units.
 #include <cstring>
 #include <vector>
 
@@ -103,18 +104,17 @@ inline uint16_t load_u16(const uint8_t *p) {
 
 }  // namespace
 
-void layout_v1(int64_t K, int64_t N, uint64_t n_esc, w12_desc *d) {
-    const uint64_t plane = uint64_t(K) * uint64_t(N) / 2;
+void layout_v2(int64_t K, int64_t N, uint64_t n_esc, w12_desc *d) {
     d->version = W12_FORMAT_VERSION;
     d->reserved = 0;
     d->K = K;
     d->N = N;
     d->G = N * (K / kGroup);
-    d->off_h = 0;
-    d->off_l = round256(d->off_h + plane);
-    d->off_e = round256(d->off_l + plane);
-    d->off_meta = round256(d->off_e + plane);
-    d->off_esc = round256(d->off_meta + 4u * uint64_t(d->G + 1));
+    d->tiles = uint64_t((N + kTileCols - 1) / kTileCols);
+    d->unit_bytes = kUnitBytes;
+    d->n_units = d->tiles * uint64_t(K / kGroup);
+    d->off_units = 0;
+    d->off_esc = round256(d->n_units * kUnitBytes);
     d->n_esc = n_esc;
     d->total_bytes = round256(d->off_esc + 2u * n_esc);
 }
@@ -135,9 +135,43 @@ extern "C" int w12_encode_plan(const uint16_t *w, int64_t K, int64_t N, int layo
     uint64_t n_esc = 0;
     for (int64_t g = 0; g < G; ++g) n_esc += count[g];
     if (n_esc >= kMaxEscapes) return W12_ERR_TOO_MANY_ESCAPES;
-    layout_v1(K, N, n_esc, d);
+    layout_v2(K, N, n_esc, d);
     return W12_OK;
 }
+
+namespace w12 {
+
+namespace {
+
+// Escape begin of every (unit, tile column): running count in unit, then
+// column order (padding columns take no escapes).  begin has U * 129 + 1
+// entries; entry u * 129 + 128 is where unit u + 1 starts.
+uint64_t escape_begins(const uint32_t *count, int64_t K, int64_t N, uint64_t U, std::vector<uint64_t> &begin) {
+    const int64_t KG = K / kGroup;
+    begin.assign(size_t(U) * (kTileCols + 1) + 1, 0);
+    uint64_t run = 0;
+    for (uint64_t u = 0; u < U; ++u) {
+        const int64_t t = int64_t(u) / KG, kg = int64_t(u) % KG;
+        for (int c = 0; c < kTileCols; ++c) {
+            begin[u * (kTileCols + 1) + c] = run;
+            const int64_t n = t * kTileCols + c;
+            if (n < N) run += count[n * KG + kg];
+        }
+        begin[u * (kTileCols + 1) + kTileCols] = run;
+    }
+    return run;
+}
+
+// Byte offset, inside its unit block, of word wi (0..15) of column c of a
+// plane: 16-byte chunk wi / 4 stored at chunk position (wi / 4) ^ ((c >> 1) & 3).
+inline uint32_t word_offset(int plane, int c, int wi) {
+    const int j = (wi >> 2) ^ ((c >> 1) & 3);
+    return uint32_t(plane * kPlaneBlock + c * 64 + j * 16 + (wi & 3) * 4);
+}
+
+}  // namespace
+
+}  // namespace w12
 
 extern "C" int w12_encode(const uint16_t *w, int64_t K, int64_t N, int layout, const w12_desc *d,
                           void *blob_host) {
@@ -145,67 +179,68 @@ extern "C" int w12_encode(const uint16_t *w, int64_t K, int64_t N, int layout, c
     if (st != W12_OK) return st;
     if (!d || !blob_host || d->K != K || d->N != N || d->version != W12_FORMAT_VERSION)
         return W12_ERR_ARG;
-    const int64_t KG = K / kGroup, G = N * KG, KW = K / 8;
+    const int64_t KG = K / kGroup, G = N * KG;
     std::vector<uint8_t> base(size_t(G > 0 ? G : 1));
     std::vector<uint32_t> count(size_t(G > 0 ? G : 1));
     if (G > 0) scan_groups(w, K, N, layout, base.data(), count.data());
-    std::vector<uint64_t> begin(size_t(G + 1));
-    uint64_t run = 0;
-    for (int64_t g = 0; g < G; ++g) {
-        begin[g] = run;
-        run += count[g];
-    }
-    begin[G] = run;
     w12_desc want;
+    layout_v2(K, N, 0, &want);
+    const uint64_t U = want.n_units;
+    std::vector<uint64_t> begin;
+    const uint64_t run = escape_begins(count.data(), K, N, U, begin);
     if (run >= kMaxEscapes) return W12_ERR_TOO_MANY_ESCAPES;
-    layout_v1(K, N, run, &want);
+    layout_v2(K, N, run, &want);
     if (std::memcmp(&want, d, sizeof want) != 0) return W12_ERR_ARG;
 
     uint8_t *blob = static_cast<uint8_t *>(blob_host);
     std::memset(blob, 0, d->total_bytes);
-    uint8_t *H = blob + d->off_h, *L = blob + d->off_l, *E = blob + d->off_e;
-    uint8_t *meta = blob + d->off_meta, *esc = blob + d->off_esc;
+    uint8_t *esc = blob + d->off_esc;
 
-#pragma omp parallel for schedule(static)
-    for (int64_t g = 0; g < G; ++g) {
-        const int64_t n = g / KG, kg = g % KG;
-        uint16_t v[kGroup];
-        load_group(w, K, N, layout, n, kg, v);
-        const unsigned b = base[g];
-        store_u32(meta + 4 * g, uint32_t(b) | uint32_t(begin[g] << 8));
-        uint64_t at = begin[g];
-        for (int p = 0; p < kGroup; ++p) {
-            const unsigned e = exp_of(v[p]);
-            if (!in_window(e, b)) {
-                const uint16_t ent = uint16_t(unsigned(p) | (e << 7));
-                std::memcpy(esc + 2 * at, &ent, 2);
-                ++at;
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t u = 0; u < int64_t(U); ++u) {
+        const int64_t t = u / KG, kg = u % KG;
+        uint8_t *ub = blob + uint64_t(u) * kUnitBytes;
+        const uint64_t *bg = &begin[uint64_t(u) * (kTileCols + 1)];
+        for (int c = 0; c < kTileCols; ++c) {
+            const int64_t n = t * kTileCols + c;
+            if (n >= N) {
+                store_u32(ub + kMetaAt + 4 * c, uint32_t(bg[c] << 8));  // padding: base 0
+                continue;
+            }
+            const int64_t gid = n * KG + kg;
+            uint16_t v[kGroup];
+            load_group(w, K, N, layout, n, kg, v);
+            const unsigned b = base[gid];
+            store_u32(ub + kMetaAt + 4 * c, uint32_t(b) | uint32_t(bg[c] << 8));
+            uint64_t at = bg[c];
+            for (int p = 0; p < kGroup; ++p) {
+                const unsigned e = exp_of(v[p]);
+                if (!in_window(e, b)) {
+                    const uint16_t ent = uint16_t(unsigned(p) | (e << 7));
+                    std::memcpy(esc + 2 * at, &ent, 2);
+                    ++at;
+                }
+            }
+            for (int wi = 0; wi < kGroup / 8; ++wi) {
+                const uint16_t *q = v + 8 * wi;
+                uint32_t hw = 0, lw = 0, ew = 0;
+                for (int s = 0; s < 8; ++s) {
+                    // byte m << 1 | sign of the pair partner (weights 2i and 2i+1)
+                    const int jh = kPermH[s], jl = kPermL[s];
+                    const uint32_t smh = ((q[jh] & 0x7Fu) << 1) | (q[jh ^ 1] >> 15);
+                    const uint32_t sml = ((q[jl] & 0x7Fu) << 1) | (q[jl ^ 1] >> 15);
+                    const unsigned ee = exp_of(q[kPermE[s]]);
+                    hw |= (smh >> 4) << (4 * s);
+                    lw |= (sml & 0xFu) << (4 * s);
+                    ew |= (in_window(ee, b) ? ee - b : 15u) << (4 * s);
+                }
+                store_u32(ub + word_offset(0, c, wi), hw);
+                store_u32(ub + word_offset(1, c, wi), lw);
+                store_u32(ub + word_offset(2, c, wi), ew);
             }
         }
-        for (int wi = 0; wi < kGroup / 8; ++wi) {
-            const uint16_t *q = v + 8 * wi;
-            uint32_t hw = 0, lw = 0, ew = 0;
-            for (int s = 0; s < 8; ++s) {
-                // byte m << 1 | sign of the pair partner (weights 2i and 2i+1)
-                const int jh = kPermH[s], jl = kPermL[s];
-                const uint32_t smh = ((q[jh] & 0x7Fu) << 1) | (q[jh ^ 1] >> 15);
-                const uint32_t sml = ((q[jl] & 0x7Fu) << 1) | (q[jl ^ 1] >> 15);
-                const uint16_t ve = q[kPermE[s]];
-                const uint32_t hn = smh >> 4;
-                const uint32_t ln = sml & 0xFu;
-                const unsigned ee = exp_of(ve);
-                const uint32_t en = in_window(ee, b) ? ee - b : 15u;
-                hw |= hn << (4 * s);
-                lw |= ln << (4 * s);
-                ew |= en << (4 * s);
-            }
-            const uint64_t word = uint64_t(n) * KW + uint64_t(kg) * 16 + wi;
-            store_u32(H + 4 * word, hw);
-            store_u32(L + 4 * word, lw);
-            store_u32(E + 4 * word, ew);
-        }
+        store_u32(ub + kMetaAt + 4 * kTileCols, uint32_t(bg[kTileCols] << 8));
     }
-    store_u32(meta + 4 * G, uint32_t(run << 8));
     return W12_OK;
 }
 
@@ -215,43 +250,60 @@ extern "C" int w12_validate(const w12_desc *d, const void *blob_host) {
         return W12_ERR_ARG;
     if (d->n_esc >= kMaxEscapes) return W12_ERR_BLOB;
     w12_desc want;
-    layout_v1(d->K, d->N, d->n_esc, &want);
+    layout_v2(d->K, d->N, d->n_esc, &want);
     if (std::memcmp(&want, d, sizeof want) != 0) return W12_ERR_BLOB;
     const uint8_t *blob = static_cast<const uint8_t *>(blob_host);
-    const int64_t K = d->K, KG = K / kGroup, G = d->G, KW = K / 8;
-    const uint8_t *E = blob + d->off_e, *meta = blob + d->off_meta, *esc = blob + d->off_esc;
-    if ((load_u32(meta + 4 * G) & 0xFFu) != 0 || (load_u32(meta + 4 * G) >> 8) != d->n_esc)
-        return W12_ERR_BLOB;
+    const int64_t K = d->K, N = d->N, KG = K / kGroup;
+    const int64_t U = int64_t(d->n_units);
+    const uint8_t *esc = blob + d->off_esc;
     int bad = 0;
-#pragma omp parallel for schedule(static) reduction(| : bad)
-    for (int64_t g = 0; g < G; ++g) {
-        const uint32_t m0 = load_u32(meta + 4 * g), m1 = load_u32(meta + 4 * (g + 1));
-        const unsigned b = m0 & 0xFFu;
-        const uint64_t lo = m0 >> 8, hi = m1 >> 8;
-        if (b > unsigned(kMaxBase) || lo > hi || hi > d->n_esc) {
-            bad |= 1;
-            continue;
-        }
-        const int64_t n = g / KG, kg = g % KG;
-        // positions whose code is 15, in pos order
-        int flagged[kGroup];
-        int nf = 0;
-        for (int wi = 0; wi < kGroup / 8; ++wi) {
-            const uint32_t ew = load_u32(E + 4 * (uint64_t(n) * KW + uint64_t(kg) * 16 + wi));
-            for (int r = 0; r < 8; ++r) {
-                const int s = (r < 4) ? 2 * r : 2 * (r - 4) + 1;  // slot of weight r in E
-                if (((ew >> (4 * s)) & 0xFu) == 15u) flagged[nf++] = 8 * wi + r;
+#pragma omp parallel for schedule(dynamic, 16) reduction(| : bad)
+    for (int64_t u = 0; u < U; ++u) {
+        const int64_t t = u / KG;
+        const uint8_t *ub = blob + uint64_t(u) * kUnitBytes;
+        // the unit's word 128 is the next unit's first begin (n_esc after the last)
+        const uint32_t last = load_u32(ub + kMetaAt + 4 * kTileCols);
+        const uint64_t next = (u + 1 < U) ? (load_u32(ub + kUnitBytes + kMetaAt) >> 8) : d->n_esc;
+        if ((last & 0xFFu) != 0 || (last >> 8) != next) bad |= 1;
+        for (int z = 0; z < kUnitBytes - kMetaAt - 4 * (kTileCols + 1); ++z)
+            if (ub[kMetaAt + 4 * (kTileCols + 1) + z] != 0) bad |= 1;
+        for (int c = 0; c < kTileCols && !bad; ++c) {
+            const uint32_t m0 = load_u32(ub + kMetaAt + 4 * c), m1 = load_u32(ub + kMetaAt + 4 * (c + 1));
+            const unsigned b = m0 & 0xFFu;
+            const uint64_t lo = m0 >> 8, hi = m1 >> 8;
+            if (b > unsigned(kMaxBase) || lo > hi || hi > d->n_esc) {
+                bad |= 1;
+                break;
+            }
+            if (t * kTileCols + c >= N) {
+                // padding column: base 0, no escapes, zero planes
+                if (b != 0 || lo != hi) bad |= 1;
+                for (int plane = 0; plane < 3; ++plane)
+                    for (int i = 0; i < 64; ++i)
+                        if (ub[plane * kPlaneBlock + c * 64 + i] != 0) bad |= 1;
+                continue;
+            }
+            // positions whose code is 15, in pos order
+            int flagged[kGroup];
+            int nf = 0;
+            for (int wi = 0; wi < kGroup / 8; ++wi) {
+                const uint32_t ew = load_u32(ub + word_offset(2, c, wi));
+                for (int r = 0; r < 8; ++r) {
+                    const int s = (r < 4) ? 2 * r : 2 * (r - 4) + 1;  // slot of weight r in E
+                    if (((ew >> (4 * s)) & 0xFu) == 15u) flagged[nf++] = 8 * wi + r;
+                }
+            }
+            if (uint64_t(nf) != hi - lo) {
+                bad |= 1;
+                break;
+            }
+            for (int i = 0; i < nf; ++i) {
+                const uint16_t ent = load_u16(esc + 2 * (lo + i));
+                const unsigned pos = ent & 0x7Fu, e = (ent >> 7) & 0xFFu;
+                if ((ent >> 15) != 0 || int(pos) != flagged[i] || in_window(e, b)) bad |= 1;
             }
         }
-        if (uint64_t(nf) != hi - lo) {
-            bad |= 1;
-            continue;
-        }
-        for (int i = 0; i < nf; ++i) {
-            const uint16_t ent = load_u16(esc + 2 * (lo + i));
-            const unsigned pos = ent & 0x7Fu, e = (ent >> 7) & 0xFFu;
-            if ((ent >> 15) != 0 || int(pos) != flagged[i] || in_window(e, b)) bad |= 1;
-        }
     }
+    if (U > 0 && (load_u32(blob + kMetaAt) >> 8) != 0) bad |= 1;  // escapes start at entry 0
     return bad ? W12_ERR_BLOB : W12_OK;
 }

@@ -11,14 +11,14 @@
 //    units, so the busiest CTA does at most one group more than the
 //    average.  A tile cut by a CTA boundary is finished by a deterministic
 //    fix-up (partial sums added in CTA order by the CTA that completes it).
-//  - Producer warp: per unit, three 2-D tensor copies (the H, L and E plane
-//    boxes: 128 columns x 64 bytes) and one 3-D tensor copy of x (every
-//    token's 128 activations of the group, 128-byte swizzle, rows past M
-//    zero-filled), all completing on the stage's "full" barrier; 4-byte
-//    asynchronous copies of each column's meta[g], meta[g + 1] arrive on
-//    the same barrier.  At the start of every tile piece it prefetches the
-//    piece's escape entries (one contiguous range of the escape list) into
-//    L1, so the rare patch-up does not wait on HBM.
+//  - Producer warp: per unit, one bulk copy of the unit block (format v2:
+//    the H, L, E planes of 128 columns x 128 k and their meta words, one
+//    contiguous 25 KB block of the blob) and one 3-D tensor copy of x
+//    (every token's 128 activations of the group, 128-byte swizzle, rows
+//    past M zero-filled), both completing on the stage's "full" barrier.
+//    At the start of every tile piece it prefetches the piece's escape
+//    entries (one contiguous range of the escape list) into L1, so the rare
+//    patch-up does not wait on HBM.
 //  - Compute warps (swap-AB, mma.m16n8k16: weights are operand A, tokens
 //    operand B): warp w owns columns 16w .. 16w + 15 of the tile; lane
 //    (g, t) rebuilds columns 16w + g and 16w + g + 8 for k = 32t .. 32t + 31
@@ -28,9 +28,10 @@
 //    agree on that k order, so no shuffle is needed.  After its last read of
 //    a stage each warp arrives on the stage's "empty" barrier.
 //  - Shared-memory reads are conflict-free: plane rows are 64 bytes (the
-//    two columns of a quarter-warp fill one 128-byte line); in the x box a
-//    token's row pair (2 r, 2 r + 1) under the 128-byte swizzle sends the 8
-//    lanes of a quarter-warp to 8 different 16-byte bank groups.
+//    two columns of a quarter-warp fill one 128-byte line, their chunks
+//    permuted alike by the format's swizzle); in the x box a token's row
+//    pair (2 r, 2 r + 1) under the 128-byte swizzle sends the 8 lanes of a
+//    quarter-warp to 8 different 16-byte bank groups.
 // Every mbarrier wait is bounded (async_common.cuh): after a timeout the
 // error word says W12_ERR_TIMEOUT and all roles run to the end without
 // waiting, so the CTA still reaches its named barriers and exits.
@@ -56,15 +57,15 @@ constexpr int kST = kCT + 32;             // + one producer warp
 constexpr int kMaxM = W12_MAX_M;
 
 // Stage layout (bytes from the stage start, stages 1024-byte aligned):
-// x box (MP tokens x 2 halves x 128 bytes), H, L, E boxes, meta pairs.
+// x box (MP tokens x 2 halves x 128 bytes), then the unit block (H, L, E
+// planes, meta words).
 template <int NT>
 struct SCfg {
     static constexpr int MP = 8 * NT;
     static constexpr int kX = MP * 256;
-    static constexpr int kH = kX, kL = kX + kPlaneBytes, kE = kX + 2 * kPlaneBytes;
-    static constexpr int kMeta = kX + 3 * kPlaneBytes;
-    static constexpr int kStage = (kX + 3 * kPlaneBytes + kMetaBytes + 1023) / 1024 * 1024;
-    static constexpr uint32_t kTx = uint32_t(kX + 3 * kPlaneBytes);  // TMA bytes per stage
+    static constexpr int kH = kX, kL = kX + kPlaneBlock, kE = kX + 2 * kPlaneBlock;
+    static constexpr int kMeta = kX + kMetaAt;
+    static constexpr int kStage = (kX + kUnitBytes + 1023) / 1024 * 1024;
 };
 
 // Ring depth for NT and CTAs per SM: as many stages as fit in the 227 KB a
@@ -114,8 +115,15 @@ __device__ __forceinline__ void frag_argmax(const float (&acc)[NT][4], int na, i
     }
 }
 
-template <int NT, int MINB, bool FUSED>
+// MT = 0: mma.sync consumers (tokens padded to 8 NT).  MT = 1, 2, 4: the
+// CUDA-core GEMV consumers for M <= MT (NT = 1): lane (g, t) multiplies its
+// rebuilt weights of rows g and g + 8, k = 32t .. 32t + 31, with each
+// token's activations (fma.rn.f32.bf16 on the bf16 halves: no unpacking),
+// and the four lanes of a row are summed with two warp shuffles at the end
+// of a tile piece.
+template <int NT, int MINB, bool FUSED, int MT = 0>
 __global__ void __launch_bounds__(kST, MINB) stream_kernel(const __grid_constant__ StreamBatch b) {
+    static_assert(MT == 0 || (NT == 1 && !FUSED), "the GEMV consumers serve plain products, M <= 4");
     using C = SCfg<NT>;
     constexpr int S = SRing<NT, MINB>::S;
     extern __shared__ unsigned char smem_dyn[];
@@ -133,7 +141,7 @@ __global__ void __launch_bounds__(kST, MINB) stream_kernel(const __grid_constant
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(&full[s], 32 + 1);  // 32 meta-copy arrivals + the expect_tx arrival
+            mbar_init(&full[s], 1);  // the producer's expect_tx arrival (+ bytes)
             mbar_init(&empty[s], kCW);
         }
         s_abort = 0;
@@ -152,10 +160,12 @@ __global__ void __launch_bounds__(kST, MINB) stream_kernel(const __grid_constant
 
     // ---------------------------------------------------------------- compute
     const int g8 = lane >> 2, t = lane & 3;
-    const int ra = 16 * warp + g8;                       // tile column of fragment row g8
-    const uint32_t pa = uint32_t(ra * 64 + 16 * t);      // this lane's 16 bytes of row ra
-    const uint32_t pb = pa + 8u * 64u;                   // ... of row ra + 8
-    const uint32_t ma = uint32_t(ra * 8), mb = ma + 64u;
+    const int ra = 16 * warp + g8;  // tile column of fragment row g8
+    // this lane's 16 bytes (logical chunk t) of plane row ra, and of row
+    // ra + 8 (same swizzle, 512 bytes on)
+    const uint32_t pa = uint32_t(ra * 64 + 16 * (t ^ ((ra >> 1) & 3)));
+    const uint32_t pb = pa + 8u * 64u;
+    const uint32_t ma = uint32_t(4 * ra), mb = ma + 32u;  // meta words ra, ra + 8
     // x box: token r, half h at row 2r + h (128 bytes), 16-byte chunk c
     // stored at c ^ (row & 7).  Lane t reads half t >> 1, chunks
     // 4 (t & 1) + sp, sp = 0..3; token 8j + g8 adds j * 2048 bytes.
@@ -175,13 +185,19 @@ __global__ void __launch_bounds__(kST, MINB) stream_kernel(const __grid_constant
         float acc[NT][4];
 #pragma unroll
         for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+        float fa[MT > 0 ? MT : 1][2][2], fb[MT > 0 ? MT : 1][2][2];  // [token][lo/hi][chain]
+#pragma unroll
+        for (int m = 0; m < (MT > 0 ? MT : 1); ++m)
+#pragma unroll
+            for (int q = 0; q < 2; ++q) fa[m][q][0] = fa[m][q][1] = fb[m][q][0] = fb[m][q][1] = 0.f;
 
         for (; u < ub; ++u) {
             mbar_wait(&full[s], ph, &s_abort, b.err);
             const uint32_t st = base + uint32_t(s) * C::kStage;
             const uint4 ha = lds128(st + C::kH + pa), la = lds128(st + C::kL + pa), ea = lds128(st + C::kE + pa);
             const uint4 hb = lds128(st + C::kH + pb), lb = lds128(st + C::kL + pb), eb = lds128(st + C::kE + pb);
-            const uint2 mA = lds64(st + C::kMeta + ma), mB = lds64(st + C::kMeta + mb);
+            const uint2 mA = make_uint2(lds32(st + C::kMeta + ma), lds32(st + C::kMeta + ma + 4u));
+            const uint2 mB = make_uint2(lds32(st + C::kMeta + mb), lds32(st + C::kMeta + mb + 4u));
             uint32_t wa[16], wb[16];
             rebuild32(ha, la, ea, base4(mA.x), wa);
             rebuild32(hb, lb, eb, base4(mB.x), wb);
@@ -189,13 +205,35 @@ __global__ void __launch_bounds__(kST, MINB) stream_kernel(const __grid_constant
                 patch_escapes(wa, mA.x, mA.y, uint32_t(32 * t), g.esc, g.n_esc, b.err);
             if (vb && (mB.x >> 8) != (mB.y >> 8))
                 patch_escapes(wb, mB.x, mB.y, uint32_t(32 * t), g.esc, g.n_esc, b.err);
+            if (MT == 0) {
 #pragma unroll
-            for (int sp = 0; sp < 4; ++sp) {
+                for (int sp = 0; sp < 4; ++sp) {
 #pragma unroll
-                for (int j = 0; j < NT; ++j) {
-                    const uint4 bx = lds128(st + uint32_t(j * 2048) + (xb0 ^ uint32_t(sp << 4)));
-                    mma_bf16(acc[j], wa[4 * sp], wb[4 * sp], wa[4 * sp + 1], wb[4 * sp + 1], bx.x, bx.y);
-                    mma_bf16(acc[j], wa[4 * sp + 2], wb[4 * sp + 2], wa[4 * sp + 3], wb[4 * sp + 3], bx.z, bx.w);
+                    for (int j = 0; j < NT; ++j) {
+                        const uint4 bx = lds128(st + uint32_t(j * 2048) + (xb0 ^ uint32_t(sp << 4)));
+                        mma_bf16(acc[j], wa[4 * sp], wb[4 * sp], wa[4 * sp + 1], wb[4 * sp + 1], bx.x, bx.y);
+                        mma_bf16(acc[j], wa[4 * sp + 2], wb[4 * sp + 2], wa[4 * sp + 3], wb[4 * sp + 3], bx.z,
+                                 bx.w);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int m = 0; m < (MT > 0 ? MT : 1); ++m) {
+                    if (m >= M) break;
+                    // token m, half t >> 1 at x-box row 2m + (t >> 1)
+                    const int xrm = 2 * m + (t >> 1);
+                    const uint32_t xm = uint32_t(xrm * 128);
+#pragma unroll
+                    for (int sp = 0; sp < 4; ++sp) {
+                        const uint4 bx =
+                            lds128(st + xm + (uint32_t((4 * (t & 1) + sp) ^ (xrm & 7)) << 4));
+                        const uint32_t xv[4] = {bx.x, bx.y, bx.z, bx.w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            fma_bf16x2(fa[m][0][q & 1], fa[m][1][q & 1], wa[4 * sp + q], xv[q]);
+                            fma_bf16x2(fb[m][0][q & 1], fb[m][1][q & 1], wb[4 * sp + q], xv[q]);
+                        }
+                    }
                 }
             }
             __syncwarp();
@@ -204,6 +242,48 @@ __global__ void __launch_bounds__(kST, MINB) stream_kernel(const __grid_constant
                 s = 0;
                 ph ^= 1u;
             }
+        }
+
+        if (MT > 0) {
+            // GEMV: fold the lane's chains, then the four lanes t of each row
+            // (lanes g8 * 4 + t); lane t == 0 ends with the row sums, which
+            // are placed where the mma epilogue expects token 0 (acc[0][0] for
+            // row g8, acc[0][2] for row g8 + 8) and tokens 1.. in a side array.
+#pragma unroll
+            for (int m = 0; m < (MT > 0 ? MT : 1); ++m) {
+                float va2 = (fa[m][0][0] + fa[m][1][0]) + (fa[m][0][1] + fa[m][1][1]);
+                float vb2 = (fb[m][0][0] + fb[m][1][0]) + (fb[m][0][1] + fb[m][1][1]);
+                va2 += __shfl_xor_sync(0xFFFFFFFFu, va2, 1);
+                vb2 += __shfl_xor_sync(0xFFFFFFFFu, vb2, 1);
+                va2 += __shfl_xor_sync(0xFFFFFFFFu, va2, 2);
+                vb2 += __shfl_xor_sync(0xFFFFFFFFu, vb2, 2);
+                fa[m][0][0] = va2;
+                fb[m][0][0] = vb2;
+            }
+            if (ua == first && ub == first + g.KG) {
+                if (t == 0) {
+#pragma unroll
+                    for (int m = 0; m < (MT > 0 ? MT : 1); ++m) {
+                        if (m >= M) break;
+                        if (na < g.N) store_out(g.y, b.y_dtype, g.N, m, na, fa[m][0][0]);
+                        if (nbb < g.N) store_out(g.y, b.y_dtype, g.N, m, nbb, fb[m][0][0]);
+                    }
+                }
+            } else {
+                const int slot = ua == u0 ? 0 : 1;
+                float *P = b.partial + (size_t(blockIdx.x) * 2 + slot) * size_t(M) * kTileN;
+                if (t == 0) {
+#pragma unroll
+                    for (int m = 0; m < (MT > 0 ? MT : 1); ++m) {
+                        if (m >= M) break;
+                        P[m * kTileN + ra] = fa[m][0][0];
+                        P[m * kTileN + ra + 8] = fb[m][0][0];
+                    }
+                }
+                stream_fixup<false>(b, g, first, nb, ub - ua, &s_last, threadIdx.x, kCT, s_best);
+            }
+            s_next_tile(b, c);
+            continue;
         }
 
         // C fragment: acc[j][0..1] = (row g8, tokens 8j + 2t, +1), [2..3] = row g8 + 8.
@@ -275,20 +355,6 @@ EncodeTiledFn encoder() {
     return fn;
 }
 
-// A plane section as [N][K/8] 32-bit words; box 16 words x 128 columns
-// (64 bytes per row: unswizzled, or with the 64-byte swizzle).
-int plane_map(CUtensorMap *m, const void *plane, int64_t K, int64_t N, bool swizzle64) {
-    const cuuint64_t dims[2] = {cuuint64_t(K / 8), cuuint64_t(N)};
-    const cuuint64_t strides[1] = {cuuint64_t(K / 2)};
-    const cuuint32_t box[2] = {16, kTileN};
-    const cuuint32_t es[2] = {1, 1};
-    return encoder()(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(plane), dims, strides, box, es,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
-               ? W12_OK
-               : W12_ERR_CUDA;
-}
-
 // x [M][K] bf16 as [M][K/64][64]; box 64 x 2 x MP (one group, every token),
 // 128-byte swizzle, tokens past M read as zeros (the mma.sync kernel).
 int x_map(CUtensorMap *m, const uint16_t *x, int64_t K, int M, int MP) {
@@ -317,19 +383,19 @@ int x_map_tc(CUtensorMap *m, const uint16_t *x, int64_t K, int M, int MP) {
                : W12_ERR_CUDA;
 }
 
-template <int NT, int MINB, bool FUSED = false>
+template <int NT, int MINB, bool FUSED = false, int MT = 0>
 int launch_t(const StreamBatch &b, int grid, cudaStream_t s) {
-    stream_kernel<NT, MINB, FUSED><<<unsigned(grid), kST, SRing<NT, MINB>::kDynSmem, s>>>(b);
+    stream_kernel<NT, MINB, FUSED, MT><<<unsigned(grid), kST, SRing<NT, MINB>::kDynSmem, s>>>(b);
     return cudaGetLastError() == cudaSuccess ? W12_OK : W12_ERR_CUDA;
 }
 
-template <int NT, int MINB, bool FUSED = false>
+template <int NT, int MINB, bool FUSED = false, int MT = 0>
 int occ_t(int *blocks) {
     const size_t smem = SRing<NT, MINB>::kDynSmem;
-    if (cudaFuncSetAttribute(stream_kernel<NT, MINB, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(stream_kernel<NT, MINB, FUSED, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(smem)) != cudaSuccess)
         return W12_ERR_CUDA;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, stream_kernel<NT, MINB, FUSED>, kST, smem) ==
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, stream_kernel<NT, MINB, FUSED, MT>, kST, smem) ==
                    cudaSuccess
                ? W12_OK
                : W12_ERR_CUDA;
@@ -398,24 +464,35 @@ int cached_map(CUtensorMap *out, const MapKey &key, Make make) {
 
 }  // namespace
 
-int stream_make_maps(StreamOne &g, const w12_desc &d, const void *blob, const uint16_t *x, int M, int MP,
-                     bool tc) {
+int stream_make_maps(StreamOne &g, const w12_desc &d, const uint16_t *x, int M, int MP, bool tc) {
     if (!encoder()) return W12_ERR_CUDA;
-    const uint8_t *bl = static_cast<const uint8_t *>(blob);
-    const int64_t K = d.K, N = d.N;
-    CUtensorMap *maps[3] = {&g.th, &g.tl, &g.te};
-    const uint64_t offs[3] = {d.off_h, d.off_l, d.off_e};
-    for (int p = 0; p < 3; ++p) {
-        const void *plane = bl + offs[p];
-        const int st = cached_map(maps[p], MapKey{reinterpret_cast<uintptr_t>(plane), K, N, tc ? -2 : -1},
-                                  [&](CUtensorMap *m) { return plane_map(m, plane, K, N, tc); });
-        if (st != W12_OK) return st;
-    }
+    const int64_t K = d.K;
     if (tc)
         return cached_map(&g.tx, MapKey{reinterpret_cast<uintptr_t>(x), K, M, -MP},
                           [&](CUtensorMap *m) { return x_map_tc(m, x, K, M, MP); });
     return cached_map(&g.tx, MapKey{reinterpret_cast<uintptr_t>(x), K, M, MP},
                       [&](CUtensorMap *m) { return x_map(m, x, K, M, MP); });
+}
+
+// The CUDA-core GEMV consumers: variant v = log2(MT) (M = 1, 2, 4), two
+// CTAs per SM.
+int stream_gemv_occupancy(int v, int *blocks) {
+    switch (v) {
+        case 0: return occ_t<1, 2, false, 1>(blocks);
+        case 1: return occ_t<1, 2, false, 2>(blocks);
+        case 2: return occ_t<1, 2, false, 4>(blocks);
+    }
+    return W12_ERR_ARG;
+}
+
+int launch_stream_gemv(const StreamBatch &b, int v, int grid, void *stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    switch (v) {
+        case 0: return launch_t<1, 2, false, 1>(b, grid, s);
+        case 1: return launch_t<1, 2, false, 2>(b, grid, s);
+        case 2: return launch_t<1, 2, false, 4>(b, grid, s);
+    }
+    return W12_ERR_ARG;
 }
 
 int stream_fused_occupancy(int v, int *blocks) {

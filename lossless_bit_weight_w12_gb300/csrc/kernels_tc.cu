@@ -7,10 +7,9 @@
 // Work split, ring and producer are those of the mma.sync stream kernel
 // (stream_device.cuh): units of one 128-k group of a 128-column tile,
 // stream-K over the whole batch, one producer warp streaming the plane
-// boxes and x with the Tensor Memory Accelerator.  Here the plane boxes use
-// the 64-byte swizzle (one thread per row reads them without bank
-// conflicts) and x comes as two boxes of 64 k x MP tokens with the 128-byte
-// swizzle: the canonical K-major layout of the UMMA B operand.
+// blocks and x with the Tensor Memory Accelerator.  Here x comes as two
+// boxes of 64 k x MP tokens with the 128-byte swizzle: the canonical
+// K-major layout of the UMMA B operand.
 //
 // Roles (one CTA per SM, 18 warps):
 //  - 16 decoder warps in two groups that take alternate stages, so two
@@ -58,9 +57,9 @@ constexpr uint32_t kAccCol = 64 * kABuf; // accumulator columns [256, 256 + MP)
 template <int MP>
 struct TCfg {
     static constexpr int kX = MP * 256;  // two boxes of MP rows x 128 bytes
-    static constexpr int kStage = (kX + 3 * kPlaneBytes + kMetaBytes + 1023) / 1024 * 1024;
-    static constexpr int kH = kX, kL = kX + kPlaneBytes, kE = kX + 2 * kPlaneBytes;
-    static constexpr int kMeta = kX + 3 * kPlaneBytes;
+    static constexpr int kStage = (kX + kUnitBytes + 1023) / 1024 * 1024;
+    static constexpr int kH = kX, kL = kX + kPlaneBlock, kE = kX + 2 * kPlaneBlock;
+    static constexpr int kMeta = kX + kMetaAt;
     static constexpr int kFit = (227 * 1024 - 1024 - 2048) / kStage;
     static constexpr int S = kFit > 8 ? 8 : kFit;
     static constexpr size_t kDynSmem = size_t(S) * kStage + 1024;
@@ -143,7 +142,7 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(&full[s], 32 + 1);  // producer: 32 meta-copy arrivals + expect_tx
+            mbar_init(&full[s], 1);  // the producer's expect_tx arrival (+ bytes)
             mbar_init(&empty[s], kDW / 2 + 1);  // one decoder group + the UMMA commit
         }
         for (int i = 0; i < kABuf; ++i) {
@@ -227,7 +226,9 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
     const int h = (warp & 7) >> 2;         // k half of the group
     const int qt = warp >> 2;              // token quarter of the epilogue
     const uint32_t lane_off = uint32_t(32 * (warp & 3)) << 16;
-    // plane row r, 16-byte chunks 2h and 2h + 1 under the 64-byte swizzle
+    // plane row r, logical 16-byte chunks 2h and 2h + 1 (the format stores
+    // chunk j of row r at j ^ ((r >> 1) & 3): a warp's 32 rows read 8
+    // different bank groups per quarter-warp)
     const uint32_t sw = uint32_t((r >> 1) & 3);
     const uint32_t p0 = uint32_t(r * 64) + ((uint32_t(2 * h) ^ sw) << 4);
     const uint32_t p1 = uint32_t(r * 64) + ((uint32_t(2 * h + 1) ^ sw) << 4);
@@ -249,7 +250,8 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
                 const uint4 h0 = lds128(st + C::kH + p0), h1 = lds128(st + C::kH + p1);
                 const uint4 l0 = lds128(st + C::kL + p0), l1 = lds128(st + C::kL + p1);
                 const uint4 e0 = lds128(st + C::kE + p0), e1 = lds128(st + C::kE + p1);
-                const uint2 mw = lds64(st + C::kMeta + uint32_t(r) * 8u);
+                const uint2 mw = make_uint2(lds32(st + C::kMeta + 4u * uint32_t(r)),
+                                            lds32(st + C::kMeta + 4u * uint32_t(r) + 4u));
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);  // planes and meta read
                 uint32_t w[32];

@@ -12,15 +12,16 @@
 
 namespace w12 {
 
-// One product y = x . W of a batch.  The tensor maps describe, for the
-// Tensor Memory Accelerator, the three plane sections as 2-D arrays of
-// 32-bit words [N columns][K/8 words] (box 16 words x 128 columns: one
-// 128-k group of a 128-column tile) and x as a 3-D array
-// [M tokens][K/64][64] bf16 (box 64 x 2 x MP: one group for every token,
-// rows past M read as zeros, 128-byte swizzle).
+// One product y = x . W of a batch.  The weights are the blob's unit blocks
+// (format v2: unit nb * KG + kg holds group kg of the 128 columns of tile
+// nb, kUnitBytes each, streamed with one bulk copy).  The tensor map
+// describes x for the Tensor Memory Accelerator: for the mma.sync kernel a
+// 3-D array [M tokens][K/64][64] bf16 (box 64 x 2 x MP: one group for every
+// token), for the tcgen05 kernel a 2-D array [M][K] (box 64 k x MP); rows
+// past M read as zeros, 128-byte swizzle.
 struct StreamOne {
-    CUtensorMap th, tl, te, tx;
-    const uint32_t *meta;  // G + 1 words
+    CUtensorMap tx;
+    const uint8_t *units;  // unit blocks
     const uint16_t *esc;   // n_esc entries
     void *y;               // [M][N]
     uint32_t *counters;    // [NB] stream-K arrival counters (zero between calls)
@@ -52,14 +53,16 @@ struct StreamBatch {
 constexpr int kStreamVariants = 10;
 int stream_variant_valid(int v);
 int stream_occupancy(int v, int *blocks_per_sm);
-// Fills the tensor maps of g from the blob and x pointers, for the mma.sync
-// kernel (tc = false: planes unswizzled, x as one 3-D box) or the tcgen05
-// kernel (tc = true: planes with the 64-byte swizzle, x as 2-D boxes of
-// 64 k x MP tokens with the 128-byte swizzle).  Returns W12_ERR_CUDA if the
-// driver's tensor-map encoder is unavailable or rejects a map.
-int stream_make_maps(StreamOne &g, const w12_desc &d, const void *blob, const uint16_t *x, int M, int MP,
-                     bool tc);
+// Fills the tensor map of x in g, for the mma.sync kernel (tc = false: one
+// 3-D box per group) or the tcgen05 kernel (tc = true: 2-D boxes of 64 k x
+// MP tokens).  Returns W12_ERR_CUDA if the driver's tensor-map encoder is
+// unavailable or rejects the map.
+int stream_make_maps(StreamOne &g, const w12_desc &d, const uint16_t *x, int M, int MP, bool tc);
 int launch_stream_batch(const StreamBatch &b, int variant, int grid, void *stream);
+// The CUDA-core GEMV consumers on the same stream (variant v = log2(MT),
+// M <= MT = 1, 2, 4).
+int stream_gemv_occupancy(int v, int *blocks_per_sm);
+int launch_stream_gemv(const StreamBatch &b, int variant, int grid, void *stream);
 // The fused lm_head + greedy verify variants (same v).
 int stream_fused_occupancy(int v, int *blocks_per_sm);
 int launch_stream_fused(const StreamBatch &b, int variant, int grid, void *stream);

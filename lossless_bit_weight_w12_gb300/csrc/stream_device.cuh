@@ -14,10 +14,25 @@
 
 namespace w12 {
 
-constexpr int kTileN = 128;               // columns per tile
-constexpr int kPlaneBytes = kTileN * 64;  // one plane box: 128 columns x 128 k
-constexpr int kMetaBytes = kTileN * 8;    // meta[g], meta[g + 1] per column
+constexpr int kTileN = kTileCols;         // columns per tile
 constexpr int kEscPrefetchLines = 64;     // escape lines prefetched per tile piece (8 KB)
+
+// Bulk global -> shared copy (TMA engine) to a shared-memory address;
+// completion counted in bytes on `bar`.  dst, src 16-byte aligned, bytes a
+// multiple of 16.
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                          uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+// Meta word `word` (0..128) of the unit block at shared address ub.
+__device__ __forceinline__ uint32_t unit_meta(uint32_t ub, int word) {
+    return lds32(ub + uint32_t(kMetaAt + 4 * word));
+}
 
 __device__ __forceinline__ uint2 lds64(uint32_t addr) {
     uint2 r;
@@ -157,76 +172,58 @@ __device__ __forceinline__ void stream_fixup(const StreamBatch &b, const StreamO
 
 
 // The producer warp of a stream kernel: for every unit of [u0, u1), once
-// the stage's previous contents are released (empty[s]), start the copies
-// of the unit into ring stage s and arm full[s]:
-//  - the H, L, E plane boxes (2-D tensor copies, evict-first in L2) at
-//    x_bytes, x_bytes + 8 KB, x_bytes + 16 KB of the stage;
+// the stage's previous contents are released (empty[s]), lane 0 starts the
+// copies of the unit into ring stage s and arms full[s] (one arrival and the
+// bytes):
+//  - the unit block (planes and meta words, kUnitBytes, evict-first in L2)
+//    with one bulk copy, at x_bytes;
 //  - x at the stage start: one 3-D box (every token, both 64-k halves,
 //    mma.sync layout), or (TC) two 2-D boxes of 64 k x MP tokens, the
-//    second at MP * 128 bytes (the canonical K-major tcgen05 operand);
-//  - meta[g], meta[g + 1] of each of the tile's columns (4-byte cp.async by
-//    the 32 lanes, which then arrive on full[s] as they land), at
-//    x_bytes + 24 KB.
-// At the start of every tile piece the piece's escape entries (a contiguous
-// range of the escape list) are prefetched into L1.  full[s] expects 33
-// arrivals (32 lanes + the expect_tx) and the tensor bytes.
+//    second at MP * 128 bytes (the canonical K-major tcgen05 operand).
+// At the start of every tile piece it prefetches the piece's escape entries
+// (a contiguous range of the escape list: escapes are listed by unit, and a
+// piece is consecutive units) into L1.
 template <int S, bool TC>
 __device__ __forceinline__ void stream_producer(const StreamBatch &b, uint32_t base, int stage_bytes,
                                                 int x_bytes, int mp, uint64_t *full, uint64_t *empty,
                                                 int *abort, int u0, int u1, int lane) {
+    if (lane != 0) return;
     const uint64_t pol = l2_evict_first_policy();
-    const uint32_t kH = uint32_t(x_bytes), kL = kH + kPlaneBytes, kE = kL + kPlaneBytes, kMeta = kE + kPlaneBytes;
-    const uint32_t tx = uint32_t(x_bytes + 3 * kPlaneBytes);
+    const uint32_t tx = uint32_t(x_bytes + kUnitBytes);
     SCur c = s_at(b, u0);
     int s = 0, issued = 0;
     uint32_t ph = 0;
     for (int u = u0; u < u1; ++u) {
         const StreamOne &g = b.g[c.gi];
         if (issued >= S && !mbar_wait(&empty[s], ph ^ 1u, abort, b.err)) break;
+        const uint8_t *unit = g.units + size_t(uint32_t(c.nb) * uint32_t(g.KG) + uint32_t(c.kg)) * kUnitBytes;
         if (u == u0 || c.kg == 0) {
-            // escape entries of this tile piece: groups [kga, kgb) of
-            // columns n0 .. nl, one contiguous range of the list
+            // escape entries of this tile piece: from the first unit's first
+            // column to the end of the piece's last unit
             const int first = g.ubase + c.nb * g.KG;
-            const int kgb = min(u1, first + g.KG) - first;
-            const int n0 = c.nb * kTileN, nl = min(g.N, n0 + kTileN) - 1;
-            uint32_t lo = 0, hi = 0;
-            if (lane == 0) {
-                lo = ldg_u32(g.meta + (uint32_t(n0) * uint32_t(g.KG) + uint32_t(c.kg))) >> 8;
-                hi = ldg_u32(g.meta + (uint32_t(nl) * uint32_t(g.KG) + uint32_t(kgb))) >> 8;
-            }
-            lo = __shfl_sync(0xFFFFFFFFu, lo, 0);
-            hi = min(__shfl_sync(0xFFFFFFFFu, hi, 0), g.n_esc);
+            const int nunits = min(u1, first + g.KG) - u;
+            const uint32_t lo = ldg_u32(reinterpret_cast<const uint32_t *>(unit + kMetaAt)) >> 8;
+            const uint32_t hi = min(ldg_u32(reinterpret_cast<const uint32_t *>(
+                                        unit + size_t(nunits - 1) * kUnitBytes + kMetaAt + 4 * kTileN)) >> 8,
+                                    g.n_esc);
             if (lo < hi) {
                 const uintptr_t a0 = reinterpret_cast<uintptr_t>(g.esc + lo) & ~uintptr_t(127);
                 const uintptr_t a1 = reinterpret_cast<uintptr_t>(g.esc + hi);
-                for (int q = lane; q < kEscPrefetchLines; q += 32) {
+                for (int q = 0; q < kEscPrefetchLines; ++q) {
                     const uintptr_t a = a0 + uintptr_t(q) * 128u;
-                    if (a < a1) prefetch_l1(reinterpret_cast<const void *>(a));
+                    if (a >= a1) break;
+                    prefetch_l1(reinterpret_cast<const void *>(a));
                 }
             }
         }
         const uint32_t st = base + uint32_t(s) * uint32_t(stage_bytes);
-#pragma unroll
-        for (int q = 0; q < kTileN / 32; ++q) {
-            const int row = lane + 32 * q, n = c.nb * kTileN + row;
-            if (n < g.N) {
-                const uint32_t gi = uint32_t(n) * uint32_t(g.KG) + uint32_t(c.kg);
-                cp_async4(st + kMeta + uint32_t(row) * 8u, g.meta + gi);
-                cp_async4(st + kMeta + uint32_t(row) * 8u + 4u, g.meta + gi + 1);
-            }
-        }
-        cp_async_mbar_arrive_noinc(&full[s]);
-        if (lane == 0) {
-            mbar_expect_tx(&full[s], tx);
-            tma_2d(st + kH, &g.th, c.kg * 16, c.nb * kTileN, &full[s], pol);
-            tma_2d(st + kL, &g.tl, c.kg * 16, c.nb * kTileN, &full[s], pol);
-            tma_2d(st + kE, &g.te, c.kg * 16, c.nb * kTileN, &full[s], pol);
-            if (TC) {
-                tma_2d_keep(st, &g.tx, 128 * c.kg, 0, &full[s]);
-                tma_2d_keep(st + uint32_t(mp) * 128u, &g.tx, 128 * c.kg + 64, 0, &full[s]);
-            } else {
-                tma_3d(st, &g.tx, 0, 2 * c.kg, 0, &full[s]);
-            }
+        mbar_expect_tx(&full[s], tx);
+        bulk_copy(st + uint32_t(x_bytes), unit, kUnitBytes, &full[s], pol);
+        if (TC) {
+            tma_2d_keep(st, &g.tx, 128 * c.kg, 0, &full[s]);
+            tma_2d_keep(st + uint32_t(mp) * 128u, &g.tx, 128 * c.kg + 64, 0, &full[s]);
+        } else {
+            tma_3d(st, &g.tx, 0, 2 * c.kg, 0, &full[s]);
         }
         s_next(b, c);
         ++issued;
@@ -235,9 +232,8 @@ __device__ __forceinline__ void stream_producer(const StreamBatch &b, uint32_t b
             ph ^= 1u;
         }
     }
-    cp_async_wait<0>();
     if (*reinterpret_cast<volatile int *>(abort)) {
-        // let the tensor copies already issued land before the CTA exits
+        // let the copies already issued land before the CTA exits
         for (int k = 0; k < S && k < issued; ++k) {
             if (--s < 0) {
                 s = S - 1;

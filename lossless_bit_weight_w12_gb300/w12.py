@@ -44,8 +44,8 @@ class W12Error(RuntimeError):
 class _CDesc(ctypes.Structure):
     _fields_ = [("version", ctypes.c_uint32), ("reserved", ctypes.c_uint32),
                 ("K", ctypes.c_int64), ("N", ctypes.c_int64), ("G", ctypes.c_int64),
-                ("off_h", ctypes.c_uint64), ("off_l", ctypes.c_uint64),
-                ("off_e", ctypes.c_uint64), ("off_meta", ctypes.c_uint64),
+                ("tiles", ctypes.c_uint64), ("unit_bytes", ctypes.c_uint64),
+                ("n_units", ctypes.c_uint64), ("off_units", ctypes.c_uint64),
                 ("off_esc", ctypes.c_uint64), ("n_esc", ctypes.c_uint64),
                 ("total_bytes", ctypes.c_uint64)]
 
@@ -57,21 +57,21 @@ class Desc:
     K: int
     N: int
     G: int
-    off_h: int
-    off_l: int
-    off_e: int
-    off_meta: int
+    tiles: int
+    unit_bytes: int
+    n_units: int
+    off_units: int
     off_esc: int
     n_esc: int
     total_bytes: int
 
     def c(self) -> _CDesc:
-        return _CDesc(self.version, 0, self.K, self.N, self.G, self.off_h, self.off_l,
-                      self.off_e, self.off_meta, self.off_esc, self.n_esc, self.total_bytes)
+        return _CDesc(self.version, 0, self.K, self.N, self.G, self.tiles, self.unit_bytes,
+                      self.n_units, self.off_units, self.off_esc, self.n_esc, self.total_bytes)
 
     @staticmethod
     def from_c(c: _CDesc) -> "Desc":
-        return Desc(c.version, c.K, c.N, c.G, c.off_h, c.off_l, c.off_e, c.off_meta,
+        return Desc(c.version, c.K, c.N, c.G, c.tiles, c.unit_bytes, c.n_units, c.off_units,
                     c.off_esc, c.n_esc, c.total_bytes)
 
 

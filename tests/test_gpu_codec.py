@@ -65,11 +65,11 @@ def test_decode_corrupt_escape_range_is_contained(dev, w12mod):
     records W12_ERR_DEVICE and finishes."""
     import torch
     w = np.full((4, 128), 0x3F80, dtype=np.uint16)
-    w[1, 5] = 0x0000  # one escape in group 1
+    w[1, 5] = 0x0000  # one escape, in column 1 (the only unit block)
     d, blob = w12mod.encode(w, w12mod.LAYOUT_NK)
     bad = blob.copy()
-    meta = bad[d.off_meta:d.off_meta + 4 * (d.G + 1)].view(np.uint32)
-    meta[2] = (meta[2] & 0xFF) | (1000 << 8)  # group 1's range now ends at 1000
+    meta = bad[3 * 8192:3 * 8192 + 4 * 129].view(np.uint32)  # the unit's meta words
+    meta[2] = (meta[2] & 0xFF) | (1000 << 8)  # column 1's range now ends at 1000
     blob_d = w12mod.upload(bad, dev)
     out = torch.empty((4, 128), dtype=torch.int16, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)

@@ -28,7 +28,7 @@ def test_exports_every_declared_symbol(w12):
     L = ctypes.CDLL(w12.LIB_PATH)
     for name in declared:
         assert hasattr(L, name), name
-    assert w12.version() == 1
+    assert w12.version() == 2
     assert w12.status_string(w12.ERR_SHAPE).startswith("W12_ERR_SHAPE")
 
 
@@ -47,8 +47,8 @@ def test_encoder_matches_oracle_bytes(w12, oracle, name, w, layout):
     d, blob = w12.encode(w, layout)
     od, oblob = oracle.encode(w, layout)
     assert (d.K, d.N, d.G, d.n_esc, d.total_bytes) == (od.K, od.N, od.G, od.n_esc, od.total_bytes)
-    assert (d.off_h, d.off_l, d.off_e, d.off_meta, d.off_esc) == \
-        (od.off_h, od.off_l, od.off_e, od.off_meta, od.off_esc)
+    assert (d.tiles, d.unit_bytes, d.n_units, d.off_units, d.off_esc) == \
+        (od.tiles, od.unit_bytes, od.n_units, od.off_units, od.off_esc)
     assert blob.tobytes() == oblob.tobytes()
     assert w12.validate(d, blob) == w12.OK
     # the oracle decodes the library's blob back to the input
@@ -68,19 +68,30 @@ def test_validate_catches_corruption(w12):
     w = synth.weights(rng, 512, 16)
     d, blob = w12.encode(w, w12.LAYOUT_NK)
     assert d.n_esc > 0
+    meta_at = 3 * 8192  # meta words of a unit block
+    last = (d.n_units - 1) * d.unit_bytes + meta_at
     bad = blob.copy()
-    bad[d.off_meta] = 250  # base of group 0 above 240
+    bad[meta_at] = 250  # base of column 0 of unit 0 above 240
     assert w12.validate(d, bad) == w12.ERR_BLOB
     bad = blob.copy()
-    meta = bad[d.off_meta:d.off_meta + 4 * (d.G + 1)].view(np.uint32)
-    meta[d.G] += 1 << 8  # sentinel no longer n_esc
+    meta = bad[last:last + 4 * 129].view(np.uint32)
+    meta[128] += 1 << 8  # the last unit's end no longer n_esc
+    assert w12.validate(d, bad) == w12.ERR_BLOB
+    bad = blob.copy()
+    meta = bad[meta_at:meta_at + 4 * 129].view(np.uint32)
+    meta[20] = 0  # a padding column (N = 16) with a base or escapes
+    meta[20] |= 3
+    assert w12.validate(d, bad) == w12.ERR_BLOB
+    bad = blob.copy()
+    bad[8192 * 2 + 64 * 40 + 3] = 0x10  # plane bytes in a padding column
     assert w12.validate(d, bad) == w12.ERR_BLOB
     bad = blob.copy()
     esc = bad[d.off_esc:d.off_esc + 2 * d.n_esc].view(np.uint16)
     esc[0] ^= 1  # an escape moved to another position
     assert w12.validate(d, bad) == w12.ERR_BLOB
     bad = blob.copy()
-    i = next(j for j in range(d.off_e, d.off_e + 64) if (blob[j] & 0x0F) != 0x0F)
+    e0 = 2 * 8192  # E plane block of unit 0, column 0's row
+    i = next(j for j in range(e0, e0 + 64) if (blob[j] & 0x0F) != 0x0F)
     bad[i] |= 0x0F  # a code-15 nibble with no escape entry
     assert w12.validate(d, bad) == w12.ERR_BLOB
     assert w12.validate(d, blob) == w12.OK

@@ -85,27 +85,46 @@ def _hexbytes(s):
 
 @pytest.mark.parametrize("name", sorted(f for f in os.listdir(GOLDEN) if f.startswith("example")))
 def test_golden_blob(oracle, name):
+    """The oracle's blob equals, byte for byte, a layout derived by hand from
+    the written format (derivations in the fixture files)."""
     g = _read_golden(name)
     K, N = int(g["K"]), int(g["N"])
     w = np.full((K, N), int(g["weights_rest"], 16), dtype=np.uint16)
-    for item in g["weights_pos"].split():
-        p, v = item.split(":")
-        w[int(p), 0] = int(v, 16)
+    for item in g["weights_at"].split():
+        kn, v = item.split(":")
+        k, n = (int(t) for t in kn.split(","))
+        w[k, n] = int(v, 16)
     d, blob = oracle.encode(w, oracle.LAYOUT_KN)
     raw = blob.tobytes()
-    off = [int(t) for t in g["off"].split()]
-    assert [d.off_h, d.off_l, d.off_e, d.off_meta, d.off_esc] == off
-    assert d.total_bytes == int(g["total"])
-    assert d.n_esc == int(g["n_esc"])
-    for key, o in (("H_head", d.off_h), ("L_head", d.off_l), ("E_head", d.off_e)):
-        want = _hexbytes(g[key])
-        assert raw[o:o + len(want)] == want, key
-    meta = _hexbytes(g["meta"])
-    assert raw[d.off_meta:d.off_meta + len(meta)] == meta
+    want_desc = [int(t) for t in g["desc"].split()]
+    assert [d.tiles, d.unit_bytes, d.n_units, d.off_units, d.off_esc, d.n_esc, d.total_bytes] == want_desc
+    assert d.G == N * (K // 128)
+    # every plane byte: the listed value, else plane_rest (real columns) or 0 (padding)
+    listed = {int(o): int(v, 16) for o, v in (t.split(":") for t in g["bytes"].split())}
+    rest = _hexbytes(g["plane_rest"])
+    for u in range(d.n_units):
+        t = u // (K // 128)
+        for plane in range(3):
+            for c in range(128):
+                real = t * 128 + c < N
+                row0 = u * d.unit_bytes + plane * 8192 + 64 * c
+                for o in range(row0, row0 + 64):
+                    want = listed.get(o, rest[plane] if real else 0)
+                    assert raw[o] == want, f"{name}: byte {o} (unit {u}, plane {plane}, column {c})"
+    for o in listed:
+        assert raw[o] == listed[o]
+    for item in g["meta"].split():
+        uw, v = item.split(":")
+        u, word = (int(x) for x in uw.split(","))
+        at = u * d.unit_bytes + 24576 + 4 * word
+        assert int.from_bytes(raw[at:at + 4], "little") == int(v, 16), f"{name}: meta {u},{word}"
+    for u in range(d.n_units):  # the 12 bytes after the meta words are zero
+        at = u * d.unit_bytes + 24576 + 4 * 129
+        assert raw[at:at + 12] == bytes(12)
     esc = _hexbytes(g["esc"])
     assert raw[d.off_esc:d.off_esc + len(esc)] == esc
-    assert oracle.group_base(w[:, 0]) == int(g["base"])
-    np.testing.assert_array_equal(oracle.decode(d, blob), w)
+    assert oracle.group_base(w[:128, 0]) == int(g["base"])
+    np.testing.assert_array_equal(oracle.decode(d, blob, oracle.LAYOUT_KN), w)
 
 
 def _group(exps, sign=0, man=0):
@@ -170,8 +189,8 @@ def test_decode_rejects_corrupt_escape_list(oracle):
     w[9, 0] = 0x0000  # one escape
     d, blob = oracle.encode(w)
     bad = blob.copy()
-    # point the sentinel past the end of the escape list
-    meta = bad[d.off_meta:d.off_meta + 8].view(np.uint32)
+    # point column 0's escape range (meta word 1 of unit 0) past the list
+    meta = bad[24576:24576 + 8].view(np.uint32)
     meta[1] = (5 << 8)
     with pytest.raises(oracle.OracleError) as e:
         oracle.decode(d, bad)
