@@ -339,7 +339,7 @@ def run_w12(args):
     w12.lib()
     hbm_peak, peak_kind = _peaks()
 
-    sweep_ms = (16, 32, 128)
+    sweep_ms = (4, 16, 32, 64, 128)
     layer, xs = build_layer(w12, dev, seed=1, M_list=(1,) + sweep_ms)
     ys, wss = make_bufs(w12, dev, layer, 1)
     x1 = xs[1]
@@ -408,19 +408,35 @@ def run_w12(args):
     for y_ref, y_e2e in zip(ys, yd):
         assert torch.equal(y_ref, y_e2e), "e2e result differs from the device-resident run"
 
-    # ---- sweep over M (same weights; inputs > L2)
-    sweep = {}
-    for M in sweep_ms:
-        ysM, wsM = make_bufs(w12, dev, layer, M)
-        n = max(3, args.steps // 2)
-        wsBM = w12.workspace(w12.gemm_batched_workspace_size(descs, M), dev)
-        bM = w12.GemmBatch(descs, blobs, xs[M], ysM, wsBM)
+    # ---- sweep over M (same weights; inputs > L2): the AUTO path, and every
+    # path that serves M (GEMV M <= 4, mma.sync, tcgen05), which shows where
+    # the tensor-core tiles overtake the GEMV and tcgen05 overtakes mma.sync
+    sweep, by_path = {}, {}
+    path_names = {1: "gemv", 2: "mma_sync", 3: "tcgen05"}
+    n = max(3, args.steps // 2)
+
+    def time_layer(xsM, ysM, wsBM, path):
+        bM = w12.GemmBatch(descs, blobs, xsM, ysM, wsBM, path)
         gM = GraphSteps(torch, lambda mark: bM(), n)
         gM.run(barrier)
         t = gM.run(barrier)
-        sweep[str(M)] = {"gbs": nbytes * n / t / 1e9, "us_per_layer": 1e6 * t / n,
-                         "frac_of_peak": nbytes * n / t / 1e9 / hbm_peak}
-        del ysM, wsM, gM
+        assert w12.get_device_error(wsBM) == 0
+        return t
+    for M in (1,) + sweep_ms:
+        ysM = [torch.empty((M, g["N"]), dtype=torch.float32, device=dev) for g in layer]
+        wsBM = w12.workspace(w12.gemm_batched_workspace_size(descs, M), dev)
+        row = {}
+        for path in (1, 2, 3):
+            if path == 1 and M > 4:
+                continue
+            t = time_layer(xs[M], ysM, wsBM, path)
+            row[path_names[path]] = round(1e6 * t / n, 2)
+        by_path[str(M)] = row
+        if M in sweep_ms:
+            t = time_layer(xs[M], ysM, wsBM, 0)
+            sweep[str(M)] = {"gbs": nbytes * n / t / 1e9, "us_per_layer": 1e6 * t / n,
+                             "frac_of_peak": nbytes * n / t / 1e9 / hbm_peak}
+        del ysM, wsBM
 
     # ---- cuBLAS BF16 GEMM on the same shapes (the 16-bit weight stream)
     bf16_rows = {}
@@ -446,6 +462,17 @@ def run_w12(args):
     verify = None
     if args.verify:
         verify = bench_lmhead(w12, torch, dev, args, barrier)
+
+    # ---- config 4 (64 layers + lm_head verify at M = 16), derived from the
+    # measured M = 16 layer step and the measured fused lm_head verify: the
+    # 64 layers stream 64 distinct weight sets, each larger than L2, so the
+    # measured step time carries over layer by layer
+    stack = None
+    if verify is not None and "16" in sweep:
+        us = 64 * sweep["16"]["us_per_layer"] + verify["us"]
+        stack = {"us_per_step": us, "tokens_per_s": 16 / (us * 1e-6),
+                 "gbs": (64 * nbytes + synth.weight_bytes_w12(5120, 151936)) / (us * 1e-6) / 1e9,
+                 "how": "64 x measured M=16 layer step + measured fused lm_head verify (derived)"}
 
     # ---- roofline of the dominant kernel: the step's single batched launch
     achieved = nbytes / t_launch / 1e9 if t_launch else None
@@ -485,8 +512,10 @@ def run_w12(args):
         "gpu_launches": args.steps,
         "roofline": roofline,
         "sweep": sweep,
+        "us_per_layer_by_path": by_path,
         "cublas_bf16": bf16_rows,
         "lmhead_verify": verify,
+        "stack_m16_estimate": stack,
         "cpu_baseline": cpu,
         "clocks": clk,
     }
