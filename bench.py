@@ -463,6 +463,25 @@ def run_w12(args):
     if args.verify:
         verify = bench_lmhead(w12, torch, dev, args, barrier)
 
+    # ---- the device encoder on the layer's largest matrix (gate_up, bf16
+    # already in HBM): plan (bases, escape counts, scan, read-back) + pack
+    enc = None
+    gi = next(i for i, g in enumerate(layer) if g["name"] == "gate_up")
+    w_dev = torch.from_numpy(layer[gi]["w_np"].view(np.int16)).to(dev)
+    w12.encode_device(w_dev)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    reps = 3
+    for _ in range(reps):
+        d_enc, blob_enc = w12.encode_device(w_dev)
+    torch.cuda.synchronize()
+    t_enc = (time.perf_counter() - t0) / reps
+    enc = {"matrix": "gate_up 5120x34816 (bf16 in HBM)", "ms": 1e3 * t_enc,
+           "gweights_per_s": layer[gi]["K"] * layer[gi]["N"] / t_enc / 1e9,
+           "bytes_equal_host_encoder": bool(torch.equal(blob_enc.cpu(), torch.from_numpy(
+               w12.encode(layer[gi]["w_np"], w12.LAYOUT_NK)[1])))}
+    del w_dev, blob_enc
+
     # ---- config 4 (64 layers + lm_head verify at M = 16), derived from the
     # measured M = 16 layer step and the measured fused lm_head verify: the
     # 64 layers stream 64 distinct weight sets, each larger than L2, so the
@@ -516,6 +535,7 @@ def run_w12(args):
         "cublas_bf16": bf16_rows,
         "lmhead_verify": verify,
         "stack_m16_estimate": stack,
+        "encode_device": enc,
         "cpu_baseline": cpu,
         "clocks": clk,
     }

@@ -167,6 +167,39 @@ int w12_encode(const uint16_t *w_host, int64_t K, int64_t N, int layout, const w
 int w12_validate(const w12_desc *d, const void *blob_host);
 
 /* --------------------------------------------------------------------- */
+/* Device encoder (the same bytes as the host encoder)                  */
+/* --------------------------------------------------------------------- */
+
+/* Bytes of workspace w12_encode_plan_device / w12_encode_device need for a
+ * K x N matrix (>= 256; 0 for a negative size). */
+size_t w12_encode_device_workspace_size(int64_t K, int64_t N);
+
+/*
+ * w12_encode_plan on the GPU, for weights already in device memory (a model
+ * loaded straight to HBM: no pass over the weights on the host).  w_dev: the
+ * bf16 matrix in layout W12_LAYOUT_KN or _NK, 16-byte aligned.  Computes
+ * every group's base and escape count into the workspace, fills *d (the
+ * descriptor w12_encode_plan gives for the same matrix) and waits for
+ * `stream` (the escape count is read back to size the blob).  Keep the
+ * workspace for w12_encode_device.  Up to 2^24 unit columns (ceil(N/128) *
+ * K/128 * 128 <= 2^24, about 2^31 weights) per matrix.
+ * Errors: W12_ERR_ARG, W12_ERR_SHAPE, W12_ERR_ALIGN, W12_ERR_WORKSPACE,
+ * W12_ERR_TOO_MANY_ESCAPES, W12_ERR_CUDA.
+ */
+int w12_encode_plan_device(const uint16_t *w_dev, int64_t K, int64_t N, int layout, w12_desc *d,
+                           void *ws_dev, size_t ws_bytes, void *stream);
+
+/*
+ * w12_encode on the GPU: writes the blob of *d (from w12_encode_plan_device
+ * on the same w_dev, layout and workspace) into blob_dev (d->total_bytes,
+ * 256-byte aligned), byte for byte what w12_encode writes.  Asynchronous on
+ * `stream`.  Errors: W12_ERR_ARG (d does not match K, N), W12_ERR_ALIGN,
+ * W12_ERR_WORKSPACE, W12_ERR_CUDA.
+ */
+int w12_encode_device(const uint16_t *w_dev, int64_t K, int64_t N, int layout, const w12_desc *d,
+                      void *blob_dev, void *ws_dev, size_t ws_bytes, void *stream);
+
+/* --------------------------------------------------------------------- */
 /* Device calls                                                          */
 /* --------------------------------------------------------------------- */
 

@@ -459,6 +459,53 @@ extern "C" int w12_verify_greedy_lmhead(const uint16_t *hidden, const w12_desc *
     return launch_stream_fused(b, fp.bp.variant, fp.bp.grid, stream);
 }
 
+extern "C" size_t w12_encode_device_workspace_size(int64_t K, int64_t N) {
+    if (K < 0 || N < 0) return 0;
+    return std::max<size_t>(256, encode_device_ws(K, N));
+}
+
+extern "C" int w12_encode_plan_device(const uint16_t *w, int64_t K, int64_t N, int layout, w12_desc *d,
+                                      void *ws, size_t ws_bytes, void *stream) {
+    if (layout != W12_LAYOUT_KN && layout != W12_LAYOUT_NK) return W12_ERR_ARG;
+    if (K < 0 || N < 0 || K % kGroup != 0) return W12_ERR_SHAPE;
+    if (!d) return W12_ERR_ARG;
+    if (K == 0 || N == 0) {
+        layout_v2(K, N, 0, d);
+        return W12_OK;
+    }
+    if (!w || !ws) return W12_ERR_ARG;
+    if (!aligned(w, 16) || !aligned(ws, 256)) return W12_ERR_ALIGN;
+    if (ws_bytes < encode_device_ws(K, N)) return W12_ERR_WORKSPACE;
+    // the escape counts are scanned in 32 bits: at most 2^24 (unit, column)
+    // slots of 128 weights (2^31 weights) per call
+    if (N >= (int64_t(1) << 31) || (N + kTileCols - 1) / kTileCols * (K / kGroup) * kTileCols >= (int64_t(1) << 24))
+        return W12_ERR_SHAPE;
+    uint32_t *total = nullptr;
+    int st = launch_encode_scan(w, K, N, layout, ws, stream, &total);
+    if (st != W12_OK) return st;
+    uint32_t n_esc = 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(&n_esc, total, sizeof n_esc, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return W12_ERR_CUDA;
+    if (n_esc >= kMaxEscapes) return W12_ERR_TOO_MANY_ESCAPES;
+    layout_v2(K, N, n_esc, d);
+    return W12_OK;
+}
+
+extern "C" int w12_encode_device(const uint16_t *w, int64_t K, int64_t N, int layout, const w12_desc *d,
+                                 void *blob, void *ws, size_t ws_bytes, void *stream) {
+    if (layout != W12_LAYOUT_KN && layout != W12_LAYOUT_NK) return W12_ERR_ARG;
+    const int st = check_desc(d);
+    if (st != W12_OK) return st;
+    if (d->K != K || d->N != N) return W12_ERR_ARG;
+    if (d->total_bytes == 0) return W12_OK;
+    if (!w || !blob || !ws) return W12_ERR_ARG;
+    if (!aligned(w, 16) || !aligned(blob, 256) || !aligned(ws, 256)) return W12_ERR_ALIGN;
+    if (ws_bytes < encode_device_ws(K, N)) return W12_ERR_WORKSPACE;
+    return launch_encode_pack(w, d, layout, blob, ws, stream);
+}
+
 extern "C" int w12_get_device_error(void *ws, int *err_host, void *stream) {
     if (!ws || !err_host) return W12_ERR_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

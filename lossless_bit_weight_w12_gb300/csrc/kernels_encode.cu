@@ -1,0 +1,351 @@
+// kernels_encode.cu -- the W12 encoder on the GPU (same bytes as the host
+// encoder in encode.cpp and as the format text in include/w12.h).
+//
+// Loading a model through the host encoder means scanning every weight on a
+// few CPU cores; here the same three steps run on the device:
+//  1. scan: one warp per group (128 k of one column): the exponent
+//     histogram, the base (the window [b, b+14], b <= 240, holding the most
+//     exponents, the largest b on a tie) and the escape count 128 - cover;
+//  2. an exclusive scan of the escape counts in unit, then column order
+//     (the order of the escape list), giving every group's first escape;
+//  3. pack: one warp per (unit, column): lanes 0..15 build word q of the H,
+//     L and E planes (pos 8q .. 8q+7) and store it at its swizzled place;
+//     escaped weights write their entries at first_escape + rank (ballot
+//     prefix); meta words follow.
+// Padding columns (past N) get base 0, no escapes and zero plane bytes (the
+// blob is zero-filled first).
+#include <cuda_runtime.h>
+
+#include "async_common.cuh"
+#include "w12_internal.h"
+
+namespace w12 {
+
+namespace {
+
+constexpr int kScanBlock = 1024;  // threads of a scan block
+
+struct EncArgs {
+    const uint16_t *w;  // [N][K] (NK) or [K][N] (KN)
+    int64_t K, N, KG;
+    int layout;
+    int64_t U;          // unit blocks
+    uint8_t *base;      // [U * 128]
+    uint32_t *count;    // [U * 128], then exclusive scan in place -> begin
+    uint32_t *block_sum;
+    uint8_t *blob;
+    uint64_t off_esc, n_esc;
+};
+
+// The 4 weights pos 4l .. 4l+3 of group (n, kg) for lane l.
+__device__ __forceinline__ void load4(const EncArgs &a, int64_t n, int64_t kg, int lane, uint16_t (&v)[4]) {
+    const int64_t k0 = kg * kGroup + 4 * lane;
+    if (a.layout == W12_LAYOUT_NK) {
+        const uint2 q = *reinterpret_cast<const uint2 *>(a.w + n * a.K + k0);
+        v[0] = uint16_t(q.x);
+        v[1] = uint16_t(q.x >> 16);
+        v[2] = uint16_t(q.y);
+        v[3] = uint16_t(q.y >> 16);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = a.w[(k0 + i) * a.N + n];
+    }
+}
+
+// Base and escape count of one group, computed by a warp.  hist: this
+// warp's 256 shared counters.
+__device__ __forceinline__ void group_base_warp(const uint16_t (&v)[4], int lane, uint32_t *hist, uint32_t &b_out,
+                                                uint32_t &esc_out) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) hist[lane * 8 + i] = 0u;
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) atomicAdd(&hist[(v[i] >> 7) & 0xFFu], 1u);
+    __syncwarp();
+    // inclusive prefix of the histogram: lane l owns bins 8l .. 8l+7
+    uint32_t p[8];
+    uint32_t run = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        run += hist[lane * 8 + i];
+        p[i] = run;
+    }
+    uint32_t excl = run;  // inclusive scan of the lane totals, then shift
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, excl, off);
+        if (lane >= off) excl += o;
+    }
+    excl -= run;
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) hist[lane * 8 + i] = p[i] + excl;  // hist now holds prefix[e] = #exp <= e
+    __syncwarp();
+    // cover(b) = #exp in [b, b+14] = prefix[b+14] - prefix[b-1]; best cover,
+    // the largest b on ties: maximise (cover << 8 | b)
+    uint32_t best = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int b = lane * 8 + i;
+        if (b <= kMaxBase) {
+            const uint32_t hi = hist[b + 14];
+            const uint32_t lo = b > 0 ? hist[b - 1] : 0u;
+            const uint32_t key = ((hi - lo) << 8) | uint32_t(b);
+            best = key > best ? key : best;
+        }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        const uint32_t o = __shfl_xor_sync(0xFFFFFFFFu, best, off);
+        best = o > best ? o : best;
+    }
+    b_out = best & 0xFFu;
+    esc_out = uint32_t(kGroup) - (best >> 8);
+    __syncwarp();
+}
+
+// 1. bases and escape counts; one warp per (unit, column) slot.
+__global__ void __launch_bounds__(256) enc_scan_kernel(const EncArgs a) {
+    __shared__ uint32_t hist[8][256];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t slots = a.U * kTileCols;
+    for (int64_t sl = int64_t(blockIdx.x) * 8 + warp; sl < slots; sl += int64_t(gridDim.x) * 8) {
+        const int64_t u = sl / kTileCols, c = sl % kTileCols;
+        const int64_t n = (u / a.KG) * kTileCols + c, kg = u % a.KG;
+        uint32_t b = 0, e = 0;
+        if (n < a.N) {  // uniform across the warp
+            uint16_t v[4];
+            load4(a, n, kg, lane, v);
+            group_base_warp(v, lane, hist[warp], b, e);
+        }
+        if (lane == 0) {
+            a.base[sl] = uint8_t(b);
+            a.count[sl] = e;
+        }
+    }
+}
+
+// 2a. exclusive scan of count[] inside blocks of kScanBlock; block totals out.
+__global__ void __launch_bounds__(kScanBlock) enc_scan_blocks(uint32_t *count, int64_t n, uint32_t *block_sum) {
+    __shared__ uint32_t warp_tot[kScanBlock / 32];
+    const int64_t i = int64_t(blockIdx.x) * kScanBlock + threadIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t v = i < n ? count[i] : 0u;
+    uint32_t x = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, x, off);
+        if (lane >= off) x += o;
+    }
+    if (lane == 31) warp_tot[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t t = warp_tot[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, t, off);
+            if (lane >= off) t += o;
+        }
+        warp_tot[lane] = t;  // inclusive
+    }
+    __syncthreads();
+    const uint32_t before = warp > 0 ? warp_tot[warp - 1] : 0u;
+    if (i < n) count[i] = before + x - v;  // exclusive within the block
+    if (threadIdx.x == kScanBlock - 1) block_sum[blockIdx.x] = warp_tot[kScanBlock / 32 - 1];
+}
+
+// 2b. exclusive scan of the block totals (one block, looping); the grand
+// total lands in block_sum[nb].
+__global__ void __launch_bounds__(kScanBlock) enc_scan_totals(uint32_t *block_sum, int64_t nb) {
+    __shared__ uint32_t warp_tot[kScanBlock / 32];
+    __shared__ uint32_t carry;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) carry = 0u;
+    __syncthreads();
+    for (int64_t base = 0; base < nb; base += kScanBlock) {
+        const int64_t i = base + threadIdx.x;
+        const uint32_t v = i < nb ? block_sum[i] : 0u;
+        uint32_t x = v;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, x, off);
+            if (lane >= off) x += o;
+        }
+        if (lane == 31) warp_tot[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            uint32_t t = warp_tot[lane];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, t, off);
+                if (lane >= off) t += o;
+            }
+            warp_tot[lane] = t;
+        }
+        __syncthreads();
+        const uint32_t before = (warp > 0 ? warp_tot[warp - 1] : 0u) + carry;
+        if (i < nb) block_sum[i] = before + x - v;
+        __syncthreads();
+        if (threadIdx.x == 0) carry += warp_tot[kScanBlock / 32 - 1];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) block_sum[nb] = carry;
+}
+
+// 2c. add the scanned block totals back.
+__global__ void __launch_bounds__(kScanBlock) enc_scan_add(uint32_t *count, int64_t n, const uint32_t *block_sum) {
+    const int64_t i = int64_t(blockIdx.x) * kScanBlock + threadIdx.x;
+    if (i < n) count[i] += block_sum[blockIdx.x];
+}
+
+// 3. pack; one warp per (unit, column) slot, lanes 0..15 one plane word each.
+__global__ void __launch_bounds__(256) enc_pack_kernel(const EncArgs a) {
+    constexpr int kPermH[8] = {4, 0, 5, 1, 6, 2, 7, 3};
+    constexpr int kPermL[8] = {0, 5, 1, 6, 2, 7, 3, 4};
+    constexpr int kPermE[8] = {0, 4, 1, 5, 2, 6, 3, 7};
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t slots = a.U * kTileCols;
+    uint16_t *esc = reinterpret_cast<uint16_t *>(a.blob + a.off_esc);
+    for (int64_t sl = int64_t(blockIdx.x) * 8 + warp; sl < slots; sl += int64_t(gridDim.x) * 8) {
+        const int64_t u = sl / kTileCols;
+        const int c = int(sl % kTileCols);
+        const int64_t n = (u / a.KG) * kTileCols + c, kg = u % a.KG;
+        uint8_t *ub = a.blob + u * kUnitBytes;
+        const uint32_t b = a.base[sl], begin = a.count[sl];
+        if (lane == 0) {
+            *reinterpret_cast<uint32_t *>(ub + kMetaAt + 4 * c) = b | (begin << 8);
+            if (c == kTileCols - 1) {
+                const uint64_t next = u + 1 < a.U ? a.count[(u + 1) * kTileCols] : a.n_esc;
+                *reinterpret_cast<uint32_t *>(ub + kMetaAt + 4 * kTileCols) = uint32_t(next << 8);
+            }
+        }
+        if (n >= a.N) continue;  // padding column: zero planes (uniform across the warp)
+        // lane q < 16: the 8 weights pos 8q .. 8q+7
+        uint16_t v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        if (lane < 16) {
+            const int64_t k0 = kg * kGroup + 8 * lane;
+            if (a.layout == W12_LAYOUT_NK) {
+                const uint4 q = *reinterpret_cast<const uint4 *>(a.w + n * a.K + k0);
+                const uint32_t wq[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    v[2 * i] = uint16_t(wq[i]);
+                    v[2 * i + 1] = uint16_t(wq[i] >> 16);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[i] = a.w[(k0 + i) * a.N + n];
+            }
+        }
+        uint32_t hw = 0, lw = 0, ew = 0, flags = 0;
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            const int jh = kPermH[s], jl = kPermL[s], je = kPermE[s];
+            const uint32_t smh = (uint32_t(v[jh] & 0x7Fu) << 1) | (uint32_t(v[jh ^ 1]) >> 15);
+            const uint32_t sml = (uint32_t(v[jl] & 0x7Fu) << 1) | (uint32_t(v[jl ^ 1]) >> 15);
+            const uint32_t ee = (v[je] >> 7) & 0xFFu;
+            const bool in = ee >= b && ee <= b + 14;
+            hw |= (smh >> 4) << (4 * s);
+            lw |= (sml & 0xFu) << (4 * s);
+            ew |= (in ? ee - b : 15u) << (4 * s);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t e = (v[i] >> 7) & 0xFFu;
+            if (lane < 16 && !(e >= b && e <= b + 14)) flags |= 1u << i;
+        }
+        if (lane < 16) {
+            const uint32_t off = uint32_t(c * 64 + (((lane >> 2) ^ ((c >> 1) & 3)) << 4) + (lane & 3) * 4);
+            *reinterpret_cast<uint32_t *>(ub + off) = hw;
+            *reinterpret_cast<uint32_t *>(ub + kPlaneBlock + off) = lw;
+            *reinterpret_cast<uint32_t *>(ub + 2 * kPlaneBlock + off) = ew;
+        }
+        // escape entries in pos order: rank = escapes of earlier lanes + earlier bits
+        const uint32_t cnt = __popc(flags);
+        uint32_t before = cnt;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, before, off);
+            if (lane >= off) before += o;
+        }
+        before -= cnt;
+        uint32_t at = begin + before;
+        for (int i = 0; i < 8; ++i) {
+            if (flags & (1u << i)) {
+                const uint32_t pos = uint32_t(8 * lane + i), e = (v[i] >> 7) & 0xFFu;
+                if (at < a.n_esc) esc[at] = uint16_t(pos | (e << 7));
+                ++at;
+            }
+        }
+    }
+}
+
+int grid_for(int64_t slots) {
+    int sms = 0;
+    if (device_sm_count(&sms) != W12_OK) return -1;
+    const int64_t g = (slots + 7) / 8;
+    const int64_t cap = int64_t(sms) * 32;
+    return int(g < cap ? (g > 0 ? g : 1) : cap);
+}
+
+}  // namespace
+
+size_t encode_device_ws(int64_t K, int64_t N) {
+    const int64_t U = ((N + kTileCols - 1) / kTileCols) * (K / kGroup);
+    const int64_t slots = U * kTileCols;
+    const int64_t nb = (slots + kScanBlock - 1) / kScanBlock;
+    return kWsHeader + round256(uint64_t(slots)) + round256(uint64_t(slots) * 4u) + round256(uint64_t(nb + 1) * 4u);
+}
+
+// Steps 1-2 into the workspace; *total_dev receives the escape count.
+int launch_encode_scan(const uint16_t *w, int64_t K, int64_t N, int layout, void *ws, void *stream,
+                       uint32_t **total_dev) {
+    EncArgs a{};
+    a.w = w;
+    a.K = K;
+    a.N = N;
+    a.KG = K / kGroup;
+    a.layout = layout;
+    a.U = ((N + kTileCols - 1) / kTileCols) * a.KG;
+    const int64_t slots = a.U * kTileCols;
+    const int64_t nb = (slots + kScanBlock - 1) / kScanBlock;
+    uint8_t *p = static_cast<uint8_t *>(ws) + kWsHeader;
+    a.base = p;
+    a.count = reinterpret_cast<uint32_t *>(p + round256(uint64_t(slots)));
+    a.block_sum = reinterpret_cast<uint32_t *>(p + round256(uint64_t(slots)) + round256(uint64_t(slots) * 4u));
+    *total_dev = a.block_sum + nb;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int grid = grid_for(slots);
+    if (grid < 0) return W12_ERR_CUDA;
+    enc_scan_kernel<<<unsigned(grid), 256, 0, s>>>(a);
+    enc_scan_blocks<<<unsigned(nb), kScanBlock, 0, s>>>(a.count, slots, a.block_sum);
+    enc_scan_totals<<<1, kScanBlock, 0, s>>>(a.block_sum, nb);
+    enc_scan_add<<<unsigned(nb), kScanBlock, 0, s>>>(a.count, slots, a.block_sum);
+    return cudaGetLastError() == cudaSuccess ? W12_OK : W12_ERR_CUDA;
+}
+
+// Step 3 (after launch_encode_scan on the same workspace).
+int launch_encode_pack(const uint16_t *w, const w12_desc *d, int layout, void *blob, void *ws, void *stream) {
+    EncArgs a{};
+    a.w = w;
+    a.K = d->K;
+    a.N = d->N;
+    a.KG = d->K / kGroup;
+    a.layout = layout;
+    a.U = int64_t(d->n_units);
+    const int64_t slots = a.U * kTileCols;
+    uint8_t *p = static_cast<uint8_t *>(ws) + kWsHeader;
+    a.base = p;
+    a.count = reinterpret_cast<uint32_t *>(p + round256(uint64_t(slots)));
+    a.blob = static_cast<uint8_t *>(blob);
+    a.off_esc = d->off_esc;
+    a.n_esc = d->n_esc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(blob, 0, d->total_bytes, s) != cudaSuccess) return W12_ERR_CUDA;
+    const int grid = grid_for(slots);
+    if (grid < 0) return W12_ERR_CUDA;
+    enc_pack_kernel<<<unsigned(grid), 256, 0, s>>>(a);
+    return cudaGetLastError() == cudaSuccess ? W12_OK : W12_ERR_CUDA;
+}
+
+}  // namespace w12

@@ -41,6 +41,14 @@ int launch_decode(const w12_desc *d, const void *blob, uint16_t *w, int layout, 
                   void *stream);
 int device_sm_count(int *sms);
 
+// Device encoder (kernels_encode.cu): workspace bytes; steps 1-2 (bases,
+// escape counts and their exclusive scan; *total_dev = escape count);
+// step 3 (pack into a blob of d's layout).
+size_t encode_device_ws(int64_t K, int64_t N);
+int launch_encode_scan(const uint16_t *w, int64_t K, int64_t N, int layout, void *ws, void *stream,
+                       uint32_t **total_dev);
+int launch_encode_pack(const uint16_t *w, const w12_desc *d, int layout, void *blob, void *ws, void *stream);
+
 struct VerifyArgs {
     const void *logits;
     int dtype;

@@ -32,6 +32,7 @@ EXPORTS = (
     "w12_verify_workspace_size", "w12_verify_greedy", "w12_verify_lmhead_workspace_size",
     "w12_verify_greedy_lmhead", "w12_get_device_error", "w12_verify_greedy_noalloc",
     "w12_gemm_batched_workspace_size", "w12_gemm_batched", "w12_gemm_batched_ex",
+    "w12_encode_device_workspace_size", "w12_encode_plan_device", "w12_encode_device",
 )
 
 
@@ -110,6 +111,10 @@ def lib():
         L.w12_gemm_batched_workspace_size.argtypes = [D, I, I64]
         L.w12_gemm_batched.argtypes = [D, P, P, I64, P, I, I, P, SZ, P]
         L.w12_gemm_batched_ex.argtypes = [D, P, P, I64, P, I, I, P, SZ, I, P]
+        L.w12_encode_device_workspace_size.restype = SZ
+        L.w12_encode_device_workspace_size.argtypes = [I64, I64]
+        L.w12_encode_plan_device.argtypes = [P, I64, I64, I, D, P, SZ, P]
+        L.w12_encode_device.argtypes = [P, I64, I64, I, D, P, P, SZ, P]
         _lib = L
     return _lib
 
@@ -187,6 +192,27 @@ def decode(d: Desc, blob_dev, w_dev, layout: int = LAYOUT_NK, err_dev=None, stre
     c = d.c()
     _check(lib().w12_decode(ctypes.byref(c), _dptr(blob_dev), _dptr(w_dev), layout,
                             _dptr(err_dev), _stream(stream)), "w12_decode")
+
+
+def encode_device(w_dev, layout: int = LAYOUT_NK, stream=None):
+    """Encode bf16 bit patterns already on the device (a torch int16/uint16
+    CUDA tensor, [N, K] for LAYOUT_NK or [K, N] for LAYOUT_KN) on the GPU;
+    returns (Desc, blob device tensor, 256-byte aligned)."""
+    import torch
+    K, N = _kn(w_dev, layout)
+    ws = workspace(lib().w12_encode_device_workspace_size(K, N), w_dev.device)
+    c = _CDesc()
+    _check(lib().w12_encode_plan_device(_dptr(w_dev), K, N, layout, ctypes.byref(c), _dptr(ws), ws.numel(),
+                                        _stream(stream)), "w12_encode_plan_device")
+    d = Desc.from_c(c)
+    t = torch.empty(d.total_bytes + 256, dtype=torch.uint8, device=w_dev.device)
+    off = (-t.data_ptr()) % 256
+    blob = t[off:off + d.total_bytes]
+    if d.total_bytes:
+        c = d.c()
+        _check(lib().w12_encode_device(_dptr(w_dev), K, N, layout, ctypes.byref(c), _dptr(blob), _dptr(ws),
+                                       ws.numel(), _stream(stream)), "w12_encode_device")
+    return d, blob
 
 
 def gemm_workspace_size(d: Desc, M: int) -> int:
