@@ -56,8 +56,9 @@ int query_device(Device *dv) {
     return W12_OK;
 }
 
-// key: 48..63 tcgen05 variants, 64..79 mma.sync stream variants, 80..95
-// the same with the fused lm_head verify, 96.. CUDA-core GEMV variants
+// key: 32..47 tcgen05 variants with the fused lm_head verify, 48..63
+// tcgen05 variants, 64..79 mma.sync stream variants, 80..95 the same with
+// the fused lm_head verify, 96.. CUDA-core GEMV variants
 int cached_occupancy(const Device &dv, int key, size_t smem, int *blocks) {
     {
         std::lock_guard<std::mutex> lock(g_cache_mu);
@@ -68,7 +69,8 @@ int cached_occupancy(const Device &dv, int key, size_t smem, int *blocks) {
             return W12_OK;
         }
     }
-    const int st = key < 64   ? tc_occupancy(key - 48, blocks)
+    const int st = key < 48   ? tc_fused_occupancy(key - 32, blocks)
+                   : key < 64 ? tc_occupancy(key - 48, blocks)
                    : key < 80 ? stream_occupancy(key - 64, blocks)
                    : key < 96 ? stream_fused_occupancy(key - 80, blocks)
                               : stream_gemv_occupancy(key - 96, blocks);
@@ -242,13 +244,13 @@ struct FusedPlan {
 
 int plan_fused(const w12_desc *d, int64_t M, FusedPlan *fp) {
     BatchPlan &bp = fp->bp;
-    int st = plan_batch(d, 1, M, W12_PATH_MMA, &bp);
+    int st = plan_batch(d, 1, M, M <= 32 ? W12_PATH_MMA : W12_PATH_TC, &bp);
     if (st != W12_OK) return st;
     Device dv;
     if (query_device(&dv) != W12_OK) return W12_ERR_CUDA;
-    bp.variant = stream_variant_for(M);
     int occ = 0;
-    if (cached_occupancy(dv, 80 + bp.variant, 0, &occ) != W12_OK || occ < 1) return W12_ERR_CUDA;
+    const int key = bp.path == W12_PATH_TC ? 32 + bp.variant : 80 + bp.variant;
+    if (cached_occupancy(dv, key, 0, &occ) != W12_OK || occ < 1) return W12_ERR_CUDA;
     bp.grid = int(std::min<int64_t>(int64_t(dv.sms) * occ, bp.U));
     size_t off = bp.stream_partial;
     off += round256(uint64_t(bp.grid) * 2u * uint64_t(M) * uint64_t(kMmaCols) * 4u);
@@ -456,7 +458,8 @@ extern "C" int w12_verify_greedy_lmhead(const uint16_t *hidden, const w12_desc *
     b.next_tok = next_tok;
     b.vR = int(R);
     b.vT = int(T);
-    return launch_stream_fused(b, fp.bp.variant, fp.bp.grid, stream);
+    return fp.bp.path == W12_PATH_TC ? launch_tc_fused(b, fp.bp.variant, fp.bp.grid, stream)
+                                     : launch_stream_fused(b, fp.bp.variant, fp.bp.grid, stream);
 }
 
 extern "C" size_t w12_encode_device_workspace_size(int64_t K, int64_t N) {

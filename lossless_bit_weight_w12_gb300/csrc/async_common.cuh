@@ -1,4 +1,5 @@
-// async_common.cuh -- mbarrier and bulk-copy (TMA engine) primitives, inline PTX.
+// async_common.cuh -- mbarrier primitives, shared-memory loads and named
+// barriers, inline PTX.
 //
 // Every wait is bounded: it polls with try_wait, backs off, and gives up after
 // kWaitLimitNs of wall time (or as soon as another thread of the CTA has
@@ -82,49 +83,6 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     return pol;
 }
 
-// Bulk global -> shared copy on the TMA engine; completion is counted in
-// bytes on `bar`.  dst, src 16-byte aligned; bytes a multiple of 16.
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
-                                         uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
-        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
-        : "memory");
-}
-
-// Same without a cache hint (small or reused data: meta words, activations).
-__device__ __forceinline__ void bulk_g2s_keep(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1], %2, [%3];" ::"r"(smem_addr(dst)),
-        "l"(src), "r"(bytes), "r"(smem_addr(bar))
-        : "memory");
-}
-
-// Per-thread asynchronous copies (LDGSTS): completion is tracked per thread
-// with commit/wait groups, so a thread that only reads back its own copies
-// needs no other synchronisation and no spin-wait.
-__device__ __forceinline__ void cp_async16_stream(uint32_t dst, const void *src, uint64_t policy) {
-    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-                 "l"(policy)
-                 : "memory");
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
-}
-
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     uint4 r;

@@ -9,14 +9,6 @@
 
 namespace w12 {
 
-// Barrier over the threads taking part in the epilogue: the whole CTA, or
-// the first nthreads of it (named barrier 1) when a producer warp is apart.
-__device__ __forceinline__ void epi_sync(int nthreads) {
-    if (nthreads == int(blockDim.x))
-        __syncthreads();
-    else
-        asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
-}
 
 // Store one output of a batched GEMV (y row-major [M][N], fp32 or bf16).
 __device__ __forceinline__ void store_out(void *y, int y_dtype, int64_t N, int64_t m, int64_t n, float v) {

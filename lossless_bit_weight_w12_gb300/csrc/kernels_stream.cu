@@ -404,9 +404,7 @@ int occ_t(int *blocks) {
 }  // namespace
 
 // v = 2 * log2(NT) + (ctas_per_sm - 1); two CTAs per SM only where the
-// ring still holds three stages.
-int stream_variant_valid(int v) { return v >= 0 && v < kStreamVariants && v != 7 && v != 9; }
-
+// ring still holds three stages (NT <= 4).
 int stream_occupancy(int v, int *blocks) {
     switch (v) {
         case 0: return occ_t<1, 1>(blocks);

@@ -40,6 +40,7 @@
 #include <cuda_runtime.h>
 
 #include "stream_device.cuh"
+#include "verify_common.cuh"
 
 namespace w12 {
 
@@ -123,7 +124,11 @@ __device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t (&r)[4]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-template <int MP>
+// FUSED: the lm_head + greedy verify epilogue (as in kernels_stream.cu):
+// tile outputs fold into a per-CTA running (value, lowest index) maximum
+// per token, split tiles are folded by the CTA that completes them, and the
+// last CTA to arrive runs the acceptance rule over every CTA's keys.
+template <int MP, bool FUSED>
 __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ StreamBatch b) {
     using C = TCfg<MP>;
     constexpr int S = C::S;
@@ -131,6 +136,7 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
     __shared__ __align__(8) uint64_t full[S], empty[S], a_full[kABuf], a_free[kABuf], acc_full, acc_empty, fin;
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort, s_last;
+    __shared__ unsigned long long s_best[FUSED ? MP : 1];
     const uint32_t base = (smem_addr(smem_dyn) + 1023u) & ~1023u;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int u0, u1;
@@ -155,6 +161,8 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
         s_abort = 0;
         mbar_fence_init();
     }
+    if (FUSED)
+        for (int m = threadIdx.x; m < MP; m += kTT) s_best[m] = 0ull;
     if (warp == kMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&s_tmem)),
                      "r"(kTmemCols)
@@ -294,11 +302,25 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty);
         if (ua == first && ub == first + g.KG) {
-            if (valid) {
+            if (valid && (!FUSED || g.y)) {
 #pragma unroll
                 for (int e = 0; e < kHalf; ++e) {
                     const int m = qt * kHalf + e;
                     if (m < M) store_out(g.y, b.y_dtype, g.N, m, n, v[e]);
+                }
+            }
+            if (FUSED) {
+                // per token: the warp's 32 rows -> one key, then the CTA maximum
+#pragma unroll
+                for (int e = 0; e < kHalf; ++e) {
+                    unsigned long long best = valid ? pack_key(v[e], uint32_t(n)) : 0ull;
+#pragma unroll
+                    for (int off = 16; off >= 1; off >>= 1) {
+                        const unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, best, off);
+                        best = o > best ? o : best;
+                    }
+                    const int m = qt * kHalf + e;
+                    if (lane == 0 && m < M && best != 0ull) atomicMax(&s_best[m], best);
                 }
             }
         } else {
@@ -309,25 +331,43 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
                 const int m = qt * kHalf + e;
                 if (m < M) P[m * kTileN + r] = v[e];
             }
-            stream_fixup<false>(b, g, first, nb, ub - ua, &s_last, threadIdx.x, kDT, nullptr);
+            stream_fixup<FUSED>(b, g, first, nb, ub - ua, &s_last, threadIdx.x, kDT, s_best);
         }
         ++piece;
         s_next_tile(b, c);
     }
+
+    if (FUSED) {
+        // publish this CTA's per-token best; the last CTA to arrive folds
+        // them and runs the acceptance rule
+        const int tid = threadIdx.x;
+        named_sync(kDT);
+        for (int m = tid; m < M; m += kDT) b.row_best[size_t(blockIdx.x) * M + m] = s_best[m];
+        __threadfence();
+        named_sync(kDT);
+        if (tid == 0) s_last = (atomicAdd(b.done, 1u) == gridDim.x - 1);
+        named_sync(kDT);
+        if (s_last) {
+            __threadfence();
+            verify_from_keys(b.row_best, int64_t(gridDim.x), M, b.vR, b.vT, b.draft, b.accept_len, b.next_tok,
+                             b.gbuf, tid, kDT);
+            if (tid == 0) *b.done = 0u;
+        }
+    }
 }
 
-template <int MP>
+template <int MP, bool FUSED = false>
 int launch_tc_t(const StreamBatch &b, int grid, cudaStream_t s) {
-    tc_kernel<MP><<<unsigned(grid), kTT, TCfg<MP>::kDynSmem, s>>>(b);
+    tc_kernel<MP, FUSED><<<unsigned(grid), kTT, TCfg<MP>::kDynSmem, s>>>(b);
     return cudaGetLastError() == cudaSuccess ? W12_OK : W12_ERR_CUDA;
 }
 
-template <int MP>
+template <int MP, bool FUSED = false>
 int occ_tc_t(int *blocks) {
-    if (cudaFuncSetAttribute(tc_kernel<MP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(tc_kernel<MP, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(TCfg<MP>::kDynSmem)) != cudaSuccess)
         return W12_ERR_CUDA;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, tc_kernel<MP>, kTT, TCfg<MP>::kDynSmem) ==
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, tc_kernel<MP, FUSED>, kTT, TCfg<MP>::kDynSmem) ==
                    cudaSuccess
                ? W12_OK
                : W12_ERR_CUDA;
@@ -345,6 +385,28 @@ int launch_tc_batch(const StreamBatch &b, int variant, int grid, void *stream) {
         case 1: return launch_tc_t<32>(b, grid, s);
         case 2: return launch_tc_t<64>(b, grid, s);
         case 3: return launch_tc_t<128>(b, grid, s);
+    }
+    return W12_ERR_ARG;
+}
+
+// The fused lm_head + verify variants (same v).
+int launch_tc_fused(const StreamBatch &b, int variant, int grid, void *stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    switch (variant) {
+        case 0: return launch_tc_t<16, true>(b, grid, s);
+        case 1: return launch_tc_t<32, true>(b, grid, s);
+        case 2: return launch_tc_t<64, true>(b, grid, s);
+        case 3: return launch_tc_t<128, true>(b, grid, s);
+    }
+    return W12_ERR_ARG;
+}
+
+int tc_fused_occupancy(int variant, int *blocks) {
+    switch (variant) {
+        case 0: return occ_tc_t<16, true>(blocks);
+        case 1: return occ_tc_t<32, true>(blocks);
+        case 2: return occ_tc_t<64, true>(blocks);
+        case 3: return occ_tc_t<128, true>(blocks);
     }
     return W12_ERR_ARG;
 }

@@ -49,9 +49,7 @@ struct StreamBatch {
 };
 
 // Kernel variants: v = 2 * log2(NT) + (ctas_per_sm - 1), NT = ceil(M / 8)
-// rounded up to a power of two (1..16).
-constexpr int kStreamVariants = 10;
-int stream_variant_valid(int v);
+// rounded up to a power of two (1..16); two CTAs per SM for NT <= 4.
 int stream_occupancy(int v, int *blocks_per_sm);
 // Fills the tensor map of x in g, for the mma.sync kernel (tc = false: one
 // 3-D box per group) or the tcgen05 kernel (tc = true: 2-D boxes of 64 k x
@@ -70,5 +68,7 @@ int launch_stream_fused(const StreamBatch &b, int variant, int grid, void *strea
 // v: MP = 16 << v tokens.
 int launch_tc_batch(const StreamBatch &b, int variant, int grid, void *stream);
 int tc_occupancy(int variant, int *blocks_per_sm);
+int launch_tc_fused(const StreamBatch &b, int variant, int grid, void *stream);
+int tc_fused_occupancy(int variant, int *blocks_per_sm);
 
 }  // namespace w12

@@ -29,25 +29,6 @@ __device__ __forceinline__ void bulk_copy(uint32_t dst, const void *src, uint32_
         : "memory");
 }
 
-// Meta word `word` (0..128) of the unit block at shared address ub.
-__device__ __forceinline__ uint32_t unit_meta(uint32_t ub, int word) {
-    return lds32(ub + uint32_t(kMetaAt + 4 * word));
-}
-
-__device__ __forceinline__ uint2 lds64(uint32_t addr) {
-    uint2 r;
-    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(addr));
-    return r;
-}
-
-__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar,
-                                       uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_addr(bar)), "l"(policy)
-        : "memory");
-}
 
 __device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2,
                                        uint64_t *bar) {
@@ -66,11 +47,6 @@ __device__ __forceinline__ void tma_2d_keep(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
-// Arrive on `bar` once every earlier cp.async of this thread has landed
-// (counts as one of the barrier's expected arrivals).
-__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t *bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
 
 __device__ __forceinline__ void prefetch_l1(const void *p) {
     asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
