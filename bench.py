@@ -312,7 +312,8 @@ def run_reference(args):
         "config": {"workload": WORKLOAD, "M": 1, "sample": f"every {every}th column of each GEMM"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"fp64 oracle GEMM on every {every}th column of each of the "
-                                   f"six layer weights, M=1; {total_w} weight-MACs per run"},
+                                   f"six layer weights, M=1; {total_w // args.steps} weight-MACs per step, "
+                                   f"{args.steps} steps"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
