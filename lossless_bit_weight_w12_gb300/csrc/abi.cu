@@ -137,8 +137,8 @@ int plan_batch(const w12_desc *d, int count, int64_t M, int path, BatchPlan *bp)
         if (!gemv_fits_32bit(&d[i])) return W12_ERR_SHAPE;
     }
     // Measured on the 27B-class layer (GB300, us per layer, GEMV / mma.sync
-    // / tcgen05): M = 1: 82.4 / 82.5 / 119, 16: - / 85.7 / 119,
-    // 32: - / 97.4 / 121, 64: - / 154 / 125, 128: - / 232 / 150.  At M = 1
+    // / tcgen05): M = 1: 82.4 / 82.5 / 107, 16: - / 85.7 / 107,
+    // 32: - / 97.4 / 110, 64: - / 154 / 113, 128: - / 232 / 148.  At M = 1
     // the weight stream is the whole cost and the CUDA-core GEMV does it
     // with the fewest tensor instructions; tcgen05 takes over above 32.
     if (path == W12_PATH_AUTO) path = M == 1 ? W12_PATH_GEMV : M <= 32 ? W12_PATH_MMA : W12_PATH_TC;

@@ -26,9 +26,12 @@
 //  - 1 producer warp (stream_producer).
 //  - 1 MMA warp: allocates and frees the tensor memory; its first thread
 //    issues the 8 UMMAs of every stage (M = 128 columns, N = MP tokens,
-//    K = 16: D += A_tmem . B_smem) once A and x are in place, and commits
-//    them to the barriers that release the stage, the A buffer and, after a
-//    piece's last stage, the accumulator.
+//    K = 16: D += A_tmem . B_smem) once A is in place (the decoders signal
+//    that only after they saw x land), and commits them to the barriers that
+//    release the stage, the A buffer and, after a piece's last stage, the
+//    accumulator.  This one thread is the path's limit: a K = 16 UMMA of
+//    M = 128 occupies the tensor core ~125 cycles at any N <= 128 (measured),
+//    so a unit costs ~1000 cycles however few tokens there are.
 // Tensor memory: A buffers at columns 0, 64, 128, 192, the accumulator at
 // 256 (MP columns); 512 columns allocated.  Four A buffers let the decoders
 // run up to four stages ahead of the UMMAs that read them.
@@ -185,7 +188,6 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
             const uint32_t idesc = idesc_bf16<MP>();
             SCur c = s_at(b, u0);
             int s = 0, i = 0, piece = 0;
-            uint32_t ph = 0;
             for (int u = u0; u < u1;) {
                 const StreamOne &g = b.g[c.gi];
                 const int first = g.ubase + c.nb * g.KG;
@@ -195,23 +197,25 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
                 tc_fence_after();
                 for (; u < ub; ++u, ++i) {
                     const uint32_t bA = uint32_t(i) % kABuf;
-                    mbar_wait(&full[s], ph, &s_abort, b.err);
+                    // The decoders that signal a_full waited for this stage's
+                    // full barrier first (x landed), so the UMMAs may read x
+                    // once a_full is observed: one wait instead of two on the
+                    // single thread that issues every UMMA of the SM (measured
+                    // ~10 % of the layer time at M <= 64).
                     mbar_wait(&a_full[bA], uint32_t(i / kABuf) & 1u, &s_abort, b.err);
                     tc_fence_after();
-                    const uint32_t st = base + uint32_t(s) * C::kStage;
+                    const uint64_t d0 = desc_sw128(base + uint32_t(s) * C::kStage);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
-                        const uint32_t xa = st + uint32_t(ks >> 2) * uint32_t(MP * 128) + 32u * uint32_t(ks & 3);
-                        umma_ts(tmem + kAccCol, tmem + bA * 64u + 8u * uint32_t(ks), desc_sw128(xa), idesc,
+                        // x box ks / 4 (k half), 16 k = 32 bytes per step inside the swizzle atom
+                        const uint64_t dx = d0 + uint64_t(((ks >> 2) * MP * 128 + 32 * (ks & 3)) >> 4);
+                        umma_ts(tmem + kAccCol, tmem + bA * 64u + 8u * uint32_t(ks), dx, idesc,
                                 (u != ua || ks != 0) ? 1u : 0u);
                     }
                     umma_commit(&empty[s]);
                     umma_commit(&a_free[bA]);
                     if (u == ub - 1) umma_commit(&acc_full);
-                    if (++s == S) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
+                    if (++s == S) s = 0;
                 }
                 ++piece;
                 s_next_tile(b, c);
