@@ -483,16 +483,8 @@ def run_w12(args):
                w12.encode(layer[gi]["w_np"], w12.LAYOUT_NK)[1])))}
     del w_dev, blob_enc
 
-    # ---- config 4 (64 layers + lm_head verify at M = 16), derived from the
-    # measured M = 16 layer step and the measured fused lm_head verify: the
-    # 64 layers stream 64 distinct weight sets, each larger than L2, so the
-    # measured step time carries over layer by layer
-    stack = None
-    if verify is not None and "16" in sweep:
-        us = 64 * sweep["16"]["us_per_layer"] + verify["us"]
-        stack = {"us_per_step": us, "tokens_per_s": 16 / (us * 1e-6),
-                 "gbs": (64 * nbytes + synth.weight_bytes_w12(5120, 151936)) / (us * 1e-6) / 1e9,
-                 "how": "64 x measured M=16 layer step + measured fused lm_head verify (derived)"}
+    # ---- config 4 measured: 64 distinct layers + the fused lm_head verify
+    stack = bench_stack(w12, torch, dev, args, barrier) if args.stack else None
 
     # ---- roofline of the dominant kernel: the step's single batched launch
     achieved = nbytes / t_launch / 1e9 if t_launch else None
@@ -535,7 +527,7 @@ def run_w12(args):
         "us_per_layer_by_path": by_path,
         "cublas_bf16": bf16_rows,
         "lmhead_verify": verify,
-        "stack_m16_estimate": stack,
+        "stack_m16": stack,
         "encode_device": enc,
         "cpu_baseline": cpu,
         "clocks": clk,
@@ -568,6 +560,86 @@ def bench_lmhead(w12, torch, dev, args, barrier):
     t = gl.run(barrier)
     b = synth.weight_bytes_w12(K, N)
     return {"us": 1e6 * t / n, "gbs": b * n / t / 1e9, "R": R, "T": T, "N": N, "K": K}
+
+
+def device_weights(torch, gen, K, N, dev):
+    """bf16 bit patterns [N, K] (int16) of the weight recipe (N(0, 0.02)
+    rounded to bf16, 1e-3 outliers x 64, 1e-4 of +-0 / subnormals), drawn
+    on the device with torch's seeded generator: the same distribution as
+    synth.weights, for timing workloads too large to draw on the host."""
+    w = (torch.randn((N, K), generator=gen, device=dev) * 0.02).to(torch.bfloat16)
+    out = torch.rand((N, K), generator=gen, device=dev) < 1e-3
+    w = torch.where(out, w * 64, w)
+    bits = w.view(torch.int16).to(torch.int32)
+    spec = torch.rand((N, K), generator=gen, device=dev) < 1e-4
+    man = torch.randint(1, 128, (N, K), generator=gen, device=dev, dtype=torch.int32)
+    zero = torch.rand((N, K), generator=gen, device=dev) < 0.5
+    sign = (torch.rand((N, K), generator=gen, device=dev) < 0.5).to(torch.int32) << 15
+    special = sign | torch.where(zero, torch.zeros_like(man), man)
+    bits = torch.where(spec, special, bits)
+    bits = torch.where(bits >= 32768, bits - 65536, bits)  # back to int16 range
+    return bits.to(torch.int16).contiguous()
+
+
+def bench_stack(w12, torch, dev, args, barrier):
+    """Config 4 measured: 64 decoder layers (six W12 linears each, one
+    batched launch per layer) + the fused lm_head (5120 -> 151936) greedy
+    verify, M = R*T = 16, every weight distinct and resident in HBM (about
+    34 GB of W12), weights drawn and encoded on the device.  One step = the
+    65 launches, captured in a CUDA graph."""
+    free, _ = torch.cuda.mem_get_info(dev)
+    need = 64 * _layer_bytes() * 1.03 + synth.weight_bytes_w12(5120, 151936) * 1.03 + 4e9
+    if free < need:
+        return {"skipped": f"needs {need / 1e9:.0f} GB of device memory, {free / 1e9:.0f} GB free"}
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4)
+    M = 16
+    t0 = time.perf_counter()
+    layers = []
+    for _ in range(synth.N_LAYERS_STACK):
+        descs, blobs = [], []
+        for name, K, N in synth.LAYER_SHAPES:
+            d, b = w12.encode_device(device_weights(torch, gen, K, N, dev))
+            descs.append(d)
+            blobs.append(b)
+        layers.append((descs, blobs))
+    K_lm, N_lm = synth.LM_HEAD_SHAPE[1], synth.LM_HEAD_SHAPE[2]
+    d_lm, b_lm = w12.encode_device(device_weights(torch, gen, K_lm, N_lm, dev))
+    torch.cuda.synchronize()
+    t_build = time.perf_counter() - t0
+    xs = [(torch.randn((M, K), generator=gen, device=dev)).to(torch.bfloat16).view(torch.int16)
+          for _, K, _ in synth.LAYER_SHAPES]
+    ys = [torch.empty((M, N), dtype=torch.float32, device=dev) for _, _, N in synth.LAYER_SHAPES]
+    ws = w12.workspace(w12.gemm_batched_workspace_size(layers[0][0], M), dev)
+    batches = [w12.GemmBatch(dl, bl, xs, ys, ws) for dl, bl in layers]
+    R, T = 1, 16
+    hidden = torch.randn((R * T, K_lm), generator=gen, device=dev).to(torch.bfloat16).view(torch.int16)
+    draft = torch.randint(0, N_lm, (R, T - 1), generator=gen, device=dev, dtype=torch.int32)
+    acc = torch.empty(R, dtype=torch.int32, device=dev)
+    nxt = torch.empty(R, dtype=torch.int32, device=dev)
+    ws_lm = w12.workspace(w12.verify_lmhead_workspace_size(d_lm, R, T), dev)
+
+    def step(mark=None):
+        for bt in batches:
+            bt()
+        w12.verify_greedy_lmhead(hidden, d_lm, b_lm, R, T, draft, acc, nxt, ws_lm)
+    n = 5
+    gw = GraphSteps(torch, step, 2)
+    gw.run(barrier)
+    del gw
+    g = GraphSteps(torch, step, n)
+    g.run(barrier)
+    t = g.run(barrier) / n
+    assert w12.get_device_error(ws) == 0 and w12.get_device_error(ws_lm) == 0
+    wbytes = 64 * _layer_bytes() + synth.weight_bytes_w12(K_lm, N_lm)
+    res = {"us_per_step": 1e6 * t, "tokens_per_s": R * T / t, "gbs": wbytes / t / 1e9,
+           "frac_of_peak": wbytes / t / 1e9 / _peaks()[0], "w12_weight_gb": wbytes / 1e9,
+           "launches_per_step": 65, "build_s": t_build,
+           "how": "64 batched layer launches + fused lm_head verify in one CUDA graph; weights drawn "
+                  "(seeded torch generator, the synth recipe's distribution) and encoded on the device"}
+    del g, batches, layers, b_lm
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_kernel_only(args):
@@ -615,6 +687,8 @@ def main():
     ap.add_argument("--impl", default="w12", choices=["w12", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-verify", dest="verify", action="store_false")
+    ap.add_argument("--no-stack", dest="stack", action="store_false",
+                    help="skip the measured 64-layer stack (config 4)")
     ap.add_argument("--kernel-only", default=None, help="time one layer GEMM by name, or \"layer\" for the batched layer (for ncu)")
     ap.add_argument("--m", type=int, default=1, help="tokens for --kernel-only")
     ap.add_argument("--path", type=int, default=0,
