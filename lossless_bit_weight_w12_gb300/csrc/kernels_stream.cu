@@ -150,6 +150,7 @@ __global__ void __launch_bounds__(kST, MINB) stream_kernel(const __grid_constant
     if (FUSED)
         for (int m = threadIdx.x; m < kMaxM; m += kST) s_best[m] = 0ull;
     __syncthreads();
+    if (threadIdx.x == 0) pdl_launch();
     if (!FUSED && u0 >= u1) return;
 
     if (warp == kCW) {
@@ -157,6 +158,7 @@ __global__ void __launch_bounds__(kST, MINB) stream_kernel(const __grid_constant
         stream_producer<S, false>(b, base, C::kStage, C::kX, C::MP, full, empty, &s_abort, u0, u1, lane);
         return;
     }
+    pdl_wait();  // nothing below touches global memory the previous kernel may write before this
 
     // ---------------------------------------------------------------- compute
     const int g8 = lane >> 2, t = lane & 3;
@@ -385,8 +387,7 @@ int x_map_tc(CUtensorMap *m, const uint16_t *x, int64_t K, int M, int MP) {
 
 template <int NT, int MINB, bool FUSED = false, int MT = 0>
 int launch_t(const StreamBatch &b, int grid, cudaStream_t s) {
-    stream_kernel<NT, MINB, FUSED, MT><<<unsigned(grid), kST, SRing<NT, MINB>::kDynSmem, s>>>(b);
-    return cudaGetLastError() == cudaSuccess ? W12_OK : W12_ERR_CUDA;
+    return launch_pdl(stream_kernel<NT, MINB, FUSED, MT>, grid, kST, SRing<NT, MINB>::kDynSmem, s, b);
 }
 
 template <int NT, int MINB, bool FUSED = false, int MT = 0>

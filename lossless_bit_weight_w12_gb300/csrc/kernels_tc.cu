@@ -176,11 +176,13 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
+    if (threadIdx.x == 0) pdl_launch();
 
     if (warp == kProdWarp) {
         if (u0 < u1) stream_producer<S, true>(b, base, C::kStage, C::kX, MP, full, empty, &s_abort, u0, u1, lane);
         return;
     }
+    pdl_wait();  // nothing below touches global memory the previous kernel may write before this
 
     if (warp == kMmaWarp) {
         // ------------------------------------------------------------ UMMA issuer
@@ -362,8 +364,7 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
 
 template <int MP, bool FUSED = false>
 int launch_tc_t(const StreamBatch &b, int grid, cudaStream_t s) {
-    tc_kernel<MP, FUSED><<<unsigned(grid), kTT, TCfg<MP>::kDynSmem, s>>>(b);
-    return cudaGetLastError() == cudaSuccess ? W12_OK : W12_ERR_CUDA;
+    return launch_pdl(tc_kernel<MP, FUSED>, grid, kTT, TCfg<MP>::kDynSmem, s, b);
 }
 
 template <int MP, bool FUSED = false>

@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_runtime.h>
 
 #include <cstddef>
 #include <cstdint>
@@ -70,5 +71,26 @@ int launch_tc_batch(const StreamBatch &b, int variant, int grid, void *stream);
 int tc_occupancy(int variant, int *blocks_per_sm);
 int launch_tc_fused(const StreamBatch &b, int variant, int grid, void *stream);
 int tc_fused_occupancy(int variant, int *blocks_per_sm);
+
+#ifdef __CUDACC__
+// Launch a stream kernel with programmatic stream serialization: it may
+// begin (and stream its first weights) while the previous kernel of the
+// stream finishes; the kernel itself waits for that kernel (griddepcontrol)
+// before it reads x or writes outputs.
+template <class Kernel>
+int launch_pdl(Kernel kernel, int grid, int threads, size_t smem, cudaStream_t s, const StreamBatch &b) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(grid));
+    cfg.blockDim = dim3(unsigned(threads));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, b) == cudaSuccess ? W12_OK : W12_ERR_CUDA;
+}
+#endif
 
 }  // namespace w12

@@ -147,6 +147,14 @@ __device__ __forceinline__ void stream_fixup(const StreamBatch &b, const StreamO
 }
 
 
+// Programmatic dependent launch: a stream kernel lets the next kernel of
+// the stream start as soon as this grid's CTAs free their SMs
+// (pdl_launch), and waits for the previous grid to complete, with its
+// memory visible, before it reads x or writes anything (pdl_wait).  Both
+// are no-ops for launches without the programmatic-serialization attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // The producer warp of a stream kernel: for every unit of [u0, u1), once
 // the stage's previous contents are released (empty[s]), lane 0 starts the
 // copies of the unit into ring stage s and arms full[s] (one arrival and the
@@ -156,6 +164,9 @@ __device__ __forceinline__ void stream_fixup(const StreamBatch &b, const StreamO
 //  - x at the stage start: one 3-D box (every token, both 64-k halves,
 //    mma.sync layout), or (TC) two 2-D boxes of 64 k x MP tokens, the
 //    second at MP * 128 bytes (the canonical K-major tcgen05 operand).
+// The weights are read-only, so the first ring's worth of unit blocks is
+// requested before pdl_wait (overlapping the previous kernel's tail); x,
+// which the previous kernel may have written, only after it.
 // At the start of every tile piece it prefetches the piece's escape entries
 // (a contiguous range of the escape list: escapes are listed by unit, and a
 // piece is consecutive units) into L1.
@@ -166,12 +177,8 @@ __device__ __forceinline__ void stream_producer(const StreamBatch &b, uint32_t b
     if (lane != 0) return;
     const uint64_t pol = l2_evict_first_policy();
     const uint32_t tx = uint32_t(x_bytes + kUnitBytes);
-    SCur c = s_at(b, u0);
-    int s = 0, issued = 0;
-    uint32_t ph = 0;
-    for (int u = u0; u < u1; ++u) {
+    auto issue_weights = [&](const SCur &c, int u, uint32_t st, uint64_t *bar) {
         const StreamOne &g = b.g[c.gi];
-        if (issued >= S && !mbar_wait(&empty[s], ph ^ 1u, abort, b.err)) break;
         const uint8_t *unit = g.units + size_t(uint32_t(c.nb) * uint32_t(g.KG) + uint32_t(c.kg)) * kUnitBytes;
         if (u == u0 || c.kg == 0) {
             // escape entries of this tile piece: from the first unit's first
@@ -192,15 +199,36 @@ __device__ __forceinline__ void stream_producer(const StreamBatch &b, uint32_t b
                 }
             }
         }
-        const uint32_t st = base + uint32_t(s) * uint32_t(stage_bytes);
-        mbar_expect_tx(&full[s], tx);
-        bulk_copy(st + uint32_t(x_bytes), unit, kUnitBytes, &full[s], pol);
+        mbar_expect_tx(bar, tx);
+        bulk_copy(st + uint32_t(x_bytes), unit, kUnitBytes, bar, pol);
+    };
+    auto issue_x = [&](const SCur &c, uint32_t st, uint64_t *bar) {
+        const StreamOne &g = b.g[c.gi];
         if (TC) {
-            tma_2d_keep(st, &g.tx, 128 * c.kg, 0, &full[s]);
-            tma_2d_keep(st + uint32_t(mp) * 128u, &g.tx, 128 * c.kg + 64, 0, &full[s]);
+            tma_2d_keep(st, &g.tx, 128 * c.kg, 0, bar);
+            tma_2d_keep(st + uint32_t(mp) * 128u, &g.tx, 128 * c.kg + 64, 0, bar);
         } else {
-            tma_3d(st, &g.tx, 0, 2 * c.kg, 0, &full[s]);
+            tma_3d(st, &g.tx, 0, 2 * c.kg, 0, bar);
         }
+    };
+    // the first ring's worth of weights, then the dependency, then their x
+    SCur c = s_at(b, u0);
+    const int P = min(S, u1 - u0);
+    SCur first_c[S];
+    for (int k = 0; k < P; ++k) {
+        first_c[k] = c;
+        issue_weights(c, u0 + k, base + uint32_t(k) * uint32_t(stage_bytes), &full[k]);
+        s_next(b, c);
+    }
+    pdl_wait();
+    for (int k = 0; k < P; ++k) issue_x(first_c[k], base + uint32_t(k) * uint32_t(stage_bytes), &full[k]);
+    int s = P == S ? 0 : P, issued = P;
+    uint32_t ph = P == S ? 1u : 0u;
+    for (int u = u0 + P; u < u1; ++u) {
+        if (!mbar_wait(&empty[s], ph ^ 1u, abort, b.err)) break;
+        const uint32_t st = base + uint32_t(s) * uint32_t(stage_bytes);
+        issue_weights(c, u, st, &full[s]);
+        issue_x(c, st, &full[s]);
         s_next(b, c);
         ++issued;
         if (++s == S) {
