@@ -27,14 +27,17 @@
 //  - 1 MMA warp: allocates and frees the tensor memory; its first thread
 //    issues the 8 UMMAs of every stage (M = 128 columns, N = MP tokens,
 //    K = 16: D += A_tmem . B_smem) once A is in place (the decoders signal
-//    that only after they saw x land), and commits them to the barriers that
-//    release the stage, the A buffer and, after a piece's last stage, the
-//    accumulator.  This one thread is the path's limit: a K = 16 UMMA of
-//    M = 128 occupies the tensor core ~125 cycles at any N <= 128 (measured),
-//    so a unit costs ~1000 cycles however few tokens there are.
-// Tensor memory: A buffers at columns 0, 64, 128, 192, the accumulator at
-// 256 (MP columns); 512 columns allocated.  Four A buffers let the decoders
-// run up to four stages ahead of the UMMAs that read them.
+//    that only after they saw x land), and commits them to the stage's
+//    empty barrier and, after a piece's last stage, to the accumulator's.
+// Tensor memory: the accumulator at column 0 (MP columns), then one A
+// buffer of 64 columns per ring stage; 512 columns allocated.  Tying the A
+// buffers to the stages lets one commit per unit release both: the
+// decoders that see a stage full again know that the UMMAs which read its
+// previous A buffer have completed (the producer refilled the stage only
+// after that commit).  On the issuing thread every mbarrier wait costs
+// ~200 cycles and every commit ~45 while its UMMAs are in flight (measured;
+// a K = 16 UMMA of M = 128 itself takes 45 cycles at N <= 32, 64 at
+// N = 128), so the thread waits once and commits once per unit.
 // Every mbarrier wait is bounded; after a timeout every role runs to its
 // end without waiting and the error word says W12_ERR_TIMEOUT.  The MMA
 // thread then waits (bounded) for its own UMMAs before the tensor memory is
@@ -54,9 +57,7 @@ constexpr int kDT = kDW * 32;
 constexpr int kProdWarp = kDW;           // producer
 constexpr int kMmaWarp = kDW + 1;        // tensor-memory owner, UMMA issuer
 constexpr int kTT = (kDW + 2) * 32;      // 576 threads
-constexpr int kABuf = 4;                 // A buffers in tensor memory (64 columns each)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCol = 64 * kABuf; // accumulator columns [256, 256 + MP)
 
 template <int MP>
 struct TCfg {
@@ -65,8 +66,11 @@ struct TCfg {
     static constexpr int kH = kX, kL = kX + kPlaneBlock, kE = kX + 2 * kPlaneBlock;
     static constexpr int kMeta = kX + kMetaAt;
     static constexpr int kFit = (227 * 1024 - 1024 - 2048) / kStage;
-    static constexpr int S = kFit > 8 ? 8 : kFit;
+    static constexpr int S = kFit > 7 ? 7 : kFit;
     static constexpr size_t kDynSmem = size_t(S) * kStage + 1024;
+    // tensor-memory columns: accumulator [0, MP), A buffer of stage s at kA + 64 s
+    static constexpr uint32_t kA = MP < 64 ? 64u : uint32_t(MP);
+    static_assert(kA + 64u * S <= kTmemCols, "A buffers exceed the tensor memory");
 };
 
 // UMMA shared-memory descriptor of a K-major operand with the 128-byte
@@ -136,7 +140,7 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
     using C = TCfg<MP>;
     constexpr int S = C::S;
     extern __shared__ unsigned char smem_dyn[];
-    __shared__ __align__(8) uint64_t full[S], empty[S], a_full[kABuf], a_free[kABuf], acc_full, acc_empty, fin;
+    __shared__ __align__(8) uint64_t full[S], empty[S], a_full[S], acc_full, acc_empty, fin;
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort, s_last;
     __shared__ unsigned long long s_best[FUSED ? MP : 1];
@@ -153,10 +157,7 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);  // the producer's expect_tx arrival (+ bytes)
             mbar_init(&empty[s], kDW / 2 + 1);  // one decoder group + the UMMA commit
-        }
-        for (int i = 0; i < kABuf; ++i) {
-            mbar_init(&a_full[i], kDW / 2);
-            mbar_init(&a_free[i], 1);
+            mbar_init(&a_full[s], kDW / 2);
         }
         mbar_init(&acc_full, 1);
         mbar_init(&acc_empty, kDW);
@@ -198,24 +199,20 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
                 if (piece > 0) mbar_wait(&acc_empty, uint32_t(piece - 1) & 1u, &s_abort, b.err);
                 tc_fence_after();
                 for (; u < ub; ++u, ++i) {
-                    const uint32_t bA = uint32_t(i) % kABuf;
                     // The decoders that signal a_full waited for this stage's
                     // full barrier first (x landed), so the UMMAs may read x
-                    // once a_full is observed: one wait instead of two on the
-                    // single thread that issues every UMMA of the SM (measured
-                    // ~10 % of the layer time at M <= 64).
-                    mbar_wait(&a_full[bA], uint32_t(i / kABuf) & 1u, &s_abort, b.err);
+                    // once a_full is observed: the only wait per unit.
+                    mbar_wait(&a_full[s], uint32_t(i / S) & 1u, &s_abort, b.err);
                     tc_fence_after();
                     const uint64_t d0 = desc_sw128(base + uint32_t(s) * C::kStage);
+                    const uint32_t ta = tmem + C::kA + 64u * uint32_t(s);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
                         // x box ks / 4 (k half), 16 k = 32 bytes per step inside the swizzle atom
                         const uint64_t dx = d0 + uint64_t(((ks >> 2) * MP * 128 + 32 * (ks & 3)) >> 4);
-                        umma_ts(tmem + kAccCol, tmem + bA * 64u + 8u * uint32_t(ks), dx, idesc,
-                                (u != ua || ks != 0) ? 1u : 0u);
+                        umma_ts(tmem, ta + 8u * uint32_t(ks), dx, idesc, (u != ua || ks != 0) ? 1u : 0u);
                     }
-                    umma_commit(&empty[s]);
-                    umma_commit(&a_free[bA]);
+                    umma_commit(&empty[s]);  // frees the stage and its A buffer
                     if (u == ub - 1) umma_commit(&acc_full);
                     if (++s == S) s = 0;
                 }
@@ -258,7 +255,8 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
         const bool valid = n < g.N;
         for (; u < ub; ++u, ++i) {
             if ((i & 1) == grp) {
-                const uint32_t bA = uint32_t(i) % kABuf;
+                // full also means the UMMAs that read this stage's A buffer
+                // last time have completed (their commit freed the stage)
                 mbar_wait(&full[s], ph, &s_abort, b.err);
                 const uint32_t st = base + uint32_t(s) * C::kStage;
                 const uint4 h0 = lds128(st + C::kH + p0), h1 = lds128(st + C::kH + p1);
@@ -278,13 +276,11 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
                     patch_escapes(wlo, mw.x, mw.y, uint32_t(64 * h), g.esc, g.n_esc, b.err);
                     patch_escapes(whi, mw.x, mw.y, uint32_t(64 * h + 32), g.esc, g.n_esc, b.err);
                 }
-                // the UMMAs of kABuf stages ago have finished reading this A buffer
-                if (i >= kABuf) mbar_wait(&a_free[bA], uint32_t(i / kABuf - 1) & 1u, &s_abort, b.err);
                 tc_fence_after();
-                tmem_st32(tmem + lane_off + bA * 64u + 32u * uint32_t(h), w);
+                tmem_st32(tmem + lane_off + C::kA + 64u * uint32_t(s) + 32u * uint32_t(h), w);
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&a_full[bA]);
+                if (lane == 0) mbar_arrive(&a_full[s]);
             }
             if (++s == S) {
                 s = 0;
@@ -300,7 +296,7 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
 #pragma unroll
         for (int q = 0; q < kHalf / 4; ++q) {
             uint32_t rr[4];
-            tmem_ld4(tmem + lane_off + kAccCol + uint32_t(qt * kHalf + 4 * q), rr);
+            tmem_ld4(tmem + lane_off + uint32_t(qt * kHalf + 4 * q), rr);
 #pragma unroll
             for (int e = 0; e < 4; ++e) v[4 * q + e] = __uint_as_float(rr[e]);
         }
