@@ -281,6 +281,13 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&a_full[s]);
+            } else if (S & 1) {
+                // With an odd ring a stage alternates between the groups, so
+                // this group's next wait on stage s would skip a phase; a
+                // parity wait can only tell the phase right after the one
+                // last seen.  Seeing the other group's fill land first keeps
+                // that true (the fill after it needs this group's release).
+                mbar_wait(&full[s], ph, &s_abort, b.err);
             }
             if (++s == S) {
                 s = 0;
