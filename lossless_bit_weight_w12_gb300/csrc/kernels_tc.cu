@@ -4,44 +4,50 @@
 // operand, the fp32 accumulator lives in tensor memory, and the tokens come
 // from shared memory.
 //
-// Work split, ring and producer are those of the mma.sync stream kernel
-// (stream_device.cuh): units of one 128-k group of a 128-column tile,
-// stream-K over the whole batch, one producer warp streaming the plane
-// blocks and x with the Tensor Memory Accelerator.  Here x comes as two
-// boxes of 64 k x MP tokens with the 128-byte swizzle: the canonical
-// K-major layout of the UMMA B operand.
+// Work split as in the mma.sync stream kernel (stream_device.cuh): units
+// of one 128-k group of a 128-column tile, stream-K over the whole batch.
+// Two rings feed a unit: the unit block (planes and meta words) lands in a
+// weight stage, and the unit's tokens -- two boxes of 64 k x MP tokens with
+// the 128-byte swizzle, the canonical K-major layout of the UMMA B operand
+// -- in a token slot.  A weight stage is free again once the decoders have
+// read it, a token slot only once the UMMAs that read it have completed, so
+// the two rings turn over at different rates; each has its own producer
+// warp.  Unit i of a CTA uses weight stage i % SW and token slot i % SX.
 //
-// Roles (one CTA per SM, 18 warps):
-//  - 16 decoder warps in two groups that take alternate stages, so two
-//    stages are decoded at once.  Thread (w, l) of a group owns tile row
+// Roles (one CTA per SM, 19 warps):
+//  - 16 decoder warps in two groups that take alternate units, so two
+//    units are decoded at once.  Thread (w, l) of a group owns tile row
 //    r = 32 (w % 4) + l (tensor-memory lane r) and half h = (w % 8) / 4 of
-//    the group's 128 k.  Per stage it rebuilds its 64 weights in registers
+//    the group's 128 k.  Per unit it rebuilds its 64 weights in registers
 //    ("reconstructing bit by bit in GEMM registers", SpecPilot summary,
 //    airadar.tv English edition, "Reasons" bullet 2), patches escapes, and
-//    stores them with tcgen05.st into the stage's A buffer (four buffers,
-//    used in turn; 64 columns, column j holding the bf16 pair k = 2j,
-//    2j + 1).  At the end of a tile piece all 16 warps read the accumulator
-//    back (tcgen05.ld; warp w takes a quarter w / 4 of the tokens) and write
-//    y or the stream-K partial slot, then run the fix-up.
-//  - 1 producer warp (stream_producer).
+//    stores them with tcgen05.st into the A buffer of the unit's token slot
+//    (64 columns, column j holding the bf16 pair k = 2j, 2j + 1).  At the
+//    end of a tile piece all 16 warps read the accumulator back (tcgen05.ld;
+//    warp w takes a quarter w / 4 of the tokens) and write y or the
+//    stream-K partial slot, then run the fix-up.
+//  - 1 weight producer warp: one bulk copy per unit block into the weight
+//    ring, and the L1 prefetch of each tile piece's escape entries.
+//  - 1 token producer warp: the two x boxes of each unit into the token ring.
 //  - 1 MMA warp: allocates and frees the tensor memory; its first thread
-//    issues the 8 UMMAs of every stage (M = 128 columns, N = MP tokens,
+//    issues the 8 UMMAs of every unit (M = 128 columns, N = MP tokens,
 //    K = 16: D += A_tmem . B_smem) once A is in place (the decoders signal
-//    that only after they saw x land), and commits them to the stage's
-//    empty barrier and, after a piece's last stage, to the accumulator's.
+//    that only after they saw the unit's tokens land), and commits them to
+//    the token slot's empty barrier and, after a piece's last unit, to the
+//    accumulator's.
 // Tensor memory: the accumulator at column 0 (MP columns), then one A
-// buffer of 64 columns per ring stage; 512 columns allocated.  Tying the A
-// buffers to the stages lets one commit per unit release both: the
-// decoders that see a stage full again know that the UMMAs which read its
-// previous A buffer have completed (the producer refilled the stage only
-// after that commit).  On the issuing thread every mbarrier wait costs
-// ~200 cycles and every commit ~45 while its UMMAs are in flight (measured;
-// a K = 16 UMMA of M = 128 itself takes 45 cycles at N <= 32, 64 at
-// N = 128), so the thread waits once and commits once per unit.
+// buffer of 64 columns per token slot; 512 columns allocated.  The slot's
+// commit releases both; decoders that see the slot full again know that
+// the UMMAs which read its A buffer last have completed (the producer
+// refilled the slot only after that commit).  On the issuing thread every
+// mbarrier wait costs ~200 cycles and every commit ~45 while its UMMAs are
+// in flight (measured; a K = 16 UMMA of M = 128 itself takes 45 cycles at
+// N <= 32, 64 at N = 128), so the thread waits once and commits once per
+// unit.
 // Every mbarrier wait is bounded; after a timeout every role runs to its
-// end without waiting and the error word says W12_ERR_TIMEOUT.  The MMA
-// thread then waits (bounded) for its own UMMAs before the tensor memory is
-// freed.
+// end without waiting and the error word says W12_ERR_TIMEOUT.  The
+// producers let their copies in flight land and the MMA thread waits
+// (bounded) for its own UMMAs before the tensor memory is freed.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -54,23 +60,25 @@ namespace {
 
 constexpr int kDW = 16;                  // decoder warps
 constexpr int kDT = kDW * 32;
-constexpr int kProdWarp = kDW;           // producer
-constexpr int kMmaWarp = kDW + 1;        // tensor-memory owner, UMMA issuer
-constexpr int kTT = (kDW + 2) * 32;      // 576 threads
+constexpr int kWProdWarp = kDW;          // weight producer
+constexpr int kXProdWarp = kDW + 1;      // token producer
+constexpr int kMmaWarp = kDW + 2;        // tensor-memory owner, UMMA issuer
+constexpr int kTT = (kDW + 3) * 32;      // 608 threads
 constexpr uint32_t kTmemCols = 512;
 
 template <int MP>
 struct TCfg {
-    static constexpr int kX = MP * 256;  // two boxes of MP rows x 128 bytes
-    static constexpr int kStage = (kX + kUnitBytes + 1023) / 1024 * 1024;
-    static constexpr int kH = kX, kL = kX + kPlaneBlock, kE = kX + 2 * kPlaneBlock;
-    static constexpr int kMeta = kX + kMetaAt;
-    static constexpr int kFit = (227 * 1024 - 1024 - 2048) / kStage;
-    static constexpr int S = kFit > 7 ? 7 : kFit;
-    static constexpr size_t kDynSmem = size_t(S) * kStage + 1024;
-    // tensor-memory columns: accumulator [0, MP), A buffer of stage s at kA + 64 s
+    static constexpr int kX = MP * 256;                        // token slot: two boxes of MP rows x 128 bytes
+    static constexpr int SX = MP >= 128 ? 3 : 4;               // token slots (and A buffers)
+    static constexpr int kXRing = SX * kX;                     // at the (1024-aligned) start of the ring
+    static constexpr int kW = (kUnitBytes + 127) / 128 * 128;  // weight stage stride
+    static constexpr int kFit = (227 * 1024 - 1024 - 2048 - kXRing) / kW;
+    static constexpr int SW = kFit > 8 ? 8 : kFit;             // weight stages, after the token ring
+    static constexpr size_t kDynSmem = size_t(kXRing) + size_t(SW) * kW + 1024;
+    // tensor-memory columns: accumulator [0, MP), A buffer of slot s at kA + 64 s
     static constexpr uint32_t kA = MP < 64 ? 64u : uint32_t(MP);
-    static_assert(kA + 64u * S <= kTmemCols, "A buffers exceed the tensor memory");
+    static_assert(kA + 64u * SX <= kTmemCols, "A buffers exceed the tensor memory");
+    static_assert(SW >= 2, "weight ring too shallow");
 };
 
 // UMMA shared-memory descriptor of a K-major operand with the 128-byte
@@ -131,6 +139,73 @@ __device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t (&r)[4]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Both rings signal a landed fill on a barrier of the decoder group that
+// owns the unit (full[2 s + (i & 1)] for unit i in slot s = i % S), so each
+// group waits on its own barriers only and sees their phases one by one.
+// The parity of unit i's fill on that barrier: the group's fills of slot s
+// are every fill of it (S even) or every other one (S odd).  A barrier
+// cannot run two phases ahead of its group: the fill after unit i's on the
+// same barrier needs the group's own release of unit i first.
+template <int S>
+__device__ __forceinline__ uint32_t group_parity(int i) {
+    const int k = i / S;
+    return uint32_t((S & 1) ? (k >> 1) : k) & 1u;
+}
+
+// Weight producer (lane 0 of its warp): unit i of the CTA into weight stage
+// i % SW, once the decoders have released the stage's previous unit.  The
+// weights are read-only, so nothing here waits for the previous kernel.
+template <int SW>
+__device__ __forceinline__ void tc_weight_producer(const StreamBatch &b, uint32_t wbase, uint32_t stride,
+                                                   uint64_t *full_w, uint64_t *empty_w, int *abort, int u0,
+                                                   int u1) {
+    const uint64_t pol = l2_evict_first_policy();
+    SCur c = s_at(b, u0);
+    int issued = 0;
+    for (int u = u0; u < u1; ++u) {
+        const int i = u - u0, s = i % SW;
+        if (i >= SW && !mbar_wait(&empty_w[s], uint32_t(i / SW - 1) & 1u, abort, b.err)) break;
+        const StreamOne &g = b.g[c.gi];
+        const uint8_t *unit = unit_block(g, c);
+        if (u == u0 || c.kg == 0) prefetch_piece_escapes(g, c, unit, u, u1);
+        uint64_t *bar = &full_w[2 * s + (i & 1)];
+        mbar_expect_tx(bar, uint32_t(kUnitBytes));
+        bulk_copy(wbase + uint32_t(s) * stride, unit, uint32_t(kUnitBytes), bar, pol);
+        s_next(b, c);
+        ++issued;
+    }
+    if (*reinterpret_cast<volatile int *>(abort))  // let the copies in flight land
+        for (int j = issued - 1; j >= 0 && j >= issued - SW; --j)
+            mbar_drain(&full_w[2 * (j % SW) + (j & 1)], group_parity<SW>(j));
+}
+
+// Token producer (lane 0 of its warp): the two 64-k boxes of unit i's tokens
+// into token slot i % SX, once the UMMAs that read the slot's previous unit
+// have completed.  x may be written by the previous kernel of the stream.
+template <int SX>
+__device__ __forceinline__ void tc_x_producer(const StreamBatch &b, uint32_t xbase, int mp, uint64_t *full_x,
+                                              uint64_t *empty_x, int *abort, int u0, int u1) {
+    pdl_wait();
+    const uint32_t kx = uint32_t(mp) * 256u;
+    SCur c = s_at(b, u0);
+    int issued = 0;
+    for (int u = u0; u < u1; ++u) {
+        const int i = u - u0, s = i % SX;
+        if (i >= SX && !mbar_wait(&empty_x[s], uint32_t(i / SX - 1) & 1u, abort, b.err)) break;
+        const StreamOne &g = b.g[c.gi];
+        const uint32_t dst = xbase + uint32_t(s) * kx;
+        uint64_t *bar = &full_x[2 * s + (i & 1)];
+        mbar_expect_tx(bar, kx);
+        tma_2d_keep(dst, &g.tx, 128 * c.kg, 0, bar);
+        tma_2d_keep(dst + uint32_t(mp) * 128u, &g.tx, 128 * c.kg + 64, 0, bar);
+        s_next(b, c);
+        ++issued;
+    }
+    if (*reinterpret_cast<volatile int *>(abort))
+        for (int j = issued - 1; j >= 0 && j >= issued - SX; --j)
+            mbar_drain(&full_x[2 * (j % SX) + (j & 1)], group_parity<SX>(j));
+}
+
 // FUSED: the lm_head + greedy verify epilogue (as in kernels_stream.cu):
 // tile outputs fold into a per-CTA running (value, lowest index) maximum
 // per token, split tiles are folded by the CTA that completes them, and the
@@ -138,13 +213,15 @@ __device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t (&r)[4]) {
 template <int MP, bool FUSED>
 __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ StreamBatch b) {
     using C = TCfg<MP>;
-    constexpr int S = C::S;
+    constexpr int SW = C::SW, SX = C::SX;
     extern __shared__ unsigned char smem_dyn[];
-    __shared__ __align__(8) uint64_t full[S], empty[S], a_full[S], acc_full, acc_empty, fin;
+    __shared__ __align__(8) uint64_t full_w[2 * SW], empty_w[SW], full_x[2 * SX], empty_x[SX], a_full[SX];
+    __shared__ __align__(8) uint64_t acc_full, acc_empty, fin;
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort, s_last;
     __shared__ unsigned long long s_best[FUSED ? MP : 1];
-    const uint32_t base = (smem_addr(smem_dyn) + 1023u) & ~1023u;
+    const uint32_t xbase = (smem_addr(smem_dyn) + 1023u) & ~1023u;  // token ring, then the weight ring
+    const uint32_t wbase = xbase + uint32_t(C::kXRing);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int u0, u1;
     {
@@ -154,10 +231,12 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
         u1 = u0 + per + (c < rem ? 1 : 0);
     }
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(&full[s], 1);  // the producer's expect_tx arrival (+ bytes)
-            mbar_init(&empty[s], kDW / 2 + 1);  // one decoder group + the UMMA commit
-            mbar_init(&a_full[s], kDW / 2);
+        for (int s = 0; s < 2 * SW; ++s) mbar_init(&full_w[s], 1);  // the producer's expect_tx arrival (+ bytes)
+        for (int s = 0; s < 2 * SX; ++s) mbar_init(&full_x[s], 1);
+        for (int s = 0; s < SW; ++s) mbar_init(&empty_w[s], kDW / 2);  // the decoder group of the unit
+        for (int s = 0; s < SX; ++s) {
+            mbar_init(&empty_x[s], 1);       // the UMMA commit
+            mbar_init(&a_full[s], kDW / 2);  // the decoder group of the unit
         }
         mbar_init(&acc_full, 1);
         mbar_init(&acc_empty, kDW);
@@ -179,8 +258,12 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
     const uint32_t tmem = s_tmem;
     if (threadIdx.x == 0) pdl_launch();
 
-    if (warp == kProdWarp) {
-        if (u0 < u1) stream_producer<S, true>(b, base, C::kStage, C::kX, MP, full, empty, &s_abort, u0, u1, lane);
+    if (warp == kWProdWarp) {
+        if (lane == 0 && u0 < u1) tc_weight_producer<SW>(b, wbase, C::kW, full_w, empty_w, &s_abort, u0, u1);
+        return;
+    }
+    if (warp == kXProdWarp) {
+        if (lane == 0 && u0 < u1) tc_x_producer<SX>(b, xbase, MP, full_x, empty_x, &s_abort, u0, u1);
         return;
     }
     pdl_wait();  // nothing below touches global memory the previous kernel may write before this
@@ -190,7 +273,7 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16<MP>();
             SCur c = s_at(b, u0);
-            int s = 0, i = 0, piece = 0;
+            int i = 0, piece = 0;
             for (int u = u0; u < u1;) {
                 const StreamOne &g = b.g[c.gi];
                 const int first = g.ubase + c.nb * g.KG;
@@ -199,22 +282,22 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
                 if (piece > 0) mbar_wait(&acc_empty, uint32_t(piece - 1) & 1u, &s_abort, b.err);
                 tc_fence_after();
                 for (; u < ub; ++u, ++i) {
-                    // The decoders that signal a_full waited for this stage's
-                    // full barrier first (x landed), so the UMMAs may read x
-                    // once a_full is observed: the only wait per unit.
-                    mbar_wait(&a_full[s], uint32_t(i / S) & 1u, &s_abort, b.err);
+                    const int sx = i % SX;
+                    // The decoders that signal a_full waited for this slot's
+                    // full barrier first (tokens landed), so the UMMAs may read
+                    // it once a_full is observed: the only wait per unit.
+                    mbar_wait(&a_full[sx], uint32_t(i / SX) & 1u, &s_abort, b.err);
                     tc_fence_after();
-                    const uint64_t d0 = desc_sw128(base + uint32_t(s) * C::kStage);
-                    const uint32_t ta = tmem + C::kA + 64u * uint32_t(s);
+                    const uint64_t d0 = desc_sw128(xbase + uint32_t(sx) * uint32_t(C::kX));
+                    const uint32_t ta = tmem + C::kA + 64u * uint32_t(sx);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
                         // x box ks / 4 (k half), 16 k = 32 bytes per step inside the swizzle atom
                         const uint64_t dx = d0 + uint64_t(((ks >> 2) * MP * 128 + 32 * (ks & 3)) >> 4);
                         umma_ts(tmem, ta + 8u * uint32_t(ks), dx, idesc, (u != ua || ks != 0) ? 1u : 0u);
                     }
-                    umma_commit(&empty[s]);  // frees the stage and its A buffer
+                    umma_commit(&empty_x[sx]);  // frees the token slot and its A buffer
                     if (u == ub - 1) umma_commit(&acc_full);
-                    if (++s == S) s = 0;
                 }
                 ++piece;
                 s_next_tile(b, c);
@@ -233,7 +316,7 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
 
     // ---------------------------------------------------------------- decoders
     const int r = 32 * (warp & 3) + lane;  // tile row = tensor-memory lane
-    const int grp = warp >> 3;             // stages of this parity
+    const int grp = warp >> 3;             // units of this parity
     const int h = (warp & 7) >> 2;         // k half of the group
     const int qt = warp >> 2;              // token quarter of the epilogue
     const uint32_t lane_off = uint32_t(32 * (warp & 3)) << 16;
@@ -245,8 +328,7 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
     const uint32_t p1 = uint32_t(r * 64) + ((uint32_t(2 * h + 1) ^ sw) << 4);
     const int M = b.M;
     SCur c = s_at(b, u0);
-    int s = 0, i = 0, piece = 0;
-    uint32_t ph = 0;
+    int i = 0, piece = 0;
     for (int u = u0; u < u1;) {
         const StreamOne &g = b.g[c.gi];
         const int nb = c.nb, first = g.ubase + nb * g.KG;
@@ -255,17 +337,16 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
         const bool valid = n < g.N;
         for (; u < ub; ++u, ++i) {
             if ((i & 1) == grp) {
-                // full also means the UMMAs that read this stage's A buffer
-                // last time have completed (their commit freed the stage)
-                mbar_wait(&full[s], ph, &s_abort, b.err);
-                const uint32_t st = base + uint32_t(s) * C::kStage;
-                const uint4 h0 = lds128(st + C::kH + p0), h1 = lds128(st + C::kH + p1);
-                const uint4 l0 = lds128(st + C::kL + p0), l1 = lds128(st + C::kL + p1);
-                const uint4 e0 = lds128(st + C::kE + p0), e1 = lds128(st + C::kE + p1);
-                const uint2 mw = make_uint2(lds32(st + C::kMeta + 4u * uint32_t(r)),
-                                            lds32(st + C::kMeta + 4u * uint32_t(r) + 4u));
+                const int s = i % SW, sx = i % SX;
+                mbar_wait(&full_w[2 * s + grp], group_parity<SW>(i), &s_abort, b.err);
+                const uint32_t st = wbase + uint32_t(s) * uint32_t(C::kW);
+                const uint4 h0 = lds128(st + p0), h1 = lds128(st + p1);
+                const uint4 l0 = lds128(st + kPlaneBlock + p0), l1 = lds128(st + kPlaneBlock + p1);
+                const uint4 e0 = lds128(st + 2 * kPlaneBlock + p0), e1 = lds128(st + 2 * kPlaneBlock + p1);
+                const uint2 mw = make_uint2(lds32(st + kMetaAt + 4u * uint32_t(r)),
+                                            lds32(st + kMetaAt + 4u * uint32_t(r) + 4u));
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[s]);  // planes and meta read
+                if (lane == 0) mbar_arrive(&empty_w[s]);  // planes and meta read
                 uint32_t w[32];
                 uint32_t(&wlo)[16] = *reinterpret_cast<uint32_t(*)[16]>(&w[0]);
                 uint32_t(&whi)[16] = *reinterpret_cast<uint32_t(*)[16]>(&w[16]);
@@ -276,22 +357,14 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
                     patch_escapes(wlo, mw.x, mw.y, uint32_t(64 * h), g.esc, g.n_esc, b.err);
                     patch_escapes(whi, mw.x, mw.y, uint32_t(64 * h + 32), g.esc, g.n_esc, b.err);
                 }
+                // the unit's tokens have landed, and with them the UMMAs that
+                // read this slot's A buffer last have completed
+                mbar_wait(&full_x[2 * sx + grp], group_parity<SX>(i), &s_abort, b.err);
                 tc_fence_after();
-                tmem_st32(tmem + lane_off + C::kA + 64u * uint32_t(s) + 32u * uint32_t(h), w);
+                tmem_st32(tmem + lane_off + C::kA + 64u * uint32_t(sx) + 32u * uint32_t(h), w);
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&a_full[s]);
-            } else if (S & 1) {
-                // With an odd ring a stage alternates between the groups, so
-                // this group's next wait on stage s would skip a phase; a
-                // parity wait can only tell the phase right after the one
-                // last seen.  Seeing the other group's fill land first keeps
-                // that true (the fill after it needs this group's release).
-                mbar_wait(&full[s], ph, &s_abort, b.err);
-            }
-            if (++s == S) {
-                s = 0;
-                ph ^= 1u;
+                if (lane == 0) mbar_arrive(&a_full[sx]);
             }
         }
 

@@ -147,6 +147,35 @@ __device__ __forceinline__ void stream_fixup(const StreamBatch &b, const StreamO
 }
 
 
+// The unit block of cursor c (format v2: unit t * KG + kg of the product).
+__device__ __forceinline__ const uint8_t *unit_block(const StreamOne &g, const SCur &c) {
+    return g.units + size_t(uint32_t(c.nb) * uint32_t(g.KG) + uint32_t(c.kg)) * kUnitBytes;
+}
+
+// At the start of a tile piece (units u .. of tile c.nb, ending at the
+// tile's last group or at u1), prefetch the piece's escape entries into
+// L1: escapes are listed by unit, so they are one contiguous range, from
+// the first unit's first column to the end of the piece's last unit.
+// At most kEscPrefetchLines lines.
+__device__ __forceinline__ void prefetch_piece_escapes(const StreamOne &g, const SCur &c, const uint8_t *unit,
+                                                       int u, int u1) {
+    const int first = g.ubase + c.nb * g.KG;
+    const int nunits = min(u1, first + g.KG) - u;
+    const uint32_t lo = ldg_u32(reinterpret_cast<const uint32_t *>(unit + kMetaAt)) >> 8;
+    const uint32_t hi = min(ldg_u32(reinterpret_cast<const uint32_t *>(unit + size_t(nunits - 1) * kUnitBytes +
+                                                                       kMetaAt + 4 * kTileN)) >> 8,
+                            g.n_esc);
+    if (lo < hi) {
+        const uintptr_t a0 = reinterpret_cast<uintptr_t>(g.esc + lo) & ~uintptr_t(127);
+        const uintptr_t a1 = reinterpret_cast<uintptr_t>(g.esc + hi);
+        for (int q = 0; q < kEscPrefetchLines; ++q) {
+            const uintptr_t a = a0 + uintptr_t(q) * 128u;
+            if (a >= a1) break;
+            prefetch_l1(reinterpret_cast<const void *>(a));
+        }
+    }
+}
+
 // Programmatic dependent launch: a stream kernel lets the next kernel of
 // the stream start as soon as this grid's CTAs free their SMs
 // (pdl_launch), and waits for the previous grid to complete, with its
@@ -179,26 +208,8 @@ __device__ __forceinline__ void stream_producer(const StreamBatch &b, uint32_t b
     const uint32_t tx = uint32_t(x_bytes + kUnitBytes);
     auto issue_weights = [&](const SCur &c, int u, uint32_t st, uint64_t *bar) {
         const StreamOne &g = b.g[c.gi];
-        const uint8_t *unit = g.units + size_t(uint32_t(c.nb) * uint32_t(g.KG) + uint32_t(c.kg)) * kUnitBytes;
-        if (u == u0 || c.kg == 0) {
-            // escape entries of this tile piece: from the first unit's first
-            // column to the end of the piece's last unit
-            const int first = g.ubase + c.nb * g.KG;
-            const int nunits = min(u1, first + g.KG) - u;
-            const uint32_t lo = ldg_u32(reinterpret_cast<const uint32_t *>(unit + kMetaAt)) >> 8;
-            const uint32_t hi = min(ldg_u32(reinterpret_cast<const uint32_t *>(
-                                        unit + size_t(nunits - 1) * kUnitBytes + kMetaAt + 4 * kTileN)) >> 8,
-                                    g.n_esc);
-            if (lo < hi) {
-                const uintptr_t a0 = reinterpret_cast<uintptr_t>(g.esc + lo) & ~uintptr_t(127);
-                const uintptr_t a1 = reinterpret_cast<uintptr_t>(g.esc + hi);
-                for (int q = 0; q < kEscPrefetchLines; ++q) {
-                    const uintptr_t a = a0 + uintptr_t(q) * 128u;
-                    if (a >= a1) break;
-                    prefetch_l1(reinterpret_cast<const void *>(a));
-                }
-            }
-        }
+        const uint8_t *unit = unit_block(g, c);
+        if (u == u0 || c.kg == 0) prefetch_piece_escapes(g, c, unit, u, u1);
         mbar_expect_tx(bar, tx);
         bulk_copy(st + uint32_t(x_bytes), unit, kUnitBytes, bar, pol);
     };
