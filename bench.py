@@ -33,6 +33,7 @@ from lossless_bit_weight_w12_gb300 import synth  # noqa: E402
 
 METRIC = "W12 GEMM effective weight GB/s (% of GB300 HBM peak) at M=1/16/32"
 UNIT = "GB/s"
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e nominal
 WORKLOAD = "27B-class dense decoder layer (q 5120->6144, k/v 5120->1024, o 6144->5120, " \
            "gate_up 5120->34816, down 17408->5120), W12 weights, M=1, seed 1"
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
@@ -145,6 +146,44 @@ def run_step(w12, layer, xs, ys, wss, mark=None):
         w12.gemm(g["desc"], g["blob"], xs[i], ys[i], wss[i])
         if done is not None:
             done()
+
+
+def step_distribution(torch, fn, nbytes, n=100, seed=0):
+    """n single steps, each between its own two events (eager launches):
+    the median step time and a bootstrap 95 % interval of the median."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    torch.cuda.synchronize()
+    for a, b in evs:
+        a.record()
+        fn()
+        b.record()
+    torch.cuda.synchronize()
+    t = np.array([a.elapsed_time(b) / 1e3 for a, b in evs])
+    med = float(np.median(t))
+    boots = np.median(np.random.default_rng(seed).choice(t, size=(2000, n), replace=True), axis=1)
+    lo, hi = np.percentile(boots, [2.5, 97.5])
+    return {"n": n, "median_us": 1e6 * med, "ci95_us": [1e6 * float(lo), 1e6 * float(hi)],
+            "min_us": 1e6 * float(t.min()), "gbs_at_median": nbytes / med / 1e9,
+            "how": "single eager launches, each between two events; bootstrap of the median (2000 resamples)"}
+
+
+def read_probe(torch, dev, gib=2, reps=10):
+    """Read-only streaming reference next to the copy peak: a torch sum over
+    `gib` GiB of int32 (each byte read once per pass)."""
+    buf = torch.ones(gib << 28, dtype=torch.int32, device=dev)
+    for _ in range(3):
+        buf.sum()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(reps):
+        buf.sum()
+    b.record()
+    torch.cuda.synchronize()
+    t = a.elapsed_time(b) / 1e3 / reps
+    nbytes = buf.numel() * 4
+    del buf
+    return {"gbs": nbytes / t / 1e9, "bytes": nbytes, "kind": f"torch sum over {gib} GiB int32 (read-only stream)"}
 
 
 def time_steps(torch, fn, steps, barrier):
@@ -409,6 +448,14 @@ def run_w12(args):
     for y_ref, y_e2e in zip(ys, yd):
         assert torch.equal(y_ref, y_e2e), "e2e result differs from the device-resident run"
 
+    # ---- the same step as single launches: median and its 95 % interval;
+    # the bytes the step actually moves (unit blocks with their meta words,
+    # escape lists, x, y); a read-only stream for reference
+    per_step = step_distribution(torch, batch, nbytes)
+    actual_bytes = (sum(int(d.total_bytes) for d in descs) + sum(x.numel() * 2 for x in x1)
+                    + sum(y.numel() * 4 for y in ys))
+    probe = read_probe(torch, dev) if rank == 0 else None
+
     # ---- sweep over M (same weights; inputs > L2): the AUTO path, and every
     # path that serves M (GEMV M <= 4, mma.sync, tcgen05), which shows where
     # the tensor-core tiles overtake the GEMV and tcgen05 overtakes mma.sync
@@ -515,6 +562,11 @@ def run_w12(args):
                    "l2": "inputs larger than L2 (511 MB of W12 weights streamed per step)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "frac_of_peak": value / world / hbm_peak,
+        "frac_of_nominal": value / world / NOMINAL_HBM_GBS,
+        "actual_bytes": {"per_step": actual_bytes, "gbs": actual_bytes / t_launch / 1e9,
+                         "what": "unit blocks (planes + meta words) + escape lists + x + y"},
+        "per_step_stats": per_step,
+        "read_probe": probe,
         "per_gemm_us": {k: 1e6 * v for k, v in per_gemm.items()},
         "unbatched_us_per_layer": 1e6 * t_sep,
         "timing": "K steps replayed from one CUDA graph (no event nodes inside); a step is one "
