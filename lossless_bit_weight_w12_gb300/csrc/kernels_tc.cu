@@ -14,7 +14,7 @@
 // the two rings turn over at different rates; each has its own producer
 // warp.  Unit i of a CTA uses weight stage i % SW and token slot i % SX.
 //
-// Roles (one CTA per SM, 19 warps):
+// Roles (one CTA per SM, 20 warps):
 //  - 16 decoder warps in two groups that take alternate units, so two
 //    units are decoded at once.  Thread (w, l) of a group owns tile row
 //    r = 32 (w % 4) + l (tensor-memory lane r) and half h = (w % 8) / 4 of
@@ -29,21 +29,23 @@
 //  - 1 weight producer warp: one bulk copy per unit block into the weight
 //    ring, and the L1 prefetch of each tile piece's escape entries.
 //  - 1 token producer warp: the two x boxes of each unit into the token ring.
-//  - 1 MMA warp: allocates and frees the tensor memory; its first thread
-//    issues the 8 UMMAs of every unit (M = 128 columns, N = MP tokens,
-//    K = 16: D += A_tmem . B_smem) once A is in place (the decoders signal
+//  - 2 MMA warps, one per unit parity (the first also allocates and frees
+//    the tensor memory): the first thread of each issues the 8 UMMAs of its
+//    units (M = 128 columns, N = MP tokens, K = 16: D_t += A_tmem . B_smem)
+//    into its own accumulator D_t once A is in place (the decoders signal
 //    that only after they saw the unit's tokens land), and commits them to
 //    the token slot's empty barrier and, after a piece's last unit, to the
-//    accumulator's.
-// Tensor memory: the accumulator at column 0 (MP columns), then one A
-// buffer of 64 columns per token slot; 512 columns allocated.  The slot's
-// commit releases both; decoders that see the slot full again know that
-// the UMMAs which read its A buffer last have completed (the producer
-// refilled the slot only after that commit).  On the issuing thread every
-// mbarrier wait costs ~200 cycles and every commit ~45 while its UMMAs are
-// in flight (measured; a K = 16 UMMA of M = 128 itself takes 45 cycles at
-// N <= 32, 64 at N = 128), so the thread waits once and commits once per
-// unit.
+//    accumulators' barrier.  The epilogue adds D_0 and D_1.
+// Tensor memory: the accumulators at columns 0 and MP, then one A buffer of
+// 64 columns per token slot; 512 columns allocated.  The slot's commit
+// releases both; decoders that see the slot full again know that the UMMAs
+// which read its A buffer last have completed (the producer refilled the
+// slot only after that commit).  A K = 16 UMMA of M = 128 takes 45 cycles
+// at N <= 32 and 64 at N = 128 (measured), but on its issuing thread every
+// mbarrier wait costs ~200 cycles and every commit ~45 while UMMAs are in
+// flight; with two issuers one's wait overlaps the other's UMMAs, and the
+// tensor core runs at the bare UMMA rate (measured: 44 cycles per UMMA
+// with a wait and a commit per 8, against 78 with one issuer).
 // Every mbarrier wait is bounded; after a timeout every role runs to its
 // end without waiting and the error word says W12_ERR_TIMEOUT.  The
 // producers let their copies in flight land and the MMA thread waits
@@ -62,8 +64,9 @@ constexpr int kDW = 16;                  // decoder warps
 constexpr int kDT = kDW * 32;
 constexpr int kWProdWarp = kDW;          // weight producer
 constexpr int kXProdWarp = kDW + 1;      // token producer
-constexpr int kMmaWarp = kDW + 2;        // tensor-memory owner, UMMA issuer
-constexpr int kTT = (kDW + 3) * 32;      // 608 threads
+constexpr int kMmaWarp = kDW + 2;        // tensor-memory owner, UMMA issuer of the even units
+constexpr int kMmaWarp1 = kDW + 3;       // UMMA issuer of the odd units
+constexpr int kTT = (kDW + 4) * 32;      // 640 threads
 constexpr uint32_t kTmemCols = 512;
 
 template <int MP>
@@ -75,8 +78,9 @@ struct TCfg {
     static constexpr int kFit = (227 * 1024 - 1024 - 2048 - kXRing) / kW;
     static constexpr int SW = kFit > 8 ? 8 : kFit;             // weight stages, after the token ring
     static constexpr size_t kDynSmem = size_t(kXRing) + size_t(SW) * kW + 1024;
-    // tensor-memory columns: accumulator [0, MP), A buffer of slot s at kA + 64 s
-    static constexpr uint32_t kA = MP < 64 ? 64u : uint32_t(MP);
+    // tensor-memory columns: accumulators [0, MP) and [MP, 2 MP), A buffer of
+    // slot s at kA + 64 s
+    static constexpr uint32_t kA = 2 * MP < 64 ? 64u : uint32_t(2 * MP);
     static_assert(kA + 64u * SX <= kTmemCols, "A buffers exceed the tensor memory");
     static_assert(SW >= 2, "weight ring too shallow");
 };
@@ -215,7 +219,7 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
     using C = TCfg<MP>;
     constexpr int SW = C::SW, SX = C::SX;
     extern __shared__ unsigned char smem_dyn[];
-    __shared__ __align__(8) uint64_t full_w[2 * SW], empty_w[SW], full_x[2 * SX], empty_x[SX], a_full[SX];
+    __shared__ __align__(8) uint64_t full_w[2 * SW], empty_w[SW], full_x[2 * SX], empty_x[SX], a_full[2 * SX];
     __shared__ __align__(8) uint64_t acc_full, acc_empty, fin;
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort, s_last;
@@ -234,13 +238,11 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
         for (int s = 0; s < 2 * SW; ++s) mbar_init(&full_w[s], 1);  // the producer's expect_tx arrival (+ bytes)
         for (int s = 0; s < 2 * SX; ++s) mbar_init(&full_x[s], 1);
         for (int s = 0; s < SW; ++s) mbar_init(&empty_w[s], kDW / 2);  // the decoder group of the unit
-        for (int s = 0; s < SX; ++s) {
-            mbar_init(&empty_x[s], 1);       // the UMMA commit
-            mbar_init(&a_full[s], kDW / 2);  // the decoder group of the unit
-        }
-        mbar_init(&acc_full, 1);
+        for (int s = 0; s < SX; ++s) mbar_init(&empty_x[s], 1);         // the unit's UMMA commit
+        for (int s = 0; s < 2 * SX; ++s) mbar_init(&a_full[s], kDW / 2);  // per decoder group, as full_x
+        mbar_init(&acc_full, 2);  // both issuers' commits after a piece's last unit
         mbar_init(&acc_empty, kDW);
-        mbar_init(&fin, 1);
+        mbar_init(&fin, 2);
         s_abort = 0;
         mbar_fence_init();
     }
@@ -268,35 +270,41 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
     }
     pdl_wait();  // nothing below touches global memory the previous kernel may write before this
 
-    if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ UMMA issuer
+    if (warp == kMmaWarp || warp == kMmaWarp1) {
+        // ----------------------------------------------------------- UMMA issuers
+        const int t = warp - kMmaWarp;  // units of parity t, accumulator t
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16<MP>();
+            const uint32_t dt = tmem + uint32_t(t * MP);
             SCur c = s_at(b, u0);
             int i = 0, piece = 0;
             for (int u = u0; u < u1;) {
                 const StreamOne &g = b.g[c.gi];
                 const int first = g.ubase + c.nb * g.KG;
-                const int ua = u, ub = min(u1, first + g.KG);
-                // the epilogue of the previous piece has read the accumulator
+                const int ub = min(u1, first + g.KG);
+                // the epilogue of the previous piece has read the accumulators
                 if (piece > 0) mbar_wait(&acc_empty, uint32_t(piece - 1) & 1u, &s_abort, b.err);
                 tc_fence_after();
+                bool fresh = true;  // this issuer's next UMMA starts its sum of the piece
                 for (; u < ub; ++u, ++i) {
-                    const int sx = i % SX;
-                    // The decoders that signal a_full waited for this slot's
-                    // full barrier first (tokens landed), so the UMMAs may read
-                    // it once a_full is observed: the only wait per unit.
-                    mbar_wait(&a_full[sx], uint32_t(i / SX) & 1u, &s_abort, b.err);
-                    tc_fence_after();
-                    const uint64_t d0 = desc_sw128(xbase + uint32_t(sx) * uint32_t(C::kX));
-                    const uint32_t ta = tmem + C::kA + 64u * uint32_t(sx);
+                    if ((i & 1) == t) {
+                        const int sx = i % SX;
+                        // The decoders that signal a_full waited for this
+                        // slot's full barrier first (tokens landed), so the
+                        // UMMAs may read it once a_full is observed.
+                        mbar_wait(&a_full[2 * sx + t], group_parity<SX>(i), &s_abort, b.err);
+                        tc_fence_after();
+                        const uint64_t d0 = desc_sw128(xbase + uint32_t(sx) * uint32_t(C::kX));
+                        const uint32_t ta = tmem + C::kA + 64u * uint32_t(sx);
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        // x box ks / 4 (k half), 16 k = 32 bytes per step inside the swizzle atom
-                        const uint64_t dx = d0 + uint64_t(((ks >> 2) * MP * 128 + 32 * (ks & 3)) >> 4);
-                        umma_ts(tmem, ta + 8u * uint32_t(ks), dx, idesc, (u != ua || ks != 0) ? 1u : 0u);
+                        for (int ks = 0; ks < 8; ++ks) {
+                            // x box ks / 4 (k half), 16 k = 32 bytes per step inside the swizzle atom
+                            const uint64_t dx = d0 + uint64_t(((ks >> 2) * MP * 128 + 32 * (ks & 3)) >> 4);
+                            umma_ts(dt, ta + 8u * uint32_t(ks), dx, idesc, (fresh && ks == 0) ? 0u : 1u);
+                        }
+                        fresh = false;
+                        umma_commit(&empty_x[sx]);  // frees the token slot and its A buffer
                     }
-                    umma_commit(&empty_x[sx]);  // frees the token slot and its A buffer
                     if (u == ub - 1) umma_commit(&acc_full);
                 }
                 ++piece;
@@ -308,9 +316,11 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
             if (piece > 0) mbar_wait(&acc_empty, uint32_t(piece - 1) & 1u, &s_abort, b.err);
         }
         __syncwarp();
-        tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
-                     : "memory");
+        if (warp == kMmaWarp) {
+            tc_fence_after();
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+                         : "memory");
+        }
         return;
     }
 
@@ -364,21 +374,27 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
                 tmem_st32(tmem + lane_off + C::kA + 64u * uint32_t(sx) + 32u * uint32_t(h), w);
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&a_full[sx]);
+                if (lane == 0) mbar_arrive(&a_full[2 * sx + grp]);
             }
         }
 
-        // ---- epilogue: accumulator row r, tokens [h MP/4, (h + 1) MP/4)
+        // ---- epilogue: accumulator row r, tokens [h MP/4, (h + 1) MP/4):
+        // D_0 + D_1, each only if its issuer had a unit in this piece
         mbar_wait(&acc_full, uint32_t(piece) & 1u, &s_abort, b.err);
         tc_fence_after();
+        const int cnt = ub - ua, ia = i - cnt;
+        const bool has0 = cnt >= 2 || (ia & 1) == 0, has1 = cnt >= 2 || (ia & 1) == 1;
         constexpr int kHalf = MP / 4;
         float v[kHalf];
 #pragma unroll
         for (int q = 0; q < kHalf / 4; ++q) {
-            uint32_t rr[4];
-            tmem_ld4(tmem + lane_off + uint32_t(qt * kHalf + 4 * q), rr);
+            uint32_t r0[4] = {0u, 0u, 0u, 0u}, r1[4] = {0u, 0u, 0u, 0u};
+            if (has0) tmem_ld4(tmem + lane_off + uint32_t(qt * kHalf + 4 * q), r0);
+            if (has1) tmem_ld4(tmem + lane_off + uint32_t(MP + qt * kHalf + 4 * q), r1);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) v[4 * q + e] = __uint_as_float(rr[e]);
+            for (int e = 0; e < 4; ++e)
+                v[4 * q + e] = has0 && has1 ? __uint_as_float(r0[e]) + __uint_as_float(r1[e])
+                                            : __uint_as_float(has0 ? r0[e] : r1[e]);
         }
         tc_fence_before();
         __syncwarp();

@@ -59,7 +59,7 @@ def gp(i, S, per_group):
     return ((k >> 1) if (S & 1) else k) & 1
 
 
-def run(SW, SX, n_units, KG, u0_off, seed, per_group=True, skip_wait=False):
+def run(SW, SX, n_units, KG, u0_off, seed, per_group=True, skip_wait=False, issuers=1):
     rnd = random.Random(seed)
     U = n_units
     # pieces: tiles of KG units, CTA range starts at offset u0_off inside a tile
@@ -71,8 +71,8 @@ def run(SW, SX, n_units, KG, u0_off, seed, per_group=True, skip_wait=False):
     full_x = [Bar(1) for _ in range(nfull * SX)]
     empty_w = [Bar(1) for _ in range(SW)]
     empty_x = [Bar(1) for _ in range(SX)]
-    a_full = [Bar(1) for _ in range(SX)]
-    acc_full, acc_empty = Bar(1), Bar(2)
+    a_full = [Bar(1) for _ in range((2 if issuers == 2 else 1) * SX)]
+    acc_full, acc_empty = Bar(issuers), Bar(2)
     wstage = [None] * SW  # content: ('fly', i) or ('ok', i)
     xslot = [None] * SX
     abuf = [None] * SX
@@ -120,7 +120,16 @@ def run(SW, SX, n_units, KG, u0_off, seed, per_group=True, skip_wait=False):
                 b.complete_tx(1)
             sched(rnd.randint(1, 25), land)
 
-    def MMA():
+    def abar(i):
+        return a_full[2 * (i % SX) + (i & 1)] if issuers == 2 else a_full[i % SX]
+
+    def apar(i):
+        return gp(i, SX, True) if issuers == 2 else (i // SX) & 1
+
+    last_done = [0, 0]  # per issuer: its UMMAs complete in issue order
+
+    def MMA(t):
+        """UMMA issuer t: every unit (issuers == 1) or the units of parity t."""
         piece = -1
         for i in range(U):
             if first_of_piece[i]:
@@ -128,26 +137,31 @@ def run(SW, SX, n_units, KG, u0_off, seed, per_group=True, skip_wait=False):
                 if piece > 0:
                     yield (acc_empty, (piece - 1) & 1)
                 assert (piece - 1) in epi_done or piece == 0
-            sx = i % SX
-            yield (a_full[sx], (i // SX) & 1)
-            assert xslot[sx] == ('ok', i), ('MMA x', i, xslot[sx])
-            assert abuf[sx] == i, ('MMA A', i, abuf[sx])
-            abuf_busy[sx] += 1
-            piece_pending[piece] = piece_pending.get(piece, 0) + 1
+            mine = issuers == 1 or (i & 1) == t
+            if mine:
+                sx = i % SX
+                yield (abar(i), apar(i))
+                assert xslot[sx] == ('ok', i), ('MMA x', i, xslot[sx])
+                assert abuf[sx] == i, ('MMA A', i, abuf[sx])
+                abuf_busy[sx] += 1
+                piece_pending[piece] = piece_pending.get(piece, 0) + 1
 
-            def done(sx=sx, i=i, p=piece, last=last_of_piece[i]):
-                assert xslot[sx] == ('ok', i) and abuf[sx] == i, ('UMMA operands changed', i)
-                abuf_busy[sx] -= 1
-                piece_pending[p] -= 1
-                empty_x[sx].arrive()
-                if last:
-                    acc_full.arrive()
-            # UMMAs complete in issue order
-            t = max(now[0] + rnd.randint(1, 30), MMA.last_done + 1)
-            MMA.last_done = t
-            seq[0] += 1
-            events.append((t, seq[0], done))
-    MMA.last_done = 0
+                def done(sx=sx, i=i, p=piece):
+                    assert xslot[sx] == ('ok', i) and abuf[sx] == i, ('UMMA operands changed', i)
+                    abuf_busy[sx] -= 1
+                    piece_pending[p] -= 1
+                    empty_x[sx].arrive()
+                # one issuer's UMMAs complete in issue order; the two
+                # issuers' interleave in any order
+                t_done = max(now[0] + rnd.randint(1, 30), last_done[t] + 1)
+                last_done[t] = t_done
+                seq[0] += 1
+                events.append((t_done, seq[0], done))
+            if last_of_piece[i]:
+                # the commit arrives once this issuer's UMMAs so far completed
+                t_done = max(now[0], last_done[t]) + 1
+                seq[0] += 1
+                events.append((t_done, seq[0], lambda: acc_full.arrive()))
 
     def DEC(grp):
         piece = 0
@@ -163,7 +177,7 @@ def run(SW, SX, n_units, KG, u0_off, seed, per_group=True, skip_wait=False):
                 assert abuf_busy[sx] == 0, ('A overwrite under UMMA', i)
                 assert xslot[sx] == ('ok', i), ('DEC x', i, xslot[sx])
                 abuf[sx] = i
-                a_full[sx].arrive()
+                abar(i).arrive()
             elif skip_wait:
                 s, sx = i % SW, i % SX
                 if SW & 1:
@@ -180,7 +194,9 @@ def run(SW, SX, n_units, KG, u0_off, seed, per_group=True, skip_wait=False):
                 piece += 1
     DEC.reads = {}
 
-    actors = {'WP': WP(), 'XP': XP(), 'MMA': MMA(), 'D0': DEC(0), 'D1': DEC(1)}
+    actors = {'WP': WP(), 'XP': XP(), 'D0': DEC(0), 'D1': DEC(1)}
+    for t in range(issuers):
+        actors[f'MMA{t}'] = MMA(t)
     waiting = {k: None for k in actors}
     sleeping = {}
     done = set()
@@ -242,6 +258,13 @@ def _cases(seeds):
 def test_ring_protocol_per_group_barriers():
     for SW, SX, n, KG, off, seed in _cases(40):
         assert run(SW, SX, n, KG, off, seed, per_group=True, skip_wait=False), (SW, SX, seed)
+
+
+def test_ring_protocol_two_issuers():
+    """Two UMMA issuers (even and odd units, one accumulator each), a_full
+    per decoder group and slot, acc_full with two arrivals."""
+    for SW, SX, n, KG, off, seed in _cases(40):
+        assert run(SW, SX, n, KG, off, seed, per_group=True, skip_wait=False, issuers=2), (SW, SX, seed)
 
 
 def test_model_catches_the_skip_wait_deadlock():
