@@ -114,12 +114,13 @@ def test_gemm_nonfinite(dev, w12mod, oracle):
         check_gemm(y, y_ref, s_ref, what=f"nonfinite path={path}")
 
 
-@pytest.mark.parametrize("path", [2, 3])
-def test_gemm_deterministic(dev, w12mod, path):
+@pytest.mark.parametrize("path,M", [(2, 16), (3, 16), (3, 64), (3, 128)])
+def test_gemm_deterministic(dev, w12mod, path, M):
     """Stream-K partial sums are added in a fixed order: repeated calls give
-    the same bits (K = 17408 spreads every column tile over several CTAs)."""
+    the same bits (K = 17408 spreads every column tile over several CTAs;
+    the tcgen05 rings are even at M = 16 and 64, odd at M = 128)."""
     import torch
-    K, N, M = 17408, 640, 16
+    K, N = 17408, 640
     rng = synth.streams(3, 2)
     w = synth.weights(rng[0], K, N)
     x = to_dev_bits(synth.activations(rng[1], M, K), dev)
@@ -134,11 +135,11 @@ def test_gemm_deterministic(dev, w12mod, path):
     assert torch.equal(ys[0], ys[1]) and torch.equal(ys[1], ys[2])
 
 
-@pytest.mark.parametrize("M", [1, 16, 32, 128])
+@pytest.mark.parametrize("M", [1, 16, 32, 64, 128])
 def test_gemm_full_layer_sampled(dev, w12mod, oracle, M):
     """Config-1..3 layer shapes at full size, in the launch configuration the
     bench times, checked on 24 sampled columns x all M rows each."""
-    seed = {1: 1, 16: 2, 32: 3, 128: 3}[M]
+    seed = {1: 1, 16: 2, 32: 3, 64: 3, 128: 3}[M]
     rng = synth.streams(seed, len(synth.LAYER_SHAPES) + 8)
     for i, (name, K, N) in enumerate(synth.LAYER_SHAPES):
         w = synth.weights(rng[i], K, N)
