@@ -3,17 +3,20 @@
 //
 // Loading a model through the host encoder means scanning every weight on a
 // few CPU cores; here the same three steps run on the device:
-//  1. scan: one warp per group (128 k of one column): the exponent
-//     histogram, the base (the window [b, b+14], b <= 240, holding the most
-//     exponents, the largest b on a tie) and the escape count 128 - cover;
+//  1. scan: one half-warp per group (128 k of one column): the base (the
+//     window [b, b+14], b <= 240, holding the most exponents, the largest b
+//     on a tie) and the escape count 128 - cover -- from the group's
+//     exponent range when it fits one window, else from its histogram;
 //  2. an exclusive scan of the escape counts in unit, then column order
 //     (the order of the escape list), giving every group's first escape;
-//  3. pack: one warp per (unit, column): lanes 0..15 build word q of the H,
-//     L and E planes (pos 8q .. 8q+7) and store it at its swizzled place;
+//  3. pack: one half-warp per (unit, column): lane q builds word q of the
+//     H, L and E planes (pos 8q .. 8q+7) and stores it at its swizzled place;
 //     escaped weights write their entries at first_escape + rank (ballot
 //     prefix); meta words follow.
-// Padding columns (past N) get base 0, no escapes and zero plane bytes (the
-// blob is zero-filled first).
+// Padding columns (past N) get base 0, no escapes and zero plane bytes; the
+// pack kernel writes every byte of the unit blocks, and the gap before the
+// escape list and the tail after it are zero-filled.  Both kernels keep the
+// loads of the next three groups in flight while they process one.
 #include <cuda_runtime.h>
 
 #include "async_common.cuh"
@@ -37,88 +40,107 @@ struct EncArgs {
     uint64_t off_esc, n_esc;
 };
 
-// The 4 weights pos 4l .. 4l+3 of group (n, kg) for lane l.
-__device__ __forceinline__ void load4(const EncArgs &a, int64_t n, int64_t kg, int lane, uint16_t (&v)[4]) {
-    const int64_t k0 = kg * kGroup + 4 * lane;
+// A group (128 k of one column) is handled by a half-warp: lane q = 0..15
+// of the half holds the 8 weights pos 8q .. 8q+7.  hmask: the half's lanes.
+__device__ __forceinline__ unsigned half_mask(int lane) { return lane < 16 ? 0x0000FFFFu : 0xFFFF0000u; }
+
+__device__ __forceinline__ void load8(const EncArgs &a, int64_t n, int64_t kg, int q, uint16_t (&v)[8]) {
+    const int64_t k0 = kg * kGroup + 8 * q;
     if (a.layout == W12_LAYOUT_NK) {
-        const uint2 q = *reinterpret_cast<const uint2 *>(a.w + n * a.K + k0);
-        v[0] = uint16_t(q.x);
-        v[1] = uint16_t(q.x >> 16);
-        v[2] = uint16_t(q.y);
-        v[3] = uint16_t(q.y >> 16);
+        const uint4 r = *reinterpret_cast<const uint4 *>(a.w + n * a.K + k0);  // 16-byte aligned: K % 128 == 0
+        const uint32_t wq[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[2 * i] = uint16_t(wq[i]);
+            v[2 * i + 1] = uint16_t(wq[i] >> 16);
+        }
     } else {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) v[i] = a.w[(k0 + i) * a.N + n];
+        for (int i = 0; i < 8; ++i) v[i] = a.w[(k0 + i) * a.N + n];
     }
 }
 
-// Base and escape count of one group, computed by a warp.  hist: this
-// warp's 256 shared counters.
-__device__ __forceinline__ void group_base_warp(const uint16_t (&v)[4], int lane, uint32_t *hist, uint32_t &b_out,
-                                                uint32_t &esc_out) {
+// Base and escape count of one group, computed by a half-warp.  When every
+// exponent lies in [emin, emin + 14] and emin <= 240, the window of the
+// largest base covering all 128 starts at emin: base emin, no escapes
+// (the common case).  Otherwise the exponent histogram (hist: the half's
+// 256 shared counters) gives cover(b) = #exp in [b, b+14] for every b <= 240,
+// and the best cover wins, the largest b on a tie.
+__device__ __forceinline__ void group_base_half(const uint16_t (&v)[8], int q, unsigned hmask, uint32_t *hist,
+                                                uint32_t &b_out, uint32_t &esc_out) {
+    uint32_t e[8], lo = 255u, hi = 0u;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) hist[lane * 8 + i] = 0u;
-    __syncwarp();
+    for (int i = 0; i < 8; ++i) {
+        e[i] = (v[i] >> 7) & 0xFFu;
+        lo = min(lo, e[i]);
+        hi = max(hi, e[i]);
+    }
+    lo = __reduce_min_sync(hmask, lo);
+    hi = __reduce_max_sync(hmask, hi);
+    if (hi - lo <= 14u && lo <= uint32_t(kMaxBase)) {
+        b_out = lo;
+        esc_out = 0u;
+        return;
+    }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) atomicAdd(&hist[(v[i] >> 7) & 0xFFu], 1u);
-    __syncwarp();
-    // inclusive prefix of the histogram: lane l owns bins 8l .. 8l+7
-    uint32_t p[8];
+    for (int i = 0; i < 16; ++i) hist[q * 16 + i] = 0u;
+    __syncwarp(hmask);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) atomicAdd(&hist[e[i]], 1u);
+    __syncwarp(hmask);
+    // inclusive prefix of the histogram: lane q owns bins 16q .. 16q+15
+    uint32_t p[16];
     uint32_t run = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        run += hist[lane * 8 + i];
+    for (int i = 0; i < 16; ++i) {
+        run += hist[q * 16 + i];
         p[i] = run;
     }
-    uint32_t excl = run;  // inclusive scan of the lane totals, then shift
+    uint32_t excl = run;  // inclusive scan of the lane totals over the half, then shift
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, excl, off);
-        if (lane >= off) excl += o;
+    for (int off = 1; off < 16; off <<= 1) {
+        const uint32_t o = __shfl_up_sync(hmask, excl, off, 16);
+        if (q >= off) excl += o;
     }
     excl -= run;
-    __syncwarp();
+    __syncwarp(hmask);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) hist[lane * 8 + i] = p[i] + excl;  // hist now holds prefix[e] = #exp <= e
-    __syncwarp();
-    // cover(b) = #exp in [b, b+14] = prefix[b+14] - prefix[b-1]; best cover,
-    // the largest b on ties: maximise (cover << 8 | b)
+    for (int i = 0; i < 16; ++i) hist[q * 16 + i] = p[i] + excl;  // hist[e] = #exp <= e
+    __syncwarp(hmask);
+    // maximise (cover << 8 | b): the best cover, the largest b on ties
     uint32_t best = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int b = lane * 8 + i;
-        if (b <= kMaxBase) {
-            const uint32_t hi = hist[b + 14];
-            const uint32_t lo = b > 0 ? hist[b - 1] : 0u;
-            const uint32_t key = ((hi - lo) << 8) | uint32_t(b);
+    for (int i = 0; i < 16; ++i) {
+        const int bb = q * 16 + i;
+        if (bb <= kMaxBase) {
+            const uint32_t top = hist[bb + 14];
+            const uint32_t below = bb > 0 ? hist[bb - 1] : 0u;
+            const uint32_t key = ((top - below) << 8) | uint32_t(bb);
             best = key > best ? key : best;
         }
     }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-        const uint32_t o = __shfl_xor_sync(0xFFFFFFFFu, best, off);
-        best = o > best ? o : best;
-    }
+    best = __reduce_max_sync(hmask, best);
     b_out = best & 0xFFu;
     esc_out = uint32_t(kGroup) - (best >> 8);
-    __syncwarp();
+    __syncwarp(hmask);  // the histogram is reused by the half's next group
 }
 
-// 1. bases and escape counts; one warp per (unit, column) slot.
+// 1. bases and escape counts; one half-warp per (unit, column) slot.
 __global__ void __launch_bounds__(256) enc_scan_kernel(const EncArgs a) {
-    __shared__ uint32_t hist[8][256];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __shared__ uint32_t hist[16][256];
+    const int lane = threadIdx.x & 31, q = lane & 15, half = threadIdx.x >> 4;
+    const unsigned hmask = half_mask(lane);
     const int64_t slots = a.U * kTileCols;
-    for (int64_t sl = int64_t(blockIdx.x) * 8 + warp; sl < slots; sl += int64_t(gridDim.x) * 8) {
+    for (int64_t sl = int64_t(blockIdx.x) * 16 + half; sl < slots; sl += int64_t(gridDim.x) * 16) {
         const int64_t u = sl / kTileCols, c = sl % kTileCols;
         const int64_t n = (u / a.KG) * kTileCols + c, kg = u % a.KG;
         uint32_t b = 0, e = 0;
-        if (n < a.N) {  // uniform across the warp
-            uint16_t v[4];
-            load4(a, n, kg, lane, v);
-            group_base_warp(v, lane, hist[warp], b, e);
+        if (n < a.N) {  // uniform across the half
+            uint16_t v[8];
+            load8(a, n, kg, q, v);
+            group_base_half(v, q, hmask, hist[half], b, e);
         }
-        if (lane == 0) {
+        if (q == 0) {
             a.base[sl] = uint8_t(b);
             a.count[sl] = e;
         }
@@ -198,93 +220,88 @@ __global__ void __launch_bounds__(kScanBlock) enc_scan_add(uint32_t *count, int6
     if (i < n) count[i] += block_sum[blockIdx.x];
 }
 
-// 3. pack; one warp per (unit, column) slot, lanes 0..15 one plane word each.
+// 3. pack; one half-warp per (unit, column) slot, lane q one word of each
+// plane (pos 8q .. 8q+7).
 __global__ void __launch_bounds__(256) enc_pack_kernel(const EncArgs a) {
     constexpr int kPermH[8] = {4, 0, 5, 1, 6, 2, 7, 3};
     constexpr int kPermL[8] = {0, 5, 1, 6, 2, 7, 3, 4};
     constexpr int kPermE[8] = {0, 4, 1, 5, 2, 6, 3, 7};
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int lane = threadIdx.x & 31, q = lane & 15, half = threadIdx.x >> 4;
+    const unsigned hmask = half_mask(lane);
     const int64_t slots = a.U * kTileCols;
     uint16_t *esc = reinterpret_cast<uint16_t *>(a.blob + a.off_esc);
-    for (int64_t sl = int64_t(blockIdx.x) * 8 + warp; sl < slots; sl += int64_t(gridDim.x) * 8) {
+    for (int64_t sl = int64_t(blockIdx.x) * 16 + half; sl < slots; sl += int64_t(gridDim.x) * 16) {
         const int64_t u = sl / kTileCols;
         const int c = int(sl % kTileCols);
         const int64_t n = (u / a.KG) * kTileCols + c, kg = u % a.KG;
+        const bool live = n < a.N;  // uniform across the half
         uint8_t *ub = a.blob + u * kUnitBytes;
         const uint32_t b = a.base[sl], begin = a.count[sl];
-        if (lane == 0) {
+        if (q == 0) {
             *reinterpret_cast<uint32_t *>(ub + kMetaAt + 4 * c) = b | (begin << 8);
             if (c == kTileCols - 1) {
                 const uint64_t next = u + 1 < a.U ? a.count[(u + 1) * kTileCols] : a.n_esc;
-                *reinterpret_cast<uint32_t *>(ub + kMetaAt + 4 * kTileCols) = uint32_t(next << 8);
+                uint32_t *tail = reinterpret_cast<uint32_t *>(ub + kMetaAt + 4 * kTileCols);
+                tail[0] = uint32_t(next << 8);
+                tail[1] = tail[2] = tail[3] = 0u;  // the unit block's last 12 bytes
             }
         }
-        if (n >= a.N) continue;  // padding column: zero planes (uniform across the warp)
-        // lane q < 16: the 8 weights pos 8q .. 8q+7
-        uint16_t v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        if (lane < 16) {
-            const int64_t k0 = kg * kGroup + 8 * lane;
-            if (a.layout == W12_LAYOUT_NK) {
-                const uint4 q = *reinterpret_cast<const uint4 *>(a.w + n * a.K + k0);
-                const uint32_t wq[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    v[2 * i] = uint16_t(wq[i]);
-                    v[2 * i + 1] = uint16_t(wq[i] >> 16);
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) v[i] = a.w[(k0 + i) * a.N + n];
-            }
-        }
+        const uint32_t off = uint32_t(c * 64 + (((q >> 2) ^ ((c >> 1) & 3)) << 4) + (q & 3) * 4);
         uint32_t hw = 0, lw = 0, ew = 0, flags = 0;
+        uint16_t v[8];
+        if (live) {
+            load8(a, n, kg, q, v);
 #pragma unroll
-        for (int s = 0; s < 8; ++s) {
-            const int jh = kPermH[s], jl = kPermL[s], je = kPermE[s];
-            const uint32_t smh = (uint32_t(v[jh] & 0x7Fu) << 1) | (uint32_t(v[jh ^ 1]) >> 15);
-            const uint32_t sml = (uint32_t(v[jl] & 0x7Fu) << 1) | (uint32_t(v[jl ^ 1]) >> 15);
-            const uint32_t ee = (v[je] >> 7) & 0xFFu;
-            const bool in = ee >= b && ee <= b + 14;
-            hw |= (smh >> 4) << (4 * s);
-            lw |= (sml & 0xFu) << (4 * s);
-            ew |= (in ? ee - b : 15u) << (4 * s);
-        }
+            for (int s = 0; s < 8; ++s) {
+                const int jh = kPermH[s], jl = kPermL[s], je = kPermE[s];
+                const uint32_t smh = (uint32_t(v[jh] & 0x7Fu) << 1) | (uint32_t(v[jh ^ 1]) >> 15);
+                const uint32_t sml = (uint32_t(v[jl] & 0x7Fu) << 1) | (uint32_t(v[jl ^ 1]) >> 15);
+                const uint32_t ee = (v[je] >> 7) & 0xFFu;
+                const bool in = ee >= b && ee <= b + 14;
+                hw |= (smh >> 4) << (4 * s);
+                lw |= (sml & 0xFu) << (4 * s);
+                ew |= (in ? ee - b : 15u) << (4 * s);
+            }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint32_t e = (v[i] >> 7) & 0xFFu;
-            if (lane < 16 && !(e >= b && e <= b + 14)) flags |= 1u << i;
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t e = (v[i] >> 7) & 0xFFu;
+                if (!(e >= b && e <= b + 14)) flags |= 1u << i;
+            }
         }
-        if (lane < 16) {
-            const uint32_t off = uint32_t(c * 64 + (((lane >> 2) ^ ((c >> 1) & 3)) << 4) + (lane & 3) * 4);
-            *reinterpret_cast<uint32_t *>(ub + off) = hw;
-            *reinterpret_cast<uint32_t *>(ub + kPlaneBlock + off) = lw;
-            *reinterpret_cast<uint32_t *>(ub + 2 * kPlaneBlock + off) = ew;
-        }
+        // every plane byte of the unit is written (zeros for padding columns)
+        *reinterpret_cast<uint32_t *>(ub + off) = hw;
+        *reinterpret_cast<uint32_t *>(ub + kPlaneBlock + off) = lw;
+        *reinterpret_cast<uint32_t *>(ub + 2 * kPlaneBlock + off) = ew;
         // escape entries in pos order: rank = escapes of earlier lanes + earlier bits
-        const uint32_t cnt = __popc(flags);
-        uint32_t before = cnt;
+        if (__any_sync(hmask, flags != 0u)) {
+            const uint32_t cnt = __popc(flags);
+            uint32_t before = cnt;
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, before, off);
-            if (lane >= off) before += o;
-        }
-        before -= cnt;
-        uint32_t at = begin + before;
-        for (int i = 0; i < 8; ++i) {
-            if (flags & (1u << i)) {
-                const uint32_t pos = uint32_t(8 * lane + i), e = (v[i] >> 7) & 0xFFu;
-                if (at < a.n_esc) esc[at] = uint16_t(pos | (e << 7));
-                ++at;
+            for (int o = 1; o < 16; o <<= 1) {
+                const uint32_t t = __shfl_up_sync(hmask, before, o, 16);
+                if (q >= o) before += t;
+            }
+            before -= cnt;
+            uint32_t at = begin + before;
+            for (int i = 0; i < 8; ++i) {
+                if (flags & (1u << i)) {
+                    const uint32_t pos = uint32_t(8 * q + i), e = (v[i] >> 7) & 0xFFu;
+                    if (at < a.n_esc) esc[at] = uint16_t(pos | (e << 7));
+                    ++at;
+                }
             }
         }
     }
 }
 
-int grid_for(int64_t slots) {
-    int sms = 0;
+// One wave of grid-stride blocks of 256 threads (16 slots per pass).
+template <class F>
+int grid_for(F kernel, int64_t slots) {
+    int sms = 0, per = 0;
     if (device_sm_count(&sms) != W12_OK) return -1;
-    const int64_t g = (slots + 7) / 8;
-    const int64_t cap = int64_t(sms) * 32;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kernel, 256, 0) != cudaSuccess || per < 1) return -1;
+    const int64_t g = (slots + 15) / 16;
+    const int64_t cap = int64_t(sms) * per;
     return int(g < cap ? (g > 0 ? g : 1) : cap);
 }
 
@@ -315,7 +332,7 @@ int launch_encode_scan(const uint16_t *w, int64_t K, int64_t N, int layout, void
     a.block_sum = reinterpret_cast<uint32_t *>(p + round256(uint64_t(slots)) + round256(uint64_t(slots) * 4u));
     *total_dev = a.block_sum + nb;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int grid = grid_for(slots);
+    const int grid = grid_for(enc_scan_kernel, slots);
     if (grid < 0) return W12_ERR_CUDA;
     enc_scan_kernel<<<unsigned(grid), 256, 0, s>>>(a);
     enc_scan_blocks<<<unsigned(nb), kScanBlock, 0, s>>>(a.count, slots, a.block_sum);
@@ -341,8 +358,15 @@ int launch_encode_pack(const uint16_t *w, const w12_desc *d, int layout, void *b
     a.off_esc = d->off_esc;
     a.n_esc = d->n_esc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(blob, 0, d->total_bytes, s) != cudaSuccess) return W12_ERR_CUDA;
-    const int grid = grid_for(slots);
+    // every byte of the unit blocks is written by the kernel; zero the rest:
+    // the gap before the escape list and the tail after it
+    uint8_t *bl = static_cast<uint8_t *>(blob);
+    const uint64_t units_end = d->n_units * uint64_t(kUnitBytes), esc_end = d->off_esc + 2u * d->n_esc;
+    if (d->off_esc > units_end && cudaMemsetAsync(bl + units_end, 0, d->off_esc - units_end, s) != cudaSuccess)
+        return W12_ERR_CUDA;
+    if (d->total_bytes > esc_end && cudaMemsetAsync(bl + esc_end, 0, d->total_bytes - esc_end, s) != cudaSuccess)
+        return W12_ERR_CUDA;
+    const int grid = grid_for(enc_pack_kernel, slots);
     if (grid < 0) return W12_ERR_CUDA;
     enc_pack_kernel<<<unsigned(grid), 256, 0, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? W12_OK : W12_ERR_CUDA;
