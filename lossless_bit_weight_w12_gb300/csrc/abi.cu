@@ -137,10 +137,11 @@ int plan_batch(const w12_desc *d, int count, int64_t M, int path, BatchPlan *bp)
         if (!gemv_fits_32bit(&d[i])) return W12_ERR_SHAPE;
     }
     // Measured on the 27B-class layer (GB300, us per layer, GEMV / mma.sync
-    // / tcgen05): M = 1: 82.4 / 82.5 / 107, 16: - / 85.7 / 107,
-    // 32: - / 97.4 / 110, 64: - / 154 / 113, 128: - / 232 / 148.  At M = 1
+    // / tcgen05): M = 1: 80.3 / 79.9 / 91.4, 16: - / 86.1 / 92.4,
+    // 32: - / 95.4 / 95.2, 64: - / 152 / 103, 128: - / 232 / 115.  At M = 1
     // the weight stream is the whole cost and the CUDA-core GEMV does it
-    // with the fewest tensor instructions; tcgen05 takes over above 32.
+    // with no tensor instructions; mma.sync and tcgen05 are level at 32,
+    // and tcgen05 takes over above it.
     if (path == W12_PATH_AUTO) path = M == 1 ? W12_PATH_GEMV : M <= 32 ? W12_PATH_MMA : W12_PATH_TC;
     if (path == W12_PATH_GEMV && M > 4) return W12_ERR_SHAPE;
     if (path != W12_PATH_GEMV && path != W12_PATH_MMA && path != W12_PATH_TC) return W12_ERR_ARG;

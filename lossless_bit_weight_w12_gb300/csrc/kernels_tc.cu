@@ -48,7 +48,7 @@
 // with a wait and a commit per 8, against 78 with one issuer).
 // Every mbarrier wait is bounded; after a timeout every role runs to its
 // end without waiting and the error word says W12_ERR_TIMEOUT.  The
-// producers let their copies in flight land and the MMA thread waits
+// producers let their copies in flight land and each MMA thread waits
 // (bounded) for its own UMMAs before the tensor memory is freed.
 #include <cuda.h>
 #include <cuda_runtime.h>
