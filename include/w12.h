@@ -22,6 +22,13 @@
  *  - Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
  *    default stream).  Device calls are asynchronous on that stream and never
  *    synchronise, except w12_get_device_error().
+ *  - The GEMM and fused-verify kernels use programmatic dependent launch:
+ *    they may start while the kernel launched just before them on the same
+ *    stream is finishing, and they start copying the weight blob (never x,
+ *    hidden, draft or a workspace) before they wait for it.  So a blob
+ *    written by that immediately preceding kernel must be set apart from the
+ *    call by another launch, an event or a synchronisation (w12_encode_device
+ *    ends with such a launch; copies and memsets need nothing).
  *  - Pointers named *_dev are device pointers, *_host host pointers.
  *  - Workspaces: a workspace of the size the matching *_workspace_size()
  *    call returns, 256-byte aligned, zero-filled by the caller before its

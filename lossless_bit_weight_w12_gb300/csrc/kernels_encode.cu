@@ -294,6 +294,12 @@ __global__ void __launch_bounds__(256) enc_pack_kernel(const EncArgs a) {
     }
 }
 
+// Launched in plain stream order after the pack kernel.  The next launch
+// on the stream may be a GEMM with programmatic dependent launch, whose
+// producers start copying the blob before they wait for the kernel before
+// them; with this one in between, the blob is complete and visible first.
+__global__ void enc_done_kernel() {}
+
 // One wave of grid-stride blocks of 256 threads (16 slots per pass).
 template <class F>
 int grid_for(F kernel, int64_t slots) {
@@ -369,6 +375,7 @@ int launch_encode_pack(const uint16_t *w, const w12_desc *d, int layout, void *b
     const int grid = grid_for(enc_pack_kernel, slots);
     if (grid < 0) return W12_ERR_CUDA;
     enc_pack_kernel<<<unsigned(grid), 256, 0, s>>>(a);
+    enc_done_kernel<<<1, 32, 0, s>>>();
     return cudaGetLastError() == cudaSuccess ? W12_OK : W12_ERR_CUDA;
 }
 
