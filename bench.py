@@ -186,6 +186,21 @@ def read_probe(torch, dev, gib=2, reps=10):
     return {"gbs": nbytes / t / 1e9, "bytes": nbytes, "kind": f"torch sum over {gib} GiB float32 (read-only stream)"}
 
 
+def max_over_ranks(torch, seconds, world, device):
+    """The slowest rank's time, on every rank (`seconds` itself at N = 1)."""
+    if world == 1:
+        return seconds
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_step, steps, world, seconds):
+    """Whole-job throughput of N replicas: every rank's units over the
+    slowest rank's time."""
+    return world * units_per_step * steps / seconds
+
+
 def time_steps(torch, fn, steps, barrier):
     """Eager timing: K calls of fn between two events on the current stream."""
     start = torch.cuda.Event(enable_timing=True)
@@ -415,11 +430,8 @@ def run_w12(args):
     dt = gsteps.run(barrier)
     clk = clocks.stop()
     t_launch = dt / args.steps
-    if world > 1:
-        t = torch.tensor([dt], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        dt = float(t.item())
-    value = world * nbytes * args.steps / dt / 1e9
+    dt = max_over_ranks(torch, dt, world, dev)
+    value = whole_job_rate(nbytes, args.steps, world, dt) / 1e9
     assert w12.get_device_error(ws_b) == 0
     del gsteps, gwarm
 
@@ -452,7 +464,7 @@ def run_w12(args):
         pin_y.copy_(yd_all, non_blocking=True)
     for _ in range(2):
         e2e_step()
-    dt_e2e = time_steps(torch, e2e_step, args.steps, barrier)
+    dt_e2e = max_over_ranks(torch, time_steps(torch, e2e_step, args.steps, barrier), world, dev)
     h2d = pin_x.numel() * pin_x.element_size()
     d2h = pin_y.numel() * pin_y.element_size()
     batch()
@@ -584,7 +596,7 @@ def run_w12(args):
         "unbatched_us_per_layer": 1e6 * t_sep,
         "timing": "K steps replayed from one CUDA graph (no event nodes inside); a step is one "
                   "batched launch; per-GEMM times from a separate unbatched graph with event nodes",
-        "e2e": {"value": world * nbytes * args.steps / dt_e2e / 1e9, "unit": UNIT,
+        "e2e": {"value": whole_job_rate(nbytes, args.steps, world, dt_e2e) / 1e9, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps,
         "roofline": roofline,
@@ -744,7 +756,7 @@ def run_kernel_only(args):
                       "gbs": synth.weight_bytes_w12(K, N) * args.steps / t / 1e9}))
 
 
-def main():
+def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
@@ -758,9 +770,14 @@ def main():
     ap.add_argument("--m", type=int, default=1, help="tokens for --kernel-only")
     ap.add_argument("--path", type=int, default=0,
                     help="--kernel-only: 0 auto, 1 GEMV, 2 mma.sync, 3 tcgen05")
-    args = ap.parse_args()
+    args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
+    return args
+
+
+def main():
+    args = parse_args()
     if args.kernel_only:
         run_kernel_only(args)
     elif args.impl == "reference":
