@@ -143,7 +143,7 @@ def make_bufs(w12, dev, layer, M):
 def run_step(w12, layer, xs, ys, wss, mark=None):
     for i, g in enumerate(layer):
         done = mark(g["name"]) if mark is not None else None
-        w12.gemm(g["desc"], g["blob"], xs[i], ys[i], wss[i])
+        w12.gemm(g["desc"], g["blob"], xs[i], ys[i], wss[i], path=w12.OPT_EARLY_WEIGHTS)
         if done is not None:
             done()
 
@@ -310,37 +310,141 @@ def traffic_for(kernel_key):
 
 # ----------------------------------------------------------------- CPU oracle
 
-def oracle_prepare(every, seed=1):
+def oracle_prepare(every, seed=1, M=1, xseed=None, weights=None, parts=1):
     """The oracle's own encoding of every `every`-th column of each of the
-    layer's six weights, with the M = 1 activations (set-up, not timed)."""
+    layer's six weights (seed `seed`, or the given [N, K] arrays), split
+    into `parts` disjoint column ranges, with M activations drawn from the
+    bench's stream for (xseed, M) (set-up, not timed).  Returns one work
+    list per part: (desc, blob, x, weight-MACs)."""
     import oracle
+    xseed = seed if xseed is None else xseed
     rng = synth.streams(seed, len(synth.LAYER_SHAPES) + 8)
-    xr = synth.streams(seed * 1000 + 1, len(synth.LAYER_SHAPES))
-    work = []
+    xr = synth.streams(xseed * 1000 + M, len(synth.LAYER_SHAPES))
+    out = [[] for _ in range(parts)]
     for i, (name, K, N) in enumerate(synth.LAYER_SHAPES):
+        w = weights[i] if weights is not None else synth.weights(rng[i], K, N)
+        x = synth.activations(xr[i], M, K)
         cols = np.arange(0, N, every)
-        w = synth.weights(rng[i], K, N)[cols]
-        x = synth.activations(xr[i], 1, K)
-        d, blob = oracle.encode(w, oracle.LAYOUT_NK)
-        work.append((d, blob, x, K * len(cols)))
-    return work
+        for p, cp in enumerate(np.array_split(cols, parts)):
+            if cp.size == 0:
+                continue
+            d, blob = oracle.encode(w[cp], oracle.LAYOUT_NK)
+            out[p].append(("gemm", (d, blob, x), M * K * len(cp)))
+    return out
 
 
 def oracle_run(work, min_seconds=0.0):
-    """Time the oracle's fp64 W12 GEMM over the prepared sample, in whole
-    passes until at least `min_seconds` have elapsed (one pass at least).
-    Returns (effective GB/s at 1.5 B per weight, weights, seconds)."""
+    """Time the oracle over a work list in whole passes until at least
+    `min_seconds` have elapsed (one pass at least).  Returns (units, seconds)
+    where units are weight-MACs (GEMM items) or verifies."""
     import oracle
     t0 = time.perf_counter()
-    nw = 0
+    n = 0
     while True:
-        for d, blob, x, n in work:
-            oracle.gemm(d, blob, x)
-            nw += n
+        for kind, args, units in work:
+            if kind == "gemm":
+                oracle.gemm(*args)
+            else:
+                oracle.verify_greedy(*args)
+            n += units
         dt = time.perf_counter() - t0
         if dt >= min_seconds:
             break
-    return 1.5 * nw / dt / 1e9, nw, dt
+    return n, dt
+
+
+def _oracle_proc(work, min_seconds, conn, go):
+    """One host process of the all-core oracle timing."""
+    sys.path.insert(0, ROOT)
+    import oracle
+    oracle.lib()
+    oracle_run(work[:1])  # warm (page in the library and the data)
+    conn.send("ready")
+    go.wait()
+    conn.send(oracle_run(work, min_seconds))
+    conn.close()
+
+
+def oracle_parallel(parts, min_seconds):
+    """The oracle, as it stands, on len(parts) host processes at once (each
+    on its own disjoint share of the work, started with spawn); the
+    timed region runs from the common start to the last process's end.
+    Returns (units, seconds)."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    go = ctx.Event()
+    procs, conns = [], []
+    for work in parts:
+        a, b = ctx.Pipe(duplex=False)
+        p = ctx.Process(target=_oracle_proc, args=(work, min_seconds, b, go), daemon=True)
+        p.start()
+        procs.append(p)
+        conns.append(a)
+    for c in conns:
+        assert c.recv() == "ready"
+    t0 = time.perf_counter()
+    go.set()
+    res = [c.recv() for c in conns]
+    wall = time.perf_counter() - t0
+    for p in procs:
+        p.join(timeout=30)
+    return sum(n for n, _ in res), wall
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline_protocol(layer_w, seconds=2.5):
+    """The oracle on the host's cores, 1 thread and all cores, on four
+    workloads: config 0 (K = N = 1024, M = 1), a config-1 layer at M = 1
+    (every 16th column of the six weights), a config-2 layer at M = 16 (the
+    same weights and columns, seed-2 activations: the oracle's time depends
+    only on the shapes; every 64th column), and config-4 verify on logits (R = 1, T = 16,
+    V = 151936, fp32; all cores: independent verifies, one per process).
+    GEMM rates are effective weight GB/s at 1.5 B per weight of the GEMM
+    (1.5 K N per pass, whatever M); verify rates are verifies per second."""
+    import oracle
+    oracle.lib()
+    cores = cpu_cores()
+    out = {}
+
+    def measure(name, parts_all, unit_scale, unit, what):
+        n1, t1 = oracle_run(parts_all[0] if len(parts_all) == 1 else sum(parts_all, []), seconds)
+        nall, tall = oracle_parallel(parts_all, seconds)
+        out[name] = {"unit": unit, "what": what,
+                     "threads_1": {"value": unit_scale(n1, t1), "units": n1, "seconds": t1},
+                     "cores_all": {"value": unit_scale(nall, tall), "units": nall, "seconds": tall,
+                                   "processes": len(parts_all)}}
+
+    def gbs(M):
+        return lambda n, t: 1.5 * n / M / t / 1e9
+
+    # config 0
+    r0 = synth.streams(0, 2)
+    w0 = synth.weights(r0[0], 1024, 1024)
+    x0 = synth.activations(r0[1], 1, 1024)
+    parts0 = []
+    for cp in np.array_split(np.arange(1024), cores):
+        d, blob = oracle.encode(w0[cp], oracle.LAYOUT_NK)
+        parts0.append([("gemm", (d, blob, x0), 1024 * len(cp))])
+    measure("config0", parts0, gbs(1), "GB/s", "K=N=1024, M=1, every output")
+    # config-1 layer, M = 1; config-2 layer, M = 16
+    measure("config1_layer_m1", oracle_prepare(16, seed=1, M=1, weights=layer_w, parts=cores), gbs(1), "GB/s",
+            "27B-class layer, M=1, every 16th column of each weight")
+    measure("config2_layer_m16", oracle_prepare(64, seed=1, M=16, xseed=2, weights=layer_w, parts=cores),
+            gbs(16), "GB/s", "27B-class layer, M=16 (seed-2 activations), every 64th column of each weight")
+    # config-4 verify on logits
+    r4 = synth.streams(4, 3)
+    V, R, T = synth.LM_HEAD_SHAPE[2], 1, 16
+    lg = synth.logits(r4[0], R * T, V)
+    dr = synth.draft_tokens(r4[1], oracle.argmax(lg).reshape(R, T), R, T, V)
+    measure("config4_verify_logits", [[("verify", (lg, R, T, dr), 1)] for _ in range(cores)],
+            lambda n, t: n / t, "verifies/s", "R=1, T=16, V=151936 fp32 logits")
+    return cores, out
 
 
 # ----------------------------------------------------------------- arms
@@ -353,23 +457,27 @@ def dist_setup(args):
 
 
 def run_reference(args):
+    """The oracle as it stands, on all the host's cores (one process per
+    core over disjoint column ranges), on a bounded sample of the same
+    workload: each step the fp64 oracle GEMM on every 16th column of each of
+    the six layer weights at M = 1."""
     world, rank, _ = dist_setup(args)
     if rank != 0:
         return
     from oracle import build as ob
     ob.build()
     every = 16
-    work = oracle_prepare(every)
+    cores = cpu_cores()
+    parts = oracle_prepare(every, parts=cores)
     # warm-up steps (untimed), then K timed steps, each a bounded sample
     for _ in range(args.warmup):
-        oracle_run(work[:1])
+        oracle_run(parts[0][:1])
     total_w, total_t = 0, 0.0
     for _ in range(args.steps):
-        _, nw, dt = oracle_run(work)
+        nw, dt = oracle_parallel(parts, 0.0)
         total_w += nw
         total_t += dt
     value = 1.5 * total_w / total_t / 1e9
-    cores = 1
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total_t / args.steps,
@@ -378,8 +486,8 @@ def run_reference(args):
         "config": {"workload": WORKLOAD, "M": 1, "sample": f"every {every}th column of each GEMM"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"fp64 oracle GEMM on every {every}th column of each of the "
-                                   f"six layer weights, M=1; {total_w // args.steps} weight-MACs per step, "
-                                   f"{args.steps} steps"},
+                                   f"six layer weights, M=1, split over {cores} host processes; "
+                                   f"{total_w // args.steps} weight-MACs per step, {args.steps} steps"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -420,7 +528,11 @@ def run_w12(args):
     descs = [g["desc"] for g in layer]
     blobs = [g["blob"] for g in layer]
     ws_b = w12.workspace(w12.gemm_batched_workspace_size(descs, 1), dev)
-    batch = w12.GemmBatch(descs, blobs, x1, ys, ws_b)
+    # The layer's weights are written once, before the timed region, so the
+    # early weight stream (W12_OPT_EARLY_WEIGHTS) is safe here and is what a
+    # serving loop over resident weights uses.
+    EARLY = w12.OPT_EARLY_WEIGHTS
+    batch = w12.GemmBatch(descs, blobs, x1, ys, ws_b, EARLY)
 
     gsteps = GraphSteps(torch, lambda mark: batch(), args.steps)
     gwarm = GraphSteps(torch, lambda mark: batch(), args.warmup)
@@ -445,32 +557,74 @@ def run_w12(args):
         assert w12.get_device_error(wsb) == 0
 
     # ---- e2e: through the public API with host buffers, copies inside.
-    # The six x live in one pinned host buffer and one device buffer (one
-    # host->device copy per step), the six y in one device buffer (one
-    # device->host copy per step).
+    # Every step copies its six x from pinned host memory to the device (one
+    # copy) and its six y back (one copy).  Two sets of device buffers and
+    # three streams pipeline the steps: step i's host->device copy and step
+    # i-1's device->host copy run under step i-1's / step i's weight stream;
+    # events keep every buffer's reuse ordered.
     xsz = [x.numel() for x in x1]
     ysz = [y.numel() for y in ys]
     pin_x = torch.cat([x.reshape(-1) for x in x1]).cpu().pin_memory()
-    pin_y = torch.empty(sum(ysz), dtype=torch.float32).pin_memory()
-    xd_all = torch.empty_like(pin_x, device=dev)
-    yd_all = torch.empty(sum(ysz), dtype=torch.float32, device=dev)
-    xd = [v.view(x.shape) for v, x in zip(torch.split(xd_all, xsz), x1)]
-    yd = [v.view(y.shape) for v, y in zip(torch.split(yd_all, ysz), ys)]
-    batch_e2e = w12.GemmBatch(descs, blobs, xd, yd, ws_b)
+    pin_y = [torch.empty(sum(ysz), dtype=torch.float32).pin_memory() for _ in range(2)]
+    xd_all = [torch.empty_like(pin_x, device=dev) for _ in range(2)]
+    yd_all = [torch.empty(sum(ysz), dtype=torch.float32, device=dev) for _ in range(2)]
+    yd = [[v.view(y.shape) for v, y in zip(torch.split(yd_all[k], ysz), ys)] for k in range(2)]
+    batch_e2e = [w12.GemmBatch(descs, blobs, [v.view(x.shape) for v, x in zip(torch.split(xd_all[k], xsz), x1)],
+                               yd[k], ws_b, EARLY) for k in range(2)]
+    s_comp = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    x_free = [None, None]   # kernel k done reading xd[k]
+    y_free = [None, None]   # copy-out of yd[k] done
 
-    def e2e_step():
-        xd_all.copy_(pin_x, non_blocking=True)
-        batch_e2e()
-        pin_y.copy_(yd_all, non_blocking=True)
-    for _ in range(2):
-        e2e_step()
-    dt_e2e = max_over_ranks(torch, time_steps(torch, e2e_step, args.steps, barrier), world, dev)
+    def e2e_steps(n):
+        """n pipelined steps; returns after enqueueing (the compute stream
+        waits for the last copy-out)."""
+        for i in range(n):
+            k = i & 1
+            with torch.cuda.stream(s_in):
+                if x_free[k] is not None:
+                    s_in.wait_event(x_free[k])
+                xd_all[k].copy_(pin_x, non_blocking=True)
+                x_in = ev()
+                x_in.record(s_in)
+            s_comp.wait_event(x_in)
+            if y_free[k] is not None:
+                s_comp.wait_event(y_free[k])
+            batch_e2e[k](s_comp)
+            done = ev()
+            done.record(s_comp)
+            x_free[k] = done
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(done)
+                pin_y[k].copy_(yd_all[k], non_blocking=True)
+                out = ev()
+                out.record(s_out)
+            y_free[k] = out
+        s_comp.wait_stream(s_out)
+
+    def time_e2e(n):
+        start = torch.cuda.Event(enable_timing=True)
+        stop = torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        start.record(s_comp)
+        s_in.wait_stream(s_comp)
+        e2e_steps(n)
+        stop.record(s_comp)
+        torch.cuda.synchronize()
+        barrier()
+        return start.elapsed_time(stop) / 1000.0
+    e2e_steps(3)
+    torch.cuda.synchronize()
+    dt_e2e = max_over_ranks(torch, time_e2e(args.steps), world, dev)
     h2d = pin_x.numel() * pin_x.element_size()
-    d2h = pin_y.numel() * pin_y.element_size()
+    d2h = pin_y[0].numel() * pin_y[0].element_size()
     batch()
     torch.cuda.synchronize()
-    for y_ref, y_e2e in zip(ys, yd):
-        assert torch.equal(y_ref, y_e2e), "e2e result differs from the device-resident run"
+    last = (args.steps - 1) & 1
+    for y_ref, y_e2e in zip(ys, torch.split(pin_y[last], ysz)):
+        assert torch.equal(y_ref.cpu().reshape(-1), y_e2e), "e2e result differs from the device-resident run"
 
     # ---- the same step as single launches: median and its 95 % interval;
     # the bytes the step actually moves (unit blocks with their meta words,
@@ -488,7 +642,7 @@ def run_w12(args):
     n = max(3, args.steps // 2)
 
     def time_layer(xsM, ysM, wsBM, path):
-        bM = w12.GemmBatch(descs, blobs, xsM, ysM, wsBM, path)
+        bM = w12.GemmBatch(descs, blobs, xsM, ysM, wsBM, path | EARLY)
         gM = GraphSteps(torch, lambda mark: bM(), n)
         gM.run(barrier)
         t = gM.run(barrier)
@@ -570,14 +724,14 @@ def run_w12(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        import oracle
-        oracle.lib()
-        every = 4
-        v, nw, tcpu = oracle_run(oracle_prepare(every), min_seconds=10.0)
-        cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"fp64 oracle GEMM on every {every}th column of each of the six layer "
-                         f"weights at M=1, whole passes for >= 10 s ({nw} weight-MACs, {tcpu:.1f} s, "
-                         f"one host thread)"}
+        cores, wl = cpu_baseline_protocol([g["w_np"] for g in layer])
+        head = wl["config1_layer_m1"]["cores_all"]
+        cpu = {"value": head["value"], "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": "fp64 oracle GEMM on every 16th column of each of the six layer weights at "
+                         f"M=1, {cores} host processes over disjoint column ranges, whole passes for "
+                         f">= 2.5 s ({head['units']} weight-MACs in {head['seconds']:.1f} s); the "
+                         "workloads below also on one thread",
+               "workloads": wl}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -585,6 +739,7 @@ def run_w12(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "M": 1, "w12_bytes_per_step": nbytes,
                    "l2": "inputs larger than L2 (511 MB of W12 weights streamed per step)",
+                   "launch": "W12_OPT_EARLY_WEIGHTS (weights resident, written before the timed region)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "frac_of_peak": value / world / hbm_peak,
         "frac_of_nominal": value / world / NOMINAL_HBM_GBS,
@@ -597,7 +752,10 @@ def run_w12(args):
         "timing": "K steps replayed from one CUDA graph (no event nodes inside); a step is one "
                   "batched launch; per-GEMM times from a separate unbatched graph with event nodes",
         "e2e": {"value": whole_job_rate(nbytes, args.steps, world, dt_e2e) / 1e9, "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "how": "public API (w12_gemm_batched) with pinned host buffers; per step one host->device "
+                       "copy of x and one device->host copy of y inside the timed region, pipelined over two "
+                       "buffer sets (copy-in, compute and copy-out streams ordered by events); eager launches"},
         "gpu_launches": args.steps,
         "roofline": roofline,
         "sweep": sweep,
@@ -688,7 +846,7 @@ def bench_stack(w12, torch, dev, args, barrier):
           for _, K, _ in synth.LAYER_SHAPES]
     ys = [torch.empty((M, N), dtype=torch.float32, device=dev) for _, _, N in synth.LAYER_SHAPES]
     ws = w12.workspace(w12.gemm_batched_workspace_size(layers[0][0], M), dev)
-    batches = [w12.GemmBatch(dl, bl, xs, ys, ws) for dl, bl in layers]
+    batches = [w12.GemmBatch(dl, bl, xs, ys, ws, w12.OPT_EARLY_WEIGHTS) for dl, bl in layers]
     R, T = 1, 16
     hidden = torch.randn((R * T, K_lm), generator=gen, device=dev).to(torch.bfloat16).view(torch.int16)
     draft = torch.randint(0, N_lm, (R, T - 1), generator=gen, device=dev, dtype=torch.int32)
@@ -732,7 +890,7 @@ def run_kernel_only(args):
         descs = [g["desc"] for g in layer]
         ys = [torch.empty((args.m, g["N"]), dtype=torch.float32, device=dev) for g in layer]
         ws = w12.workspace(w12.gemm_batched_workspace_size(descs, args.m), dev)
-        b = w12.GemmBatch(descs, [g["blob"] for g in layer], xs[args.m], ys, ws, args.path)
+        b = w12.GemmBatch(descs, [g["blob"] for g in layer], xs[args.m], ys, ws, args.path | w12.OPT_EARLY_WEIGHTS)
         for _ in range(args.warmup):
             b()
         t = time_steps(torch, b, args.steps, lambda: None)

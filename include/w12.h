@@ -24,11 +24,16 @@
  *    synchronise, except w12_get_device_error().
  *  - The GEMM and fused-verify kernels use programmatic dependent launch:
  *    they may start while the kernel launched just before them on the same
- *    stream is finishing, and they start copying the weight blob (never x,
- *    hidden, draft or a workspace) before they wait for it.  So a blob
- *    written by that immediately preceding kernel must be set apart from the
- *    call by another launch, an event or a synchronisation (w12_encode_device
- *    ends with such a launch; copies and memsets need nothing).
+ *    stream is finishing, but by default they read nothing in global memory
+ *    (blob, x, hidden, draft, workspace) before that kernel has completed,
+ *    so any producer of their inputs is safe.  The GEMM calls take one
+ *    option, W12_OPT_EARLY_WEIGHTS (OR-ed into the path argument of the
+ *    _ex calls): the first weight copies then start before the wait, under
+ *    the previous kernel's tail; the caller promises that the blob was not
+ *    written by the kernel launched just before the call on the same stream
+ *    (another launch, an event or a synchronisation in between suffices;
+ *    w12_encode_device ends with such a launch; copies and memsets are not
+ *    kernels and need nothing).
  *  - Pointers named *_dev are device pointers, *_host host pointers.
  *  - Workspaces: a workspace of the size the matching *_workspace_size()
  *    call returns, 256-byte aligned, zero-filled by the caller before its
@@ -81,6 +86,11 @@ extern "C" {
                            in tensor memory, M <= 128                                    */
 
 #define W12_MAX_M 128
+
+/* Option bit of the path argument of w12_gemm_ex / w12_gemm_batched_ex:
+ * start streaming the weights before the previous kernel of the stream has
+ * completed (see the conventions above).  Default off. */
+#define W12_OPT_EARLY_WEIGHTS 0x100
 
 /*
  * Descriptor of one encoded K x N matrix (format v2).
@@ -148,6 +158,12 @@ int w12_version(void);
 /* --------------------------------------------------------------------- */
 
 /*
+ * Defined by: the W12 format (SpecPilot summary, airadar.tv English edition,
+ * "Reasons" bullet 2: BF16 split into three 4-bit planes; hotrepo.ai
+ * StargazerX0/SpecPilot page, "项目介绍" paragraph 2: lossless, decoded
+ * bit-exactly).  The group size, base rule, escape list and packing are this
+ * library's reading (the format description above).
+ *
  * Size the blob for a bf16 matrix w (host, layout W12_LAYOUT_KN or _NK,
  * K % 128 == 0; K or N may be 0).  Fills every field of *d, counting the
  * escapes.  Errors: W12_ERR_ARG, W12_ERR_SHAPE, W12_ERR_TOO_MANY_ESCAPES.
@@ -156,6 +172,8 @@ int w12_version(void);
 int w12_encode_plan(const uint16_t *w_host, int64_t K, int64_t N, int layout, w12_desc *d);
 
 /*
+ * Defined by: as w12_encode_plan ("Reasons" bullet 2; "项目介绍" paragraph 2).
+ *
  * Encode w into blob_host (d->total_bytes bytes, any alignment; padding is
  * written as zeros).  *d must come from w12_encode_plan on the same w.
  * Errors: W12_ERR_ARG (d does not match w), W12_ERR_SHAPE.
@@ -164,6 +182,9 @@ int w12_encode(const uint16_t *w_host, int64_t K, int64_t N, int layout, const w
                void *blob_host);
 
 /*
+ * Defined by: the format description above (this library's reading of
+ * "Reasons" bullet 2).
+ *
  * Check a host blob against its descriptor: the offsets and sizes, base
  * range, meta monotonicity and sentinel, escape positions and order, that
  * every code-15 nibble has exactly one escape entry and that every escape is
@@ -182,6 +203,8 @@ int w12_validate(const w12_desc *d, const void *blob_host);
 size_t w12_encode_device_workspace_size(int64_t K, int64_t N);
 
 /*
+ * Defined by: as w12_encode_plan ("Reasons" bullet 2; "项目介绍" paragraph 2).
+ *
  * w12_encode_plan on the GPU, for weights already in device memory (a model
  * loaded straight to HBM: no pass over the weights on the host).  w_dev: the
  * bf16 matrix in layout W12_LAYOUT_KN or _NK, 16-byte aligned.  Computes
@@ -197,6 +220,8 @@ int w12_encode_plan_device(const uint16_t *w_dev, int64_t K, int64_t N, int layo
                            void *ws_dev, size_t ws_bytes, void *stream);
 
 /*
+ * Defined by: as w12_encode ("Reasons" bullet 2; "项目介绍" paragraph 2).
+ *
  * w12_encode on the GPU: writes the blob of *d (from w12_encode_plan_device
  * on the same w_dev, layout and workspace) into blob_dev (d->total_bytes,
  * 256-byte aligned), byte for byte what w12_encode writes.  Asynchronous on
@@ -211,6 +236,9 @@ int w12_encode_device(const uint16_t *w_dev, int64_t K, int64_t N, int layout, c
 /* --------------------------------------------------------------------- */
 
 /*
+ * Defined by: "项目介绍" paragraph 2 (W12 is decoded bit-exactly) and
+ * "Reasons" bullet 2 (the three planes are rebuilt bit by bit).
+ *
  * Decode a device blob (256-byte aligned) back to bf16 bit patterns in w_dev
  * (K*N uint16, 16-byte aligned) in the given layout.  Bit-exact inverse of
  * w12_encode.  Errors: W12_ERR_ARG, W12_ERR_ALIGN, W12_ERR_CUDA.  Escape
@@ -225,6 +253,11 @@ int w12_decode(const w12_desc *d, const void *blob_dev, uint16_t *w_dev, int lay
 size_t w12_gemm_workspace_size(const w12_desc *d, int64_t M);
 
 /*
+ * Defined by: "Reasons" bullet 2 (the planes are rebuilt bit by bit inside the
+ * GEMM's registers) and "项目介绍" paragraph 2 (a bit-exact decode inside the
+ * GEMM, batch 1-32); the first paragraph of the summary (a decode step reads
+ * every weight) makes it a weight stream.
+ *
  * y[m, n] = sum_k x[m, k] * W[k, n] for m < M, n < N.
  *   x_dev: [M][K] row-major bf16, 16-byte aligned.
  *   y_dev: [M][N] row-major, y_dtype W12_F32 (4-byte aligned) or W12_BF16
@@ -237,8 +270,9 @@ size_t w12_gemm_workspace_size(const w12_desc *d, int64_t M);
 int w12_gemm(const w12_desc *d, const void *blob_dev, const uint16_t *x_dev, int64_t M,
              void *y_dev, int y_dtype, void *ws_dev, size_t ws_bytes, void *stream);
 
-/* w12_gemm with an explicit path (W12_PATH_*); W12_ERR_SHAPE if the path
- * does not serve this M. */
+/* w12_gemm with an explicit path (W12_PATH_*, optionally OR-ed with
+ * W12_OPT_EARLY_WEIGHTS); W12_ERR_SHAPE if the path does not serve this M,
+ * W12_ERR_ARG for an unknown path or option bit. */
 int w12_gemm_ex(const w12_desc *d, const void *blob_dev, const uint16_t *x_dev, int64_t M,
                 void *y_dev, int y_dtype, void *ws_dev, size_t ws_bytes, int path,
                 void *stream);
@@ -251,6 +285,8 @@ int w12_gemm_ex(const w12_desc *d, const void *blob_dev, const uint16_t *x_dev, 
 size_t w12_gemm_batched_workspace_size(const w12_desc *descs, int count, int64_t M);
 
 /*
+ * Defined by: as w12_gemm ("Reasons" bullet 2; "项目介绍" paragraph 2).
+ *
  * count independent products y_i = x_i . W_i (1 <= count <= W12_MAX_BATCH,
  * every K_i, N_i > 0) with one M, e.g. the linears of a decoder layer, in ONE
  * kernel launch: the work units of all products (stream-K units of columns x
@@ -267,16 +303,51 @@ int w12_gemm_batched(const w12_desc *descs, const void *const *blobs_dev,
                      const uint16_t *const *x_dev, int64_t M, void *const *y_dev, int y_dtype,
                      int count, void *ws_dev, size_t ws_bytes, void *stream);
 
-/* w12_gemm_batched with an explicit path (W12_PATH_*); W12_ERR_SHAPE if the
- * path does not serve this M. */
+/* w12_gemm_batched with an explicit path (W12_PATH_*, optionally OR-ed with
+ * W12_OPT_EARLY_WEIGHTS); W12_ERR_SHAPE if the path does not serve this M,
+ * W12_ERR_ARG for an unknown path or option bit. */
 int w12_gemm_batched_ex(const w12_desc *descs, const void *const *blobs_dev,
                         const uint16_t *const *x_dev, int64_t M, void *const *y_dev, int y_dtype,
                         int count, void *ws_dev, size_t ws_bytes, int path, void *stream);
+
+/*
+ * Test hooks of w12_gemm_batched_debug (no counterpart on the pages: they
+ * exist to exercise the kernels' bounded waits on a GPU).
+ *   withhold_unit: -1, or a work unit (0 <= unit < the batch's unit count)
+ *     whose weight copy the producer never issues, so that the consumers'
+ *     wait on it runs out and the call records W12_ERR_TIMEOUT.
+ *   wait_limit_us: the limit of one bounded wait in microseconds (0: the
+ *     default of 2 s; at most 10 s).
+ */
+typedef struct w12_debug_opts {
+    int32_t withhold_unit;
+    uint32_t wait_limit_us;
+} w12_debug_opts;
+
+/*
+ * w12_gemm_batched_ex with test hooks.  With withhold_unit = -1 and
+ * wait_limit_us = 0 it is w12_gemm_batched_ex.  After a withheld unit the
+ * outputs are undefined and word 0 of the workspace reads W12_ERR_TIMEOUT;
+ * every kernel still runs to its end (no wait is unbounded), the
+ * workspace's counters are left at zero, and the next call on the same
+ * workspace is correct.  Errors: as w12_gemm_batched_ex; W12_ERR_ARG for a
+ * NULL dbg or a hook out of range.
+ */
+int w12_gemm_batched_debug(const w12_desc *descs, const void *const *blobs_dev,
+                           const uint16_t *const *x_dev, int64_t M, void *const *y_dev, int y_dtype,
+                           int count, void *ws_dev, size_t ws_bytes, int path,
+                           const w12_debug_opts *dbg, void *stream);
 
 /* Bytes of workspace w12_verify_greedy needs (>= 256). */
 size_t w12_verify_workspace_size(int64_t R, int64_t T, int64_t V);
 
 /*
+ * Defined by: "Risks" bullet 3 of the SpecPilot summary (lossless means every
+ * committed token is the target model's own greedy choice) and the
+ * hotrepo.ai page's "结果与验证" (each committed token is checked against the
+ * target's choice at its position).  Tie, NaN and -0 handling and the draft
+ * alignment are this library's reading (the pages are silent on them).
+ *
  * Greedy verification of R draft blocks of T positions on logits.
  *   logits_dev: [R*T][V] row-major, dtype W12_F32 or W12_BF16, 16-byte aligned.
  *   draft_dev:  [R][T-1] int32 (may be NULL when T == 1).
@@ -298,6 +369,9 @@ int w12_verify_greedy(const void *logits_dev, int dtype, int64_t R, int64_t T, i
 size_t w12_verify_lmhead_workspace_size(const w12_desc *d_lm, int64_t R, int64_t T);
 
 /*
+ * Defined by: as w12_gemm (the lm_head product) and w12_verify_greedy (the
+ * acceptance rule): "Reasons" bullet 2, "Risks" bullet 3, "结果与验证".
+ *
  * Fused lm_head + greedy verification: logits = hidden @ W_lm (the W12
  * decode-GEMM, fp32 accumulation), then the rule of w12_verify_greedy on
  * those fp32 logits, without writing them unless logits_out_dev is given.
@@ -351,7 +425,10 @@ int w12_verify_greedy_noalloc(const void *logits_dev, int dtype, int64_t R, int6
 /*
  * Read (and clear) the sticky device error word of a workspace: waits for
  * `stream`, copies word 0 to *err_host, then zeroes it.  Returns W12_OK or
- * W12_ERR_CUDA.  *err_host is W12_OK or W12_ERR_DEVICE.
+ * W12_ERR_CUDA.  *err_host is W12_OK or the first error recorded since the
+ * word was last cleared: W12_ERR_DEVICE (a kernel met an escape index
+ * outside the escape list) or W12_ERR_TIMEOUT (a bounded wait ran out; the
+ * call's outputs are undefined).
  */
 int w12_get_device_error(void *ws_dev, int *err_host, void *stream);
 

@@ -86,24 +86,6 @@ bool gemv_fits_32bit(const w12_desc *d) {
     return d->K < lim && d->N < lim && d->K / 8 * d->N < lim && d->G < lim;
 }
 
-int verify_plan(int64_t rows, int64_t V, int *grid, int64_t *splits, int64_t *chunk) {
-    Device dv;
-    if (query_device(&dv) != W12_OK) return W12_ERR_CUDA;
-    int64_t sp = std::max<int64_t>(1, ceil_div(4 * int64_t(dv.sms), rows));
-    sp = std::min<int64_t>(sp, std::max<int64_t>(1, ceil_div(V, 1024)));
-    int64_t ch = ceil_div(ceil_div(V, sp), 8) * 8;
-    sp = ceil_div(V, ch);
-    *splits = sp;
-    *chunk = ch;
-    *grid = int(std::min<int64_t>(rows * sp, int64_t(dv.sms) * 8));
-    return W12_OK;
-}
-
-size_t verify_ws(int64_t rows, int64_t splits) {
-    return kWsHeader + 256 + round256(uint64_t(rows * splits) * 8u) + round256(uint64_t(rows) * 4u);
-}
-
-
 // Workspace layout of a batch: header (error word), then per product its
 // stream-K counters, then the partial sums (two slots per CTA).  Every path
 // is the same weight stream (units of 128 columns x one 128-k group, one
@@ -115,7 +97,8 @@ struct BatchPlan {
     int64_t U = 0;
     size_t counters[kMaxBatch] = {}, partial[kMaxBatch] = {};
     int64_t steps[kMaxBatch] = {}, NB[kMaxBatch] = {}, ubase[kMaxBatch] = {};
-    size_t stream_partial = 0;  // MMA path: [grid][2][M][128] floats
+    size_t stream_partial = 0;  // [grid][slots][M][128] floats
+    int slots = 2;              // partial slots per CTA: 2, or 4 on the tcgen05 path (pair order)
     size_t total = 0;
 };
 
@@ -168,28 +151,45 @@ int plan_batch(const w12_desc *d, int count, int64_t M, int path, BatchPlan *bp)
         cpt = kMmaCols;
         uk = kGroup;
     }
+    // The tcgen05 path runs the tiles of a product in pairs (units (pair,
+    // group, tile of the pair)); an odd tile count is padded by a phantom
+    // tile, whose units copy and store nothing.
+    const bool pairs = path == W12_PATH_TC;
+    bp->slots = pairs ? 4 : 2;
     size_t off = kWsHeader;
     for (int i = 0; i < count; ++i) {
         bp->steps[i] = ceil_div(d[i].K, uk);
         bp->NB[i] = ceil_div(d[i].N, cpt);
         bp->ubase[i] = bp->U;
-        bp->U += bp->steps[i] * bp->NB[i];
+        bp->U += bp->steps[i] * (pairs ? (bp->NB[i] + 1) / 2 * 2 : bp->NB[i]);
         bp->counters[i] = off;
         off += round256(4u * uint64_t(std::max<int64_t>(bp->NB[i], 1)));
     }
     if (bp->U >= (int64_t(1) << 31)) return W12_ERR_SHAPE;
     bp->grid = int(std::min<int64_t>(int64_t(dv.sms) * occ, std::max<int64_t>(bp->U, 1)));
     bp->stream_partial = off;
-    off += round256(uint64_t(bp->grid) * 2u * uint64_t(M) * uint64_t(cpt) * 4u);
+    off += round256(uint64_t(bp->grid) * uint64_t(bp->slots) * uint64_t(M) * uint64_t(cpt) * 4u);
     bp->total = off;
     return W12_OK;
 }
 
 // The TMA-fed mma.sync path: one tensor map per plane and one for x per product.
+// Launch options of one call (defaults: weights read only after the
+// previous kernel of the stream, no test hook, the default wait limit).
+struct LaunchOpts {
+    bool early_weights = false;
+    int32_t withhold_unit = -1;
+    uint64_t wait_ns = 0;
+};
+
 int fill_stream_batch(const w12_desc *d, const void *const *blobs, const uint16_t *const *xs, int64_t M,
-                      void *const *ys, int y_dtype, int count, void *ws, const BatchPlan &bp, StreamBatch *out) {
+                      void *const *ys, int y_dtype, int count, void *ws, const BatchPlan &bp,
+                      const LaunchOpts &opt, StreamBatch *out) {
     uint8_t *w = static_cast<uint8_t *>(ws);
     StreamBatch &b = *out;
+    b.early_weights = opt.early_weights ? 1 : 0;
+    b.withhold_unit = opt.withhold_unit;
+    b.wait_ns = opt.wait_ns;
     b.count = count;
     b.M = int(M);
     b.y_dtype = y_dtype;
@@ -218,10 +218,11 @@ int fill_stream_batch(const w12_desc *d, const void *const *blobs, const uint16_
 }
 
 int run_stream_batch(const w12_desc *d, const void *const *blobs, const uint16_t *const *xs, int64_t M,
-                     void *const *ys, int y_dtype, int count, void *ws, const BatchPlan &bp, void *stream) {
+                     void *const *ys, int y_dtype, int count, void *ws, const BatchPlan &bp,
+                     const LaunchOpts &opt, void *stream) {
     StreamBatch b;
     std::memset(&b, 0, sizeof b);
-    const int st = fill_stream_batch(d, blobs, xs, M, ys, y_dtype, count, ws, bp, &b);
+    const int st = fill_stream_batch(d, blobs, xs, M, ys, y_dtype, count, ws, bp, opt, &b);
     if (st != W12_OK) return st;
     switch (bp.path) {
         case W12_PATH_TC: return launch_tc_batch(b, bp.variant, bp.grid, stream);
@@ -232,8 +233,18 @@ int run_stream_batch(const w12_desc *d, const void *const *blobs, const uint16_t
 
 // Launch a planned batch (all K_i, N_i > 0; pointers already checked).
 int run_batch(const w12_desc *d, const void *const *blobs, const uint16_t *const *xs, int64_t M,
-              void *const *ys, int y_dtype, int count, void *ws, const BatchPlan &bp, void *stream) {
-    return run_stream_batch(d, blobs, xs, M, ys, y_dtype, count, ws, bp, stream);
+              void *const *ys, int y_dtype, int count, void *ws, const BatchPlan &bp, const LaunchOpts &opt,
+              void *stream) {
+    return run_stream_batch(d, blobs, xs, M, ys, y_dtype, count, ws, bp, opt, stream);
+}
+
+// Split the path argument of the _ex calls into the path and its options.
+int split_path(int path_opts, int *path, LaunchOpts *opt) {
+    if (path_opts & ~(W12_OPT_EARLY_WEIGHTS | 0xFF)) return W12_ERR_ARG;
+    *path = path_opts & 0xFF;
+    if (*path < W12_PATH_AUTO || *path > W12_PATH_TC) return W12_ERR_ARG;
+    opt->early_weights = (path_opts & W12_OPT_EARLY_WEIGHTS) != 0;
+    return W12_OK;
 }
 
 // Fused lm_head + verify: the stream-K plan of the one product, then the
@@ -254,7 +265,7 @@ int plan_fused(const w12_desc *d, int64_t M, FusedPlan *fp) {
     if (cached_occupancy(dv, key, 0, &occ) != W12_OK || occ < 1) return W12_ERR_CUDA;
     bp.grid = int(std::min<int64_t>(int64_t(dv.sms) * occ, bp.U));
     size_t off = bp.stream_partial;
-    off += round256(uint64_t(bp.grid) * 2u * uint64_t(M) * uint64_t(kMmaCols) * 4u);
+    off += round256(uint64_t(bp.grid) * uint64_t(bp.slots) * uint64_t(M) * uint64_t(kMmaCols) * 4u);
     fp->off_best = off;
     off += round256(uint64_t(bp.grid) * uint64_t(M) * 8u);
     fp->off_done = off;
@@ -266,6 +277,33 @@ int plan_fused(const w12_desc *d, int64_t M, FusedPlan *fp) {
 }
 
 }  // namespace
+
+// Work split of the greedy verify kernel for `rows` rows of V logits: about
+// four (row, slice) work items per SM, slices of `chunk` logits (a multiple
+// of 8).  Shared by w12_verify_greedy and w12_verify_greedy_noalloc.
+int verify_plan(int64_t rows, int64_t V, int *grid, int64_t *splits, int64_t *chunk) {
+    Device dv;
+    if (query_device(&dv) != W12_OK) return W12_ERR_CUDA;
+    int64_t sp = std::max<int64_t>(1, ceil_div(4 * int64_t(dv.sms), rows));
+    sp = std::min<int64_t>(sp, std::max<int64_t>(1, ceil_div(V, 1024)));
+    int64_t ch = ceil_div(ceil_div(V, sp), 8) * 8;
+    sp = ceil_div(V, ch);
+    *splits = sp;
+    *chunk = ch;
+    *grid = int(std::min<int64_t>(rows * sp, int64_t(dv.sms) * 8));
+    return W12_OK;
+}
+
+size_t verify_ws(int64_t rows, int64_t splits) {
+    return kWsHeader + 256 + round256(uint64_t(rows * splits) * 8u) + round256(uint64_t(rows) * 4u);
+}
+
+void verify_layout(void *ws, int64_t rows, int64_t splits, VerifyArgs *a) {
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    a->counter = reinterpret_cast<uint32_t *>(w + kWsHeader);
+    a->partial = reinterpret_cast<unsigned long long *>(w + kWsHeader + 256);
+    a->gbuf = reinterpret_cast<int32_t *>(w + kWsHeader + 256 + round256(uint64_t(rows * splits) * 8u));
+}
 
 }  // namespace w12
 
@@ -307,13 +345,15 @@ extern "C" size_t w12_gemm_workspace_size(const w12_desc *d, int64_t M) {
 }
 
 extern "C" int w12_gemm_ex(const w12_desc *d, const void *blob, const uint16_t *x, int64_t M,
-                           void *y, int y_dtype, void *ws, size_t ws_bytes, int path,
+                           void *y, int y_dtype, void *ws, size_t ws_bytes, int path_opts,
                            void *stream) {
     int st = check_desc(d);
     if (st != W12_OK) return st;
     if (M < 1 || M > W12_MAX_M) return W12_ERR_SHAPE;
     if (y_dtype != W12_F32 && y_dtype != W12_BF16) return W12_ERR_ARG;
-    if (path < W12_PATH_AUTO || path > W12_PATH_TC) return W12_ERR_ARG;
+    int path;
+    LaunchOpts opt;
+    if (split_path(path_opts, &path, &opt) != W12_OK) return W12_ERR_ARG;
     if (d->N == 0) return W12_OK;
     if (!y) return W12_ERR_ARG;
     if (!aligned(y, y_dtype == W12_F32 ? 4 : 2)) return W12_ERR_ALIGN;
@@ -332,7 +372,7 @@ extern "C" int w12_gemm_ex(const w12_desc *d, const void *blob, const uint16_t *
     const void *blobs[1] = {blob};
     const uint16_t *xs[1] = {x};
     void *ys[1] = {y};
-    return run_batch(d, blobs, xs, M, ys, y_dtype, 1, ws, bp, stream);
+    return run_batch(d, blobs, xs, M, ys, y_dtype, 1, ws, bp, opt, stream);
 }
 
 extern "C" int w12_gemm(const w12_desc *d, const void *blob, const uint16_t *x, int64_t M, void *y,
@@ -352,12 +392,13 @@ extern "C" size_t w12_gemm_batched_workspace_size(const w12_desc *d, int count, 
     return need;
 }
 
-extern "C" int w12_gemm_batched_ex(const w12_desc *d, const void *const *blobs, const uint16_t *const *xs,
-                                   int64_t M, void *const *ys, int y_dtype, int count, void *ws,
-                                   size_t ws_bytes, int path, void *stream) {
+namespace {
+
+int gemm_batched_opts(const w12_desc *d, const void *const *blobs, const uint16_t *const *xs, int64_t M,
+                      void *const *ys, int y_dtype, int count, void *ws, size_t ws_bytes, int path,
+                      const LaunchOpts &opt, void *stream) {
     if (!blobs || !xs || !ys) return W12_ERR_ARG;
     if (y_dtype != W12_F32 && y_dtype != W12_BF16) return W12_ERR_ARG;
-    if (path < W12_PATH_AUTO || path > W12_PATH_TC) return W12_ERR_ARG;
     BatchPlan bp;
     int st = plan_batch(d, count, M, path, &bp);
     if (st != W12_OK) return st;
@@ -369,7 +410,31 @@ extern "C" int w12_gemm_batched_ex(const w12_desc *d, const void *const *blobs, 
     }
     if (!ws || ws_bytes < bp.total) return W12_ERR_WORKSPACE;
     if (!aligned(ws, 256)) return W12_ERR_ALIGN;
-    return run_batch(d, blobs, xs, M, ys, y_dtype, count, ws, bp, stream);
+    if (opt.withhold_unit >= bp.U) return W12_ERR_ARG;
+    return run_batch(d, blobs, xs, M, ys, y_dtype, count, ws, bp, opt, stream);
+}
+
+}  // namespace
+
+extern "C" int w12_gemm_batched_ex(const w12_desc *d, const void *const *blobs, const uint16_t *const *xs,
+                                   int64_t M, void *const *ys, int y_dtype, int count, void *ws,
+                                   size_t ws_bytes, int path_opts, void *stream) {
+    int path;
+    LaunchOpts opt;
+    if (split_path(path_opts, &path, &opt) != W12_OK) return W12_ERR_ARG;
+    return gemm_batched_opts(d, blobs, xs, M, ys, y_dtype, count, ws, ws_bytes, path, opt, stream);
+}
+
+extern "C" int w12_gemm_batched_debug(const w12_desc *d, const void *const *blobs, const uint16_t *const *xs,
+                                      int64_t M, void *const *ys, int y_dtype, int count, void *ws,
+                                      size_t ws_bytes, int path_opts, const w12_debug_opts *dbg, void *stream) {
+    int path;
+    LaunchOpts opt;
+    if (!dbg || split_path(path_opts, &path, &opt) != W12_OK) return W12_ERR_ARG;
+    if (dbg->withhold_unit < -1 || dbg->wait_limit_us > 10000000u) return W12_ERR_ARG;
+    opt.withhold_unit = dbg->withhold_unit;
+    opt.wait_ns = uint64_t(dbg->wait_limit_us) * 1000u;
+    return gemm_batched_opts(d, blobs, xs, M, ys, y_dtype, count, ws, ws_bytes, path, opt, stream);
 }
 
 extern "C" int w12_gemm_batched(const w12_desc *d, const void *const *blobs, const uint16_t *const *xs,
@@ -401,7 +466,6 @@ extern "C" int w12_verify_greedy(const void *logits, int dtype, int64_t R, int64
     if (verify_plan(a.rows, V, &grid, &a.splits, &a.chunk) != W12_OK) return W12_ERR_CUDA;
     if (!ws || ws_bytes < verify_ws(a.rows, a.splits)) return W12_ERR_WORKSPACE;
     if (!aligned(ws, 256)) return W12_ERR_ALIGN;
-    uint8_t *w = static_cast<uint8_t *>(ws);
     a.logits = logits;
     a.dtype = dtype;
     a.R = R;
@@ -410,9 +474,7 @@ extern "C" int w12_verify_greedy(const void *logits, int dtype, int64_t R, int64
     a.draft = draft;
     a.accept_len = accept_len;
     a.next_tok = next_tok;
-    a.counter = reinterpret_cast<uint32_t *>(w + kWsHeader);
-    a.partial = reinterpret_cast<unsigned long long *>(w + kWsHeader + 256);
-    a.gbuf = reinterpret_cast<int32_t *>(w + kWsHeader + 256 + round256(uint64_t(a.rows * a.splits) * 8u));
+    verify_layout(ws, a.rows, a.splits, &a);
     return launch_verify(a, grid, stream);
 }
 
@@ -449,7 +511,7 @@ extern "C" int w12_verify_greedy_lmhead(const uint16_t *hidden, const w12_desc *
     const void *blobs[1] = {blob};
     const uint16_t *xs[1] = {hidden};
     void *ys[1] = {logits_out};
-    st = fill_stream_batch(d, blobs, xs, M, ys, W12_F32, 1, ws, fp.bp, &b);
+    st = fill_stream_batch(d, blobs, xs, M, ys, W12_F32, 1, ws, fp.bp, LaunchOpts{}, &b);
     if (st != W12_OK) return st;
     b.row_best = reinterpret_cast<unsigned long long *>(w + fp.off_best);
     b.done = reinterpret_cast<uint32_t *>(w + fp.off_done);

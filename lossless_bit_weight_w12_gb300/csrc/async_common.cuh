@@ -2,9 +2,10 @@
 // barriers, inline PTX.
 //
 // Every wait is bounded: it polls with try_wait, backs off, and gives up after
-// kWaitLimitNs of wall time (or as soon as another thread of the CTA has
-// given up), recording W12_ERR_TIMEOUT in the caller's error word.  No kernel
-// of this library can spin forever.
+// the CTA's wait limit (kWaitLimitNs unless a launch asks for a shorter one)
+// of wall time, or as soon as another thread of the CTA has given up,
+// recording W12_ERR_TIMEOUT in the caller's error word.  No kernel of this
+// library can spin forever.
 #pragma once
 
 #include <cstdint>
@@ -14,6 +15,14 @@
 namespace w12 {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+// Shared per-CTA wait state: the abort flag every bounded wait polls, and the
+// wall-time limit of one wait.
+struct WaitCtl {
+    int abort;
+    int pad;
+    uint64_t limit_ns;
+};
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -57,23 +66,40 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete.  Returns false (and
-// sets *abort and *err) on timeout, or false at once if *abort is already set.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                          int *err) {
+// sets ctl->abort and *err) on timeout, or false at once if the CTA has
+// already aborted.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, WaitCtl *ctl, int *err) {
     if (mbar_try_wait(bar, parity)) return true;
+    volatile int *abort = &ctl->abort;
+    const uint64_t limit = ctl->limit_ns;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t i = 0;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
         if ((i & 255u) == 255u) {
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
+            if (global_timer_ns() - t0 > limit) {
                 *abort = 1;
-                if (err) *err = W12_ERR_TIMEOUT;
+                if (err) atomicCAS(err, 0, W12_ERR_TIMEOUT);  // the first error of a call wins
                 return false;
             }
         }
         __nanosleep(32);
     }
+}
+
+// Bounded wait that ignores the abort flag (used only to let copies or
+// tensor-core operations that are already in flight finish before the CTA
+// exits after a timeout).
+__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > limit_ns) return;
+        __nanosleep(64);
+    }
+}
+
+__device__ __forceinline__ bool aborted(const WaitCtl *ctl) {
+    return *reinterpret_cast<const volatile int *>(&ctl->abort) != 0;
 }
 
 // L2 policy for data read exactly once (the weight planes).

@@ -27,6 +27,14 @@ namespace w12 {
 
 constexpr uint32_t kSignManMask = 0x807F807Fu;
 
+// Record a device error in a workspace's error word: the first error of a
+// call wins (a CTA that gave up on a bounded wait may read a stage that
+// never filled and meet garbage escape indices afterwards; the timeout is
+// what the caller must see).
+__device__ __forceinline__ void record_error(int *err, int code) {
+    if (err) atomicCAS(err, 0, code);
+}
+
 // Streaming 16-byte load: read once, keep out of L1, ask L2 for 256-byte lines.
 __device__ __forceinline__ uint4 ldg_stream(const void *p) {
     uint4 r;
@@ -104,7 +112,7 @@ __device__ __forceinline__ void patch_escapes(uint32_t out[16], uint32_t m0, uin
                                                   uint64_t n_esc, int *err) {
     const uint32_t lo = m0 >> 8, hi = m1 >> 8;
     if (hi < lo || uint64_t(hi) > n_esc || hi - lo > 128u) {
-        if (err) *err = W12_ERR_DEVICE;
+        record_error(err, W12_ERR_DEVICE);
         return;
     }
     for (uint32_t i = lo; i < hi; ++i) {

@@ -128,7 +128,8 @@ __global__ void __launch_bounds__(kST, MINB) stream_kernel(const __grid_constant
     constexpr int S = SRing<NT, MINB>::S;
     extern __shared__ unsigned char smem_dyn[];
     __shared__ __align__(8) uint64_t full[S], empty[S];
-    __shared__ int s_abort, s_last;
+    __shared__ WaitCtl s_ctl;
+    __shared__ int s_last;
     __shared__ unsigned long long s_best[FUSED ? kMaxM : 1];
     const uint32_t base = (smem_addr(smem_dyn) + 1023u) & ~1023u;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -144,7 +145,7 @@ __global__ void __launch_bounds__(kST, MINB) stream_kernel(const __grid_constant
             mbar_init(&full[s], 1);  // the producer's expect_tx arrival (+ bytes)
             mbar_init(&empty[s], kCW);
         }
-        s_abort = 0;
+        wait_ctl_init(&s_ctl, b);
         mbar_fence_init();
     }
     if (FUSED)
@@ -155,7 +156,7 @@ __global__ void __launch_bounds__(kST, MINB) stream_kernel(const __grid_constant
 
     if (warp == kCW) {
         if (u0 >= u1) return;
-        stream_producer<S, false>(b, base, C::kStage, C::kX, C::MP, full, empty, &s_abort, u0, u1, lane);
+        stream_producer<S, false>(b, base, C::kStage, C::kX, C::MP, full, empty, &s_ctl, u0, u1, lane);
         return;
     }
     pdl_wait();  // nothing below touches global memory the previous kernel may write before this
@@ -194,7 +195,7 @@ __global__ void __launch_bounds__(kST, MINB) stream_kernel(const __grid_constant
             for (int q = 0; q < 2; ++q) fa[m][q][0] = fa[m][q][1] = fb[m][q][0] = fb[m][q][1] = 0.f;
 
         for (; u < ub; ++u) {
-            mbar_wait(&full[s], ph, &s_abort, b.err);
+            mbar_wait(&full[s], ph, &s_ctl, b.err);
             const uint32_t st = base + uint32_t(s) * C::kStage;
             const uint4 ha = lds128(st + C::kH + pa), la = lds128(st + C::kL + pa), ea = lds128(st + C::kE + pa);
             const uint4 hb = lds128(st + C::kH + pb), lb = lds128(st + C::kL + pb), eb = lds128(st + C::kE + pb);

@@ -12,7 +12,6 @@
 // on every GPU that loads the library until the process exits.
 #include <cuda_runtime.h>
 
-#include <algorithm>
 #include <mutex>
 
 #include "w12_internal.h"
@@ -48,8 +47,6 @@ int scratch_address(void **out) {
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
-int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
-
 }  // namespace
 
 }  // namespace w12
@@ -66,23 +63,12 @@ extern "C" int w12_verify_greedy_noalloc(const void *logits, int dtype, int64_t 
         !aligned(next_tok, 4) || (draft && !aligned(draft, 4)))
         return W12_ERR_ALIGN;
 
-    // Same work split as w12_verify_greedy: about four work items per SM.
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return W12_ERR_CUDA;
+    // The same work split and scratch layout as w12_verify_greedy.
+    VerifyArgs a;
+    int grid;
     const int64_t rows = R * T;
-    int64_t splits = std::max<int64_t>(1, ceil_div(4 * int64_t(sms), rows));
-    splits = std::min<int64_t>(splits, std::max<int64_t>(1, ceil_div(V, 1024)));
-    const int64_t chunk = ceil_div(ceil_div(V, splits), 8) * 8;
-    splits = ceil_div(V, chunk);
-    const int grid = int(std::min<int64_t>(rows * splits, int64_t(sms) * 8));
-
-    // Scratch layout: [0, 256) error word, [256, 512) arrival counter, then
-    // the partial keys (rows * splits * 8 bytes), then the tokens (rows * 4).
-    const uint64_t keys = round256(uint64_t(rows * splits) * 8u);
-    const uint64_t need = kWsHeader + 256 + keys + round256(uint64_t(rows) * 4u);
-    if (need > W12_NOALLOC_SCRATCH_BYTES) return W12_ERR_WORKSPACE;
+    if (verify_plan(rows, V, &grid, &a.splits, &a.chunk) != W12_OK) return W12_ERR_CUDA;
+    if (verify_ws(rows, a.splits) > W12_NOALLOC_SCRATCH_BYTES) return W12_ERR_WORKSPACE;
 
     void *scratch = nullptr;
     int st = scratch_address(&scratch);
@@ -93,7 +79,6 @@ extern "C" int w12_verify_greedy_noalloc(const void *logits, int dtype, int64_t 
     // arrival counter must start at zero.
     if (cudaMemsetAsync(ws, 0, kWsHeader + 256, s) != cudaSuccess) return W12_ERR_CUDA;
 
-    VerifyArgs a;
     a.logits = logits;
     a.dtype = dtype;
     a.R = R;
@@ -103,10 +88,6 @@ extern "C" int w12_verify_greedy_noalloc(const void *logits, int dtype, int64_t 
     a.draft = draft;
     a.accept_len = accept_len;
     a.next_tok = next_tok;
-    a.counter = reinterpret_cast<uint32_t *>(ws + kWsHeader);
-    a.partial = reinterpret_cast<unsigned long long *>(ws + kWsHeader + 256);
-    a.gbuf = reinterpret_cast<int32_t *>(ws + kWsHeader + 256 + keys);
-    a.splits = splits;
-    a.chunk = chunk;
+    verify_layout(ws, rows, a.splits, &a);
     return launch_verify(a, grid, stream);
 }

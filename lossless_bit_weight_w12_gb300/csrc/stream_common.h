@@ -47,6 +47,15 @@ struct StreamBatch {
     const int32_t *draft;          // [vR][vT - 1]
     int32_t *accept_len, *next_tok, *gbuf;
     int vR, vT;
+    // Launch options.  early_weights: the producers request the first ring's
+    // worth of weight unit blocks before griddepcontrol.wait (the blob must
+    // not be written by the kernel launched just before; W12_OPT_EARLY_WEIGHTS).
+    // wait_ns: the limit of one bounded wait (0: kWaitLimitNs).  withhold_unit:
+    // a test hook (w12_gemm_batched_debug), -1 normally; the unit whose weight
+    // copy the producer never issues, so that a wait on it runs out.
+    int early_weights;
+    int32_t withhold_unit;
+    uint64_t wait_ns;
 };
 
 // Kernel variants: v = 2 * log2(NT) + (ctas_per_sm - 1), NT = ceil(M / 8)

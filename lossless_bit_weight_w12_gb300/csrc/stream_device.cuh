@@ -52,16 +52,6 @@ __device__ __forceinline__ void prefetch_l1(const void *p) {
     asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
 }
 
-// Bounded wait that ignores the abort flag (used only to let copies that
-// are already in flight land before the CTA exits after a timeout).
-__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity) {
-    const uint64_t t0 = global_timer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (global_timer_ns() - t0 > kWaitLimitNs) return;
-        __nanosleep(64);
-    }
-}
-
 // Unit cursor: product gi, column tile nb, group kg.
 struct SCur {
     int gi, nb, kg;
@@ -193,27 +183,33 @@ __device__ __forceinline__ void pdl_launch() { asm volatile("griddepcontrol.laun
 //  - x at the stage start: one 3-D box (every token, both 64-k halves,
 //    mma.sync layout), or (TC) two 2-D boxes of 64 k x MP tokens, the
 //    second at MP * 128 bytes (the canonical K-major tcgen05 operand).
-// The weights are read-only, so the first ring's worth of unit blocks is
-// requested before pdl_wait (overlapping the previous kernel's tail); x,
-// which the previous kernel may have written, only after it.
+// Nothing is read before griddepcontrol.wait (the previous kernel of the
+// stream may have written the blob or x), unless the launch asked for the
+// early weight stream (b.early_weights): then the first ring's worth of
+// unit blocks is requested before it, overlapping the previous kernel's
+// tail, and x only after it.
 // At the start of every tile piece it prefetches the piece's escape entries
 // (a contiguous range of the escape list: escapes are listed by unit, and a
 // piece is consecutive units) into L1.
+// The test hook b.withhold_unit leaves one unit's stage unarmed: its
+// consumers' bounded wait runs out (W12_ERR_TIMEOUT).
 template <int S, bool TC>
 __device__ __forceinline__ void stream_producer(const StreamBatch &b, uint32_t base, int stage_bytes,
                                                 int x_bytes, int mp, uint64_t *full, uint64_t *empty,
-                                                int *abort, int u0, int u1, int lane) {
+                                                WaitCtl *ctl, int u0, int u1, int lane) {
     if (lane != 0) return;
     const uint64_t pol = l2_evict_first_policy();
     const uint32_t tx = uint32_t(x_bytes + kUnitBytes);
     auto issue_weights = [&](const SCur &c, int u, uint32_t st, uint64_t *bar) {
+        if (u == b.withhold_unit) return;
         const StreamOne &g = b.g[c.gi];
         const uint8_t *unit = unit_block(g, c);
         if (u == u0 || c.kg == 0) prefetch_piece_escapes(g, c, unit, u, u1);
         mbar_expect_tx(bar, tx);
         bulk_copy(st + uint32_t(x_bytes), unit, kUnitBytes, bar, pol);
     };
-    auto issue_x = [&](const SCur &c, uint32_t st, uint64_t *bar) {
+    auto issue_x = [&](const SCur &c, int u, uint32_t st, uint64_t *bar) {
+        if (u == b.withhold_unit) return;
         const StreamOne &g = b.g[c.gi];
         if (TC) {
             tma_2d_keep(st, &g.tx, 128 * c.kg, 0, bar);
@@ -222,24 +218,30 @@ __device__ __forceinline__ void stream_producer(const StreamBatch &b, uint32_t b
             tma_3d(st, &g.tx, 0, 2 * c.kg, 0, bar);
         }
     };
-    // the first ring's worth of weights, then the dependency, then their x
+    // the first ring's worth of weights (before or after the dependency),
+    // then their x
     SCur c = s_at(b, u0);
     const int P = min(S, u1 - u0);
     SCur first_c[S];
+    if (!b.early_weights) pdl_wait();
     for (int k = 0; k < P; ++k) {
         first_c[k] = c;
         issue_weights(c, u0 + k, base + uint32_t(k) * uint32_t(stage_bytes), &full[k]);
         s_next(b, c);
     }
-    pdl_wait();
-    for (int k = 0; k < P; ++k) issue_x(first_c[k], base + uint32_t(k) * uint32_t(stage_bytes), &full[k]);
+    if (b.early_weights) pdl_wait();
+    for (int k = 0; k < P; ++k)
+        issue_x(first_c[k], u0 + k, base + uint32_t(k) * uint32_t(stage_bytes), &full[k]);
     int s = P == S ? 0 : P, issued = P;
     uint32_t ph = P == S ? 1u : 0u;
     for (int u = u0 + P; u < u1; ++u) {
-        if (!mbar_wait(&empty[s], ph ^ 1u, abort, b.err)) break;
+        // a consumer that gave up arrives without waiting for its copy, and
+        // sets the abort flag before that arrival: stop here, so that every
+        // copy in flight is among the last ring's worth drained below
+        if (!mbar_wait(&empty[s], ph ^ 1u, ctl, b.err) || aborted(ctl)) break;
         const uint32_t st = base + uint32_t(s) * uint32_t(stage_bytes);
         issue_weights(c, u, st, &full[s]);
-        issue_x(c, st, &full[s]);
+        issue_x(c, u, st, &full[s]);
         s_next(b, c);
         ++issued;
         if (++s == S) {
@@ -247,16 +249,22 @@ __device__ __forceinline__ void stream_producer(const StreamBatch &b, uint32_t b
             ph ^= 1u;
         }
     }
-    if (*reinterpret_cast<volatile int *>(abort)) {
+    if (aborted(ctl)) {
         // let the copies already issued land before the CTA exits
         for (int k = 0; k < S && k < issued; ++k) {
             if (--s < 0) {
                 s = S - 1;
                 ph ^= 1u;
             }
-            mbar_drain(&full[s], ph);
+            mbar_drain(&full[s], ph, ctl->limit_ns);
         }
     }
+}
+
+// Set up the CTA's wait state (one thread, before the CTA's first barrier).
+__device__ __forceinline__ void wait_ctl_init(WaitCtl *ctl, const StreamBatch &b) {
+    ctl->abort = 0;
+    ctl->limit_ns = b.wait_ns ? b.wait_ns : kWaitLimitNs;
 }
 
 }  // namespace w12

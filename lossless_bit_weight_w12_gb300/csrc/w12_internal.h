@@ -63,4 +63,13 @@ struct VerifyArgs {
 };
 int launch_verify(const VerifyArgs &a, int grid, void *stream);
 
+// The greedy verify kernel's work split for `rows` rows of V logits (grid,
+// slices per row, logits per slice; W12_ERR_CUDA if the device query
+// fails), the scratch bytes it needs, and the scratch layout (counter,
+// per-slice keys, per-row tokens) inside a buffer of that size.  Shared by
+// w12_verify_greedy and w12_verify_greedy_noalloc.
+int verify_plan(int64_t rows, int64_t V, int *grid, int64_t *splits, int64_t *chunk);
+size_t verify_ws(int64_t rows, int64_t splits);
+void verify_layout(void *ws, int64_t rows, int64_t splits, VerifyArgs *a);
+
 }  // namespace w12

@@ -23,6 +23,7 @@ ERR_TOO_MANY_ESCAPES, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE = 6, 7, 8, 9
 LAYOUT_KN, LAYOUT_NK = 0, 1
 F32, BF16 = 0, 1
 PATH_AUTO, PATH_GEMV, PATH_MMA, PATH_TC = 0, 1, 2, 3
+OPT_EARLY_WEIGHTS = 0x100  # OR into a path: weight copies start under the previous kernel's tail
 MAX_M = 128
 
 # every symbol include/w12.h declares
@@ -33,6 +34,7 @@ EXPORTS = (
     "w12_verify_greedy_lmhead", "w12_get_device_error", "w12_verify_greedy_noalloc",
     "w12_gemm_batched_workspace_size", "w12_gemm_batched", "w12_gemm_batched_ex",
     "w12_encode_device_workspace_size", "w12_encode_plan_device", "w12_encode_device",
+    "w12_gemm_batched_debug",
 )
 
 
@@ -49,6 +51,10 @@ class _CDesc(ctypes.Structure):
                 ("n_units", ctypes.c_uint64), ("off_units", ctypes.c_uint64),
                 ("off_esc", ctypes.c_uint64), ("n_esc", ctypes.c_uint64),
                 ("total_bytes", ctypes.c_uint64)]
+
+
+class _CDebug(ctypes.Structure):
+    _fields_ = [("withhold_unit", ctypes.c_int32), ("wait_limit_us", ctypes.c_uint32)]
 
 
 @dataclass(frozen=True)
@@ -115,6 +121,7 @@ def lib():
         L.w12_encode_device_workspace_size.argtypes = [I64, I64]
         L.w12_encode_plan_device.argtypes = [P, I64, I64, I, D, P, SZ, P]
         L.w12_encode_device.argtypes = [P, I64, I64, I, D, P, P, SZ, P]
+        L.w12_gemm_batched_debug.argtypes = [D, P, P, I64, P, I, I, P, SZ, I, ctypes.POINTER(_CDebug), P]
         _lib = L
     return _lib
 
@@ -271,6 +278,18 @@ class GemmBatch:
 def gemm_batched(descs, blobs, xs, ys, ws, path: int = PATH_AUTO, stream=None):
     """ys[i] = xs[i] @ W_i for every i, in one launch."""
     GemmBatch(descs, blobs, xs, ys, ws, path)(stream)
+
+
+def gemm_batched_debug(descs, blobs, xs, ys, ws, withhold_unit: int = -1, wait_limit_us: int = 0,
+                       path: int = PATH_AUTO, stream=None):
+    """w12_gemm_batched_debug: the batched GEMM with the test hooks (a
+    withheld weight copy, a short wait limit)."""
+    b = GemmBatch(descs, blobs, xs, ys, ws, path)
+    dbg = _CDebug(withhold_unit, wait_limit_us)
+    _check(lib().w12_gemm_batched_debug(b.descs, b.blobs, b.xs, b.M, b.ys, b.y_dtype, b.count, _dptr(ws),
+                                        ws.numel() * ws.element_size(), path, ctypes.byref(dbg),
+                                        _stream(stream)),
+           "w12_gemm_batched_debug")
 
 
 def verify_workspace_size(R: int, T: int, V: int) -> int:

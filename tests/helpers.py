@@ -38,3 +38,27 @@ def check_gemm(y, y_ref, s_ref, bf16=False, what=""):
         raise AssertionError(
             f"{what}: {int(bad.sum())} outputs outside tolerance; first {tuple(i)}: "
             f"y={y[tuple(i)]!r} ref={y_ref[tuple(i)]!r} tol={tol[tuple(i)]!r}")
+
+
+def ref_gemm_f64(w, xs, chunk=4096):
+    """The GEMM's definition on the uncompressed weights: y = x . W summed in
+    float64 (a product of two bf16 values is exact in float64), and the
+    tolerance scale S = |x| . |W|.  w: bf16 bits [N, K]; xs: a list of bf16
+    bits [M_i, K].  Returns [(y_ref, s_ref)] per x, [M_i, N] each.  Column
+    chunks bound the float64 copy of W.  This is the definition the oracle's
+    GEMM is pinned to (tests/test_oracle_gemm_verify.py), applied to every
+    output of a full-size matrix where the oracle itself would take minutes."""
+    N, K = w.shape
+    xa = np.concatenate([bf16_bits_to_f64(x) for x in xs], axis=0)
+    ya = np.empty((xa.shape[0], N), dtype=np.float64)
+    sa = np.empty((xa.shape[0], N), dtype=np.float64)
+    xabs = np.abs(xa)
+    for c0 in range(0, N, chunk):
+        wf = bf16_bits_to_f64(w[c0:c0 + chunk])
+        ya[:, c0:c0 + chunk] = xa @ wf.T
+        sa[:, c0:c0 + chunk] = xabs @ np.abs(wf).T
+    out, r = [], 0
+    for x in xs:
+        out.append((ya[r:r + x.shape[0]], sa[r:r + x.shape[0]]))
+        r += x.shape[0]
+    return out

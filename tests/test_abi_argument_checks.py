@@ -54,6 +54,8 @@ def test_gemm_checks(w12, desc):
     assert gemm(dt=7) == w12.ERR_ARG
     assert gemm(path=9) == w12.ERR_ARG
     assert gemm(path=-1) == w12.ERR_ARG
+    assert gemm(path=0x200) == w12.ERR_ARG  # an unknown option bit
+    assert gemm(path=w12.OPT_EARLY_WEIGHTS | 9) == w12.ERR_ARG
     assert gemm(y=None) == w12.ERR_ARG
     assert gemm(y=DEV + 2, dt=F32) == w12.ERR_ALIGN  # fp32 y: 4-byte aligned
     assert gemm(y=DEV + 1, dt=BF16) == w12.ERR_ALIGN  # bf16 y: 2-byte aligned
@@ -82,6 +84,23 @@ def test_batched_gemm_checks(w12, desc):
     assert L.w12_gemm_batched_ex(arr, None, ptrs, 4, ptrs, w12.F32, 1, DEV, 1 << 20, 0, None) == w12.ERR_ARG
     assert L.w12_gemm_batched_ex(arr, ptrs, ptrs, 4, ptrs, 5, 1, DEV, 1 << 20, 0, None) == w12.ERR_ARG
     assert L.w12_gemm_batched_ex(arr, ptrs, ptrs, 4, ptrs, w12.F32, 1, DEV, 1 << 20, 7, None) == w12.ERR_ARG
+    assert L.w12_gemm_batched_ex(arr, ptrs, ptrs, 4, ptrs, w12.F32, 1, DEV, 1 << 20, 0x400, None) == w12.ERR_ARG
+
+
+def test_batched_debug_checks(w12, desc):
+    """The test-hook entry point rejects a missing or out-of-range hook
+    before it looks at anything else."""
+    L = w12.lib()
+    arr = (type(desc.c()) * 1)(desc.c())
+    ptrs = (ctypes.c_void_p * 1)(DEV)
+
+    def dbg_call(dbg, path=0):
+        return L.w12_gemm_batched_debug(arr, ptrs, ptrs, 4, ptrs, w12.F32, 1, DEV, 1 << 20, path,
+                                        dbg, None)
+    assert dbg_call(None) == w12.ERR_ARG
+    assert dbg_call(ctypes.byref(w12._CDebug(-2, 0))) == w12.ERR_ARG
+    assert dbg_call(ctypes.byref(w12._CDebug(-1, 20_000_000))) == w12.ERR_ARG
+    assert dbg_call(ctypes.byref(w12._CDebug(-1, 0)), path=9) == w12.ERR_ARG
 
 
 def test_decode_checks(w12, desc):

@@ -7,7 +7,9 @@ Config 4: the full stack -- 64 layers of the 27B-class linears plus the
 lm_head 5120 -> 151936 at M = 16 (one draft block of T = 16), seed 4.
  - every layer's six matrices: GPU decode bit-exact against the generated
    weights, and the batched W12 GEMM at M = 16 within the tolerance on
-   sampled columns (the oracle encodes and multiplies those columns);
+   sampled columns (the oracle encodes and multiplies those columns); at
+   layers 0, 31 and 63 every output of all six matrices against the float64
+   definition y = x W (numpy on the uncompressed weights);
  - the lm_head: fused greedy verify.  The fp64 reference logits are the
    definition y = h W computed with numpy's float64 matmul on the generated
    (uncompressed) weights; the drafts follow their argmax for a geometric
@@ -21,7 +23,7 @@ hidden -> 386; drafts -> 387.
 import numpy as np
 import pytest
 
-from helpers import check_gemm, dev_bits_to_np, to_dev_bits
+from helpers import check_gemm, dev_bits_to_np, ref_gemm_f64, to_dev_bits
 from lossless_bit_weight_w12_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -86,6 +88,9 @@ def test_config4_full_stack(dev, w12mod, oracle):
                 ns = np.unique(np.r_[pick.integers(0, N, 6), [N - 1]])
                 y_ref, s_ref = oracle.gemm(*oracle.encode(ws_np[i][ns], oracle.LAYOUT_NK), xs[i])
                 check_gemm(y[:, ns], y_ref, s_ref, what=f"config 4 layer {layer} {name}")
+            if layer in (0, L // 2 - 1, L - 1):  # every output against the float64 definition
+                (y_ref, s_ref), = ref_gemm_f64(ws_np[i], [xs[i]])
+                check_gemm(y, y_ref, s_ref, what=f"config 4 layer {layer} {name} (every output)")
         del blobs, ys, ws_np
 
     # lm_head + fused greedy verify

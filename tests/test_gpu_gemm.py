@@ -9,7 +9,7 @@ bit-exactly inside the GEMM).
 import numpy as np
 import pytest
 
-from helpers import bf16_bits_to_f64, check_gemm, dev_bits_to_np, to_dev_bits
+from helpers import bf16_bits_to_f64, check_gemm, dev_bits_to_np, ref_gemm_f64, to_dev_bits
 from lossless_bit_weight_w12_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -135,25 +135,39 @@ def test_gemm_deterministic(dev, w12mod, path, M):
     assert torch.equal(ys[0], ys[1]) and torch.equal(ys[1], ys[2])
 
 
-@pytest.mark.parametrize("M", [1, 16, 32, 64, 128])
-def test_gemm_full_layer_sampled(dev, w12mod, oracle, M):
-    """Config-1..3 layer shapes at full size, in the launch configuration the
-    bench times, checked on 24 sampled columns x all M rows each."""
-    seed = {1: 1, 16: 2, 32: 3, 64: 3, 128: 3}[M]
+FULL_MS = (1, 16, 32, 64, 128)
+
+
+def _layer_inputs(seed, Ms):
+    """The layer's six weights (stream i) and, per M, their activations."""
     rng = synth.streams(seed, len(synth.LAYER_SHAPES) + 8)
+    ws = [synth.weights(rng[i], K, N) for i, (_, K, N) in enumerate(synth.LAYER_SHAPES)]
+    xs = {M: [synth.activations(synth.streams(seed * 1000 + M, len(synth.LAYER_SHAPES))[i], M, K)
+              for i, (_, K, _) in enumerate(synth.LAYER_SHAPES)] for M in Ms}
+    return ws, xs
+
+
+@pytest.mark.parametrize("seed", [1, 3])
+def test_gemm_full_layer_every_output(dev, w12mod, oracle, seed):
+    """Config-1..3 layer shapes at full size, one GEMM launch per matrix as
+    w12_gemm plans it, at M = 1, 16, 32, 64, 128 on the AUTO path and every
+    path that serves M: every output against the float64 definition, and 24
+    sampled columns against the oracle itself."""
+    ws, xs = _layer_inputs(seed, FULL_MS)
     for i, (name, K, N) in enumerate(synth.LAYER_SHAPES):
-        w = synth.weights(rng[i], K, N)
-        x = synth.activations(rng[len(synth.LAYER_SHAPES) + i], M, K)
+        w = ws[i]
         d, blob = w12mod.encode(w, w12mod.LAYOUT_NK)
         blob_d = w12mod.upload(blob, dev)
-        pick = np.random.default_rng(i)
-        ns = np.unique(np.r_[pick.integers(0, N, 22), [0, N - 1]])
-        # the oracle encodes and multiplies only the sampled columns
+        refs = dict(zip(FULL_MS, ref_gemm_f64(w, [xs[M][i] for M in FULL_MS])))
+        ns = np.unique(np.r_[np.random.default_rng(i).integers(0, N, 22), [0, N - 1]])
         od, oblob = oracle.encode(w[ns], oracle.LAYOUT_NK)
-        y_ref, s_ref = oracle.gemm(od, oblob, x)
-        for path in [0] + ([] if M == 1 else [2, 3]):
-            y = _run(w12mod, dev, d, blob_d, x, path)
-            check_gemm(y[:, ns], y_ref, s_ref, what=f"{name} M={M} path={path}")
+        for M in FULL_MS:
+            y_ref, s_ref = refs[M]
+            yo_ref, so_ref = oracle.gemm(od, oblob, xs[M][i])
+            for path in [0] + _paths(M):
+                y = _run(w12mod, dev, d, blob_d, xs[M][i], path)
+                check_gemm(y, y_ref, s_ref, what=f"{name} M={M} path={path} (every output)")
+                check_gemm(y[:, ns], yo_ref, so_ref, what=f"{name} M={M} path={path} (oracle)")
         del blob_d
 
 
@@ -250,26 +264,35 @@ def test_gemm_batched_repeatable(dev, w12mod, M, path):
         assert np.array_equal(a, bb)
 
 
-@pytest.mark.parametrize("M", [1, 4, 16, 128])
-def test_gemm_batched_full_layer(dev, w12mod, oracle, M):
-    """The layer's six linears in one launch, full size, sampled columns."""
-    rng = synth.streams(1, len(synth.LAYER_SHAPES) + 8)
-    items, ws_ = [], []
+def test_gemm_batched_full_layer(dev, w12mod, oracle):
+    """The layer's six linears in one launch (the launch the bench times),
+    full size, M = 1, 4, 16, 32, 64, 128 on the AUTO path and every path that
+    serves M: every output against the float64 definition, sampled columns
+    against the oracle."""
+    Ms = (1, 4, 16, 32, 64, 128)
+    ws, xs = _layer_inputs(1, Ms)
+    items = {M: [] for M in Ms}
+    refs = {M: [] for M in Ms}
+    orefs = {M: [] for M in Ms}
+    blobs = []
     for i, (name, K, N) in enumerate(synth.LAYER_SHAPES):
-        w = synth.weights(rng[i], K, N)
-        x = synth.activations(rng[len(synth.LAYER_SHAPES) + i], M, K)
-        d, blob = w12mod.encode(w, w12mod.LAYOUT_NK)
-        items.append((d, w12mod.upload(blob, dev), x))
-        ws_.append(w)
-    refs = []
-    for i, (name, K, N) in enumerate(synth.LAYER_SHAPES):
+        d, blob = w12mod.encode(ws[i], w12mod.LAYOUT_NK)
+        blobs.append((d, w12mod.upload(blob, dev)))
+        for M, r in zip(Ms, ref_gemm_f64(ws[i], [xs[M][i] for M in Ms])):
+            refs[M].append(r)
         ns = np.unique(np.r_[np.random.default_rng(i).integers(0, N, 20), [0, N - 1]])
-        refs.append((ns, oracle.gemm(*oracle.encode(ws_[i][ns], oracle.LAYOUT_NK), items[i][2])))
-    for path in [0] + _paths(M):
-        ys = _batched(w12mod, dev, items, M, path=path)
-        for i, (name, K, N) in enumerate(synth.LAYER_SHAPES):
-            ns, (y_ref, s_ref) = refs[i]
-            check_gemm(ys[i][:, ns], y_ref, s_ref, what=f"batched {name} M={M} path={path}")
+        od, oblob = oracle.encode(ws[i][ns], oracle.LAYOUT_NK)
+        for M in Ms:
+            orefs[M].append((ns, oracle.gemm(od, oblob, xs[M][i])))
+    for M in Ms:
+        items = [(d, b, xs[M][i]) for i, (d, b) in enumerate(blobs)]
+        for path in [0] + _paths(M):
+            ys = _batched(w12mod, dev, items, M, path=path)
+            for i, (name, K, N) in enumerate(synth.LAYER_SHAPES):
+                y_ref, s_ref = refs[M][i]
+                check_gemm(ys[i], y_ref, s_ref, what=f"batched {name} M={M} path={path} (every output)")
+                ns, (yo, so) = orefs[M][i]
+                check_gemm(ys[i][:, ns], yo, so, what=f"batched {name} M={M} path={path} (oracle)")
 
 
 def test_gemm_batched_argument_errors(dev, w12mod):
