@@ -98,7 +98,7 @@ struct BatchPlan {
     size_t counters[kMaxBatch] = {}, partial[kMaxBatch] = {};
     int64_t steps[kMaxBatch] = {}, NB[kMaxBatch] = {}, ubase[kMaxBatch] = {};
     size_t stream_partial = 0;  // [grid][slots][M][128] floats
-    int slots = 2;              // partial slots per CTA: 2, or 4 on the tcgen05 path (pair order)
+    int slots = 2;              // partial slots per CTA (a CTA's first and last tile pieces)
     size_t total = 0;
 };
 
@@ -120,12 +120,13 @@ int plan_batch(const w12_desc *d, int count, int64_t M, int path, BatchPlan *bp)
         if (!gemv_fits_32bit(&d[i])) return W12_ERR_SHAPE;
     }
     // Measured on the 27B-class layer (GB300, us per layer, GEMV / mma.sync
-    // / tcgen05): M = 1: 80.3 / 79.9 / 91.4, 16: - / 86.1 / 92.4,
-    // 32: - / 95.4 / 95.2, 64: - / 152 / 103, 128: - / 232 / 115.  At M = 1
-    // the weight stream is the whole cost and the CUDA-core GEMV does it
-    // with no tensor instructions; mma.sync and tcgen05 are level at 32,
-    // and tcgen05 takes over above it.
-    if (path == W12_PATH_AUTO) path = M == 1 ? W12_PATH_GEMV : M <= 32 ? W12_PATH_MMA : W12_PATH_TC;
+    // / tcgen05, early weight stream): M = 1: 79.9 / 79.3 / 86.8,
+    // 4: 120.1 / 79.9 / 86.8, 16: - / 84.9 / 87.9, 32: - / 94.2 / 90.3,
+    // 64: - / 156 / 98.5, 128: - / 229 / 111.4.  At M = 1 the weight stream
+    // is the whole cost and the warp-shuffle GEMV does it on the CUDA cores
+    // (within 1 % of mma.sync); mma.sync serves the small blocks and tcgen05
+    // takes over above 16 tokens.
+    if (path == W12_PATH_AUTO) path = M == 1 ? W12_PATH_GEMV : M <= 16 ? W12_PATH_MMA : W12_PATH_TC;
     if (path == W12_PATH_GEMV && M > 4) return W12_ERR_SHAPE;
     if (path != W12_PATH_GEMV && path != W12_PATH_MMA && path != W12_PATH_TC) return W12_ERR_ARG;
     Device dv;
@@ -151,17 +152,13 @@ int plan_batch(const w12_desc *d, int count, int64_t M, int path, BatchPlan *bp)
         cpt = kMmaCols;
         uk = kGroup;
     }
-    // The tcgen05 path runs the tiles of a product in pairs (units (pair,
-    // group, tile of the pair)); an odd tile count is padded by a phantom
-    // tile, whose units copy and store nothing.
-    const bool pairs = path == W12_PATH_TC;
-    bp->slots = pairs ? 4 : 2;
+    bp->slots = 2;
     size_t off = kWsHeader;
     for (int i = 0; i < count; ++i) {
         bp->steps[i] = ceil_div(d[i].K, uk);
         bp->NB[i] = ceil_div(d[i].N, cpt);
         bp->ubase[i] = bp->U;
-        bp->U += bp->steps[i] * (pairs ? (bp->NB[i] + 1) / 2 * 2 : bp->NB[i]);
+        bp->U += bp->steps[i] * bp->NB[i];
         bp->counters[i] = off;
         off += round256(4u * uint64_t(std::max<int64_t>(bp->NB[i], 1)));
     }
@@ -256,7 +253,7 @@ struct FusedPlan {
 
 int plan_fused(const w12_desc *d, int64_t M, FusedPlan *fp) {
     BatchPlan &bp = fp->bp;
-    int st = plan_batch(d, 1, M, M <= 32 ? W12_PATH_MMA : W12_PATH_TC, &bp);
+    int st = plan_batch(d, 1, M, M <= 16 ? W12_PATH_MMA : W12_PATH_TC, &bp);
     if (st != W12_OK) return st;
     Device dv;
     if (query_device(&dv) != W12_OK) return W12_ERR_CUDA;

@@ -1,11 +1,12 @@
 // async_common.cuh -- mbarrier primitives, shared-memory loads and named
 // barriers, inline PTX.
 //
-// Every wait is bounded: it polls with try_wait, backs off, and gives up after
-// the CTA's wait limit (kWaitLimitNs unless a launch asks for a shorter one)
-// of wall time, or as soon as another thread of the CTA has given up,
-// recording W12_ERR_TIMEOUT in the caller's error word.  No kernel of this
-// library can spin forever.
+// Every wait is bounded: it waits with try_wait (the hardware parks the warp
+// until the phase completes, for at most kSuspendNs at a time) and gives up
+// after the CTA's wait limit (kWaitLimitNs unless a launch asks for a
+// shorter one) of wall time, or as soon as another thread of the CTA has
+// given up, recording W12_ERR_TIMEOUT in the caller's error word.  No kernel
+// of this library can spin forever.
 #pragma once
 
 #include <cstdint>
@@ -65,6 +66,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the warp is parked by the hardware
+// until the phase completes or about `ns` nanoseconds have passed, instead
+// of polling (a polling loop takes issue slots from the warps that work).
+constexpr uint32_t kSuspendNs = 200000;  // 0.2 ms: an abort is seen within it
+
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete.  Returns false (and
 // sets ctl->abort and *err) on timeout, or false at once if the CTA has
 // already aborted.
@@ -73,17 +90,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, WaitCt
     volatile int *abort = &ctl->abort;
     const uint64_t limit = ctl->limit_ns;
     const uint64_t t0 = global_timer_ns();
-    for (uint32_t i = 0;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
+    for (;;) {
         if (*abort) return false;
-        if ((i & 255u) == 255u) {
-            if (global_timer_ns() - t0 > limit) {
-                *abort = 1;
-                if (err) atomicCAS(err, 0, W12_ERR_TIMEOUT);  // the first error of a call wins
-                return false;
-            }
+        if (mbar_try_wait_sleep(bar, parity, kSuspendNs)) return true;
+        if (global_timer_ns() - t0 > limit) {
+            *abort = 1;
+            if (err) atomicCAS(err, 0, W12_ERR_TIMEOUT);  // the first error of a call wins
+            return false;
         }
-        __nanosleep(32);
     }
 }
 
@@ -92,9 +106,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, WaitCt
 // exits after a timeout).
 __device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
     const uint64_t t0 = global_timer_ns();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!mbar_try_wait_sleep(bar, parity, kSuspendNs)) {
         if (global_timer_ns() - t0 > limit_ns) return;
-        __nanosleep(64);
     }
 }
 

@@ -16,7 +16,7 @@
 // right moves every field of both halves into its bf16 place, the two signs
 // crossing over.  The base is at most 240, so b + code (<= 255) never carries
 // between bytes.  An escape (code 15) leaves a wrong exponent that
-// patch_escapes() replaces.
+// esc_apply() (or patch_escapes()) replaces.
 #pragma once
 
 #include <cstdint>
@@ -128,6 +128,63 @@ __device__ __forceinline__ void patch_escapes(uint32_t out[16], uint32_t m0, uin
         for (int q = 0; q < 16; ++q)
             if (uint32_t(q) == idx) out[q] = (out[q] & ~mask) | val;
     }
+}
+
+// Escape patch-up split in two, so that the (rare) escape entries are read
+// while the rebuild runs: esc_begin() is called as soon as a column's meta
+// words m0 = meta[c], m1 = meta[c + 1] are in registers; it checks the
+// column's entry range (a corrupt range records W12_ERR_DEVICE and is not
+// followed) and starts the load of its first entry.  esc_apply() then
+// patches every entry whose pos falls in the 32 weights [pos0, pos0 + 32)
+// held in out[16] (pair r/2 of word r/8 ...), the first from the register,
+// any further ones (two or more escapes in one column of a group) loaded
+// then.
+struct EscPending {
+    uint32_t lo, hi, e0;
+};
+
+__device__ __forceinline__ uint32_t ldg_u16(const uint16_t *p) {
+    uint16_t r;
+    asm("ld.global.nc.u16 %0, [%1];" : "=h"(r) : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ EscPending esc_begin(bool col_valid, uint32_t m0, uint32_t m1, const uint16_t *esc,
+                                                uint64_t n_esc, int *err) {
+    EscPending e{m0 >> 8, m1 >> 8, 0u};
+    if (!col_valid || e.lo == e.hi) {
+        e.hi = e.lo;  // nothing to patch
+        return e;
+    }
+    if (e.hi < e.lo || uint64_t(e.hi) > n_esc || e.hi - e.lo > 128u) {
+        record_error(err, W12_ERR_DEVICE);
+        e.hi = e.lo;
+        return e;
+    }
+    e.e0 = ldg_u16(esc + e.lo);
+    return e;
+}
+
+__device__ __forceinline__ void esc_patch_one(uint32_t out[16], uint32_t pos0, uint32_t ent) {
+    const uint32_t pos = ent & 0x7Fu;
+    if ((pos & ~31u) != pos0) return;
+    const uint32_t j = pos & 31u;
+    const uint32_t idx = (j >> 3) * 4 + ((j & 7u) >> 1);
+    const uint32_t sh = (j & 1u) * 16u;
+    const uint32_t mask = 0x7F80u << sh;
+    const uint32_t val = (ent & 0x7F80u) << sh;
+#pragma unroll
+    for (int q = 0; q < 16; ++q)
+        if (uint32_t(q) == idx) out[q] = (out[q] & ~mask) | val;
+}
+
+// Patch the 32 weights of out (positions [pos0, pos0 + 32)) from a pending
+// escape range.
+__device__ __forceinline__ void esc_apply(const EscPending &e, uint32_t out[16], uint32_t pos0,
+                                          const uint16_t *esc) {
+    if (e.lo == e.hi) return;
+    esc_patch_one(out, pos0, e.e0);
+    for (uint32_t i = e.lo + 1; i < e.hi; ++i) esc_patch_one(out, pos0, ldg_u16(esc + i));
 }
 
 // Float ordering key for the argmax: larger key = larger value; NaN above

@@ -4,54 +4,53 @@
 // operand, the fp32 accumulator lives in tensor memory, and the tokens come
 // from shared memory.
 //
-// Work split: stream-K over units of one 128-k group of a 128-column tile,
-// as in the mma.sync stream kernel (stream_device.cuh), but in PAIR order:
-// the tiles of a product are taken two at a time (a phantom tile pads an odd
-// count), and within a pair the units run (kg, tile 0), (kg, tile 1),
-// (kg + 1, tile 0), ...  A "step" is the two units of one k-group of a pair:
-// both multiply the same tokens, so one token box (two boxes of 64 k x MP
-// tokens with the 128-byte swizzle, the canonical K-major layout of the UMMA
-// B operand) serves two units, and the tile of a unit is its parity.  CTA c
-// takes a balanced contiguous range of units (it may start or end in the
-// middle of a step).
+// Work split as in the mma.sync stream kernel (stream_device.cuh): units
+// of one 128-k group of a 128-column tile, stream-K over the whole batch.
+// Two rings feed a unit: the unit block (planes and meta words) lands in a
+// weight stage, and the unit's tokens -- two boxes of 64 k x MP tokens with
+// the 128-byte swizzle, the canonical K-major layout of the UMMA B operand
+// -- in a token slot.  A weight stage is free again once the decoders have
+// read it, a token slot only once the UMMAs that read it have completed, so
+// the two rings turn over at different rates; each has its own producer
+// warp.  Unit i of a CTA uses weight stage i % SW and token slot i % SX.
 //
 // Roles (one CTA per SM, 20 warps):
-//  - 16 decoder warps in two groups; group j takes the units of parity j
-//    (tile j of each pair), so two units are decoded at once.  Thread (w, l)
-//    of a group owns tile row r = 32 (w % 4) + l (tensor-memory lane r) and
-//    half h = (w % 8) / 4 of the group's 128 k.  Per unit it rebuilds its 64
-//    weights in registers ("reconstructing bit by bit in GEMM registers",
-//    SpecPilot summary, airadar.tv English edition, "Reasons" bullet 2),
-//    patches escapes, and stores them with tcgen05.st into one of the
-//    group's A buffers (64 columns, column c holding the bf16 pair k = 2c,
-//    2c + 1).  At the end of a tile piece the group reads its accumulator
-//    back (tcgen05.ld; warp w takes half (w % 8) / 4 of the tokens) and
-//    writes y or the stream-K partial slot, then runs the fix-up.
-//  - 1 weight producer warp: one bulk copy per unit block into the group's
-//    weight ring, and the L1 prefetch of each tile piece's escape entries.
-//  - 1 token producer warp: one token box per step into the token ring.
-//  - 2 MMA warps, issuer j for the units of parity j (the first also
-//    allocates and frees the tensor memory): the first thread of each
-//    issues the 8 UMMAs of a unit (M = 128 columns, N = MP tokens, K = 16:
-//    D_j += A_tmem . B_smem) once the step's tokens have landed and the
-//    unit's A buffer is written, then commits them to the A buffer's empty
-//    barrier, and after the step to the token slot's empty barrier (two
-//    arrivals, one per issuer, so a slot turns over only when both tiles'
-//    UMMAs have read it); after a piece's last unit it commits to the
-//    accumulator's full barrier.
-// The three rings are independent: a weight stage is free once the decoders
-// have read it, an A buffer once its UMMAs have completed, a token slot once
-// both issuers' UMMAs of the step have completed; so the decoders never wait
-// for tokens, and the token ring prefetches as far ahead as it is deep.
-// Tensor memory: D_0 at column 0, D_1 at MP, then the A buffers (NA per
-// group); 512 columns allocated.  A K = 16 UMMA of M = 128 takes 45 cycles
+//  - 16 decoder warps in two groups that take alternate units, so two
+//    units are decoded at once.  Thread (w, l) of a group owns tile row
+//    r = 32 (w % 4) + l (tensor-memory lane r) and half h = (w % 8) / 4 of
+//    the group's 128 k.  Per unit it rebuilds its 64 weights in registers
+//    ("reconstructing bit by bit in GEMM registers", SpecPilot summary,
+//    airadar.tv English edition, "Reasons" bullet 2), patches escapes, and
+//    stores them with tcgen05.st into the A buffer of the unit's token slot
+//    (64 columns, column j holding the bf16 pair k = 2j, 2j + 1).  At the
+//    end of a tile piece all 16 warps read the accumulator back (tcgen05.ld;
+//    warp w takes a quarter w / 4 of the tokens) and write y or the
+//    stream-K partial slot, then run the fix-up.
+//  - 1 weight producer warp: one bulk copy per unit block into the weight
+//    ring, and the L1 prefetch of each tile piece's escape entries.
+//  - 1 token producer warp: the two x boxes of each unit into the token ring.
+//  - 2 MMA warps, one per unit parity (the first also allocates and frees
+//    the tensor memory): the first thread of each issues the 8 UMMAs of its
+//    units (M = 128 columns, N = MP tokens, K = 16: D_t += A_tmem . B_smem)
+//    into its own accumulator D_t once A is in place (the decoders signal
+//    that only after they saw the unit's tokens land), and commits them to
+//    the token slot's empty barrier and, after a piece's last unit, to the
+//    accumulators' barrier.  The epilogue adds D_0 and D_1.
+// Tensor memory: the accumulators at columns 0 and MP, then one A buffer of
+// 64 columns per token slot; 512 columns allocated.  The slot's commit
+// releases both; decoders that see the slot full again know that the UMMAs
+// which read its A buffer last have completed (the producer refilled the
+// slot only after that commit).  A K = 16 UMMA of M = 128 takes 45 cycles
 // at N <= 32 and 64 at N = 128 (measured), but on its issuing thread every
 // mbarrier wait costs ~200 cycles and every commit ~45 while UMMAs are in
-// flight; with two issuers one's wait overlaps the other's UMMAs.
+// flight; with two issuers one's wait overlaps the other's UMMAs, and the
+// tensor core runs at the bare UMMA rate (measured: 44 cycles per UMMA
+// with a wait and a commit per 8, against 78 with one issuer).
 // Every mbarrier wait is bounded; after a timeout every role runs to its
 // end without waiting and the error word says W12_ERR_TIMEOUT.  The
-// producers let their copies in flight land and the MMA threads wait
-// (bounded) for their UMMAs before the tensor memory is freed.
+// producers stop issuing once the CTA has aborted and let their copies in
+// flight land, and each MMA thread waits (bounded) for its own UMMAs before
+// the tensor memory is freed.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -64,31 +63,27 @@ namespace {
 
 constexpr int kDW = 16;                  // decoder warps
 constexpr int kDT = kDW * 32;
-constexpr int kGT = kDT / 2;             // threads of one decoder group
 constexpr int kWProdWarp = kDW;          // weight producer
 constexpr int kXProdWarp = kDW + 1;      // token producer
-constexpr int kMmaWarp = kDW + 2;        // tensor-memory owner, UMMA issuer of tile 0
+constexpr int kMmaWarp = kDW + 2;        // tensor-memory owner, UMMA issuer of the even units
+constexpr int kMmaWarp1 = kDW + 3;       // UMMA issuer of the odd units
 constexpr int kTT = (kDW + 4) * 32;      // 640 threads
 constexpr uint32_t kTmemCols = 512;
-// named barriers: 1 all decoders, 2 + j decoder group j, 4 decoders + the
-// tensor-memory owner (end of the kernel)
-constexpr uint32_t kBarGroup = 2, kBarEnd = 4;
 
 template <int MP>
 struct TCfg {
     static constexpr int kX = MP * 256;                        // token slot: two boxes of MP rows x 128 bytes
-    static constexpr int SX = MP >= 128 ? 2 : MP >= 64 ? 4 : MP >= 32 ? 3 : 4;  // token slots
+    static constexpr int SX = MP >= 128 ? 3 : 4;               // token slots (and A buffers)
     static constexpr int kXRing = SX * kX;                     // at the (1024-aligned) start of the ring
     static constexpr int kW = (kUnitBytes + 127) / 128 * 128;  // weight stage stride
     static constexpr int kFit = (227 * 1024 - 1024 - 2048 - kXRing) / kW;
-    static constexpr int SWG = (kFit > 8 ? 8 : kFit) / 2;      // weight stages per decoder group
-    static constexpr size_t kDynSmem = size_t(kXRing) + size_t(2 * SWG) * kW + 1024;
-    // tensor-memory columns: accumulators [0, MP) and [MP, 2 MP); A buffer a
-    // of group j at kA + 64 (j NA + a)
+    static constexpr int SW = kFit > 8 ? 8 : kFit;             // weight stages, after the token ring
+    static constexpr size_t kDynSmem = size_t(kXRing) + size_t(SW) * kW + 1024;
+    // tensor-memory columns: accumulators [0, MP) and [MP, 2 MP), A buffer of
+    // slot s at kA + 64 s
     static constexpr uint32_t kA = 2 * MP < 64 ? 64u : uint32_t(2 * MP);
-    static constexpr int NA = int((kTmemCols - kA) / 128u) > 4 ? 4 : int((kTmemCols - kA) / 128u);
-    static_assert(kA + 128u * NA <= kTmemCols, "A buffers exceed the tensor memory");
-    static_assert(SWG >= 2 && NA >= 2, "rings too shallow");
+    static_assert(kA + 64u * SX <= kTmemCols, "A buffers exceed the tensor memory");
+    static_assert(SW >= 2, "weight ring too shallow");
 };
 
 // UMMA shared-memory descriptor of a K-major operand with the 128-byte
@@ -141,263 +136,89 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// Load 8 consecutive 32-bit columns of this thread's lane (no wait).
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-                   "=r"(r[7])
+// Load 4 consecutive 32-bit columns of this thread's lane (tmem_ld_wait()
+// before the registers are used).
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t (&r)[4]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                  : "r"(taddr));
 }
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ void named_sync_id(uint32_t id, uint32_t nthreads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+// Both rings signal a landed fill on a barrier of the decoder group that
+// owns the unit (full[2 s + (i & 1)] for unit i in slot s = i % S), so each
+// group waits on its own barriers only and sees their phases one by one.
+// The parity of unit i's fill on that barrier: the group's fills of slot s
+// are every fill of it (S even) or every other one (S odd).  A barrier
+// cannot run two phases ahead of its group: the fill after unit i's on the
+// same barrier needs the group's own release of unit i first.
+template <int S>
+__device__ __forceinline__ uint32_t group_parity(int i) {
+    const int k = i / S;
+    return uint32_t((S & 1) ? (k >> 1) : k) & 1u;
 }
 
-__device__ __forceinline__ void named_arrive_id(uint32_t id, uint32_t nthreads) {
-    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-// A slot of a ring: index and the parity of its current fill.
-struct Ring {
-    int s;
-    uint32_t ph;
-    template <int S>
-    __device__ __forceinline__ void next() {
-        if (++s == S) {
-            s = 0;
-            ph ^= 1u;
-        }
-    }
-};
-
-// Cursor over the pair order of a batch: product gi, pair p, group kg,
-// tile j of the pair (tile 2 p + j of the product).  Every product has an
-// even number of units (KG x the tile count rounded up to even), so the
-// parity of a unit index is its j.
-struct PCur {
-    int gi, p, kg, j;
-};
-
-__device__ __forceinline__ int pairs_of(const StreamOne &g) { return (g.NB + 1) >> 1; }
-
-__device__ __forceinline__ PCur p_at(const StreamBatch &b, int u) {
-    PCur c{0, 0, 0, 0};
-    while (c.gi + 1 < b.count && u >= b.g[c.gi + 1].ubase) ++c.gi;
-    const int local = u - b.g[c.gi].ubase, KG = b.g[c.gi].KG;
-    c.p = local / (2 * KG);
-    const int r = local - c.p * 2 * KG;
-    c.kg = r >> 1;
-    c.j = r & 1;
-    return c;
-}
-
-// The next step (same j).
-__device__ __forceinline__ void p_next_step(const StreamBatch &b, PCur &c) {
-    if (++c.kg == b.g[c.gi].KG) {
-        c.kg = 0;
-        if (++c.p == pairs_of(b.g[c.gi])) {
-            c.p = 0;
-            ++c.gi;
-        }
-    }
-}
-
-__device__ __forceinline__ void p_next(const StreamBatch &b, PCur &c) {
-    if (c.j == 0) {
-        c.j = 1;
-    } else {
-        c.j = 0;
-        p_next_step(b, c);
-    }
-}
-
-__device__ __forceinline__ int pair_first(const StreamBatch &b, const PCur &c) {
-    return b.g[c.gi].ubase + c.p * 2 * b.g[c.gi].KG;
-}
-
-// The units of tile j of the pair that starts at unit pf (KG groups) which
-// lie in [lo, hi): their number.
-__device__ __forceinline__ int tile_units_in(int pf, int KG, int j, int lo, int hi) {
-    lo = max(lo, pf + j);
-    hi = min(hi, pf + 2 * KG);
-    if (hi <= lo) return 0;
-    // units pf + j + 2 t for t = 0 .. KG - 1
-    const int t0 = (lo - pf - j + 1) >> 1, t1 = (hi - pf - j + 1) >> 1;
-    return t1 - t0;
-}
-
-// L1 prefetch of the escape entries of tile nb's groups [kg0, kg1) (one
-// contiguous range of the escape list), at most kEscPrefetchLines lines.
-__device__ __forceinline__ void prefetch_tile_escapes(const StreamOne &g, int nb, int kg0, int kg1) {
-    const uint8_t *u0 = g.units + size_t(uint32_t(nb) * uint32_t(g.KG) + uint32_t(kg0)) * kUnitBytes;
-    const uint8_t *u1 = g.units + size_t(uint32_t(nb) * uint32_t(g.KG) + uint32_t(kg1 - 1)) * kUnitBytes;
-    const uint32_t lo = ldg_u32(reinterpret_cast<const uint32_t *>(u0 + kMetaAt)) >> 8;
-    const uint32_t hi = min(ldg_u32(reinterpret_cast<const uint32_t *>(u1 + kMetaAt + 4 * kTileN)) >> 8, g.n_esc);
-    if (lo < hi) {
-        const uintptr_t a0 = reinterpret_cast<uintptr_t>(g.esc + lo) & ~uintptr_t(127);
-        const uintptr_t a1 = reinterpret_cast<uintptr_t>(g.esc + hi);
-        for (int q = 0; q < kEscPrefetchLines; ++q) {
-            const uintptr_t a = a0 + uintptr_t(q) * 128u;
-            if (a >= a1) break;
-            prefetch_l1(reinterpret_cast<const void *>(a));
-        }
-    }
-}
-
-// Weight producer (lane 0 of its warp): unit u of the CTA into the next
-// stage of group u & 1's weight ring, once the group has released the
-// stage's previous unit.  A phantom tile's unit (the padding tile of an odd
-// tile count) copies nothing: the producer only arrives on the stage.
-template <int SWG>
+// Weight producer (lane 0 of its warp): unit i of the CTA into weight stage
+// i % SW, once the decoders have released the stage's previous unit.  It
+// reads the blob only after the previous kernel of the stream completed,
+// unless the launch asked for the early weight stream (b.early_weights: the
+// blob is not written by that kernel).  The test hook b.withhold_unit
+// leaves one unit's stage unarmed, so its decoders' bounded wait runs out.
+template <int SW>
 __device__ __forceinline__ void tc_weight_producer(const StreamBatch &b, uint32_t wbase, uint32_t stride,
-                                                   uint64_t (*full_w)[SWG], uint64_t (*empty_w)[SWG],
-                                                   WaitCtl *ctl, int u0, int u1) {
+                                                   uint64_t *full_w, uint64_t *empty_w, WaitCtl *ctl, int u0,
+                                                   int u1) {
     if (!b.early_weights) pdl_wait();
     const uint64_t pol = l2_evict_first_policy();
-    Ring r[2] = {{0, 0u}, {0, 0u}};
-    int issued[2] = {0, 0};
-    PCur c = p_at(b, u0);
-    for (int u = u0; u < u1; ++u, p_next(b, c)) {
-        const int j = c.j;
-        Ring &q = r[j];
+    SCur c = s_at(b, u0);
+    int issued = 0;
+    for (int u = u0; u < u1; ++u) {
+        const int i = u - u0, s = i % SW;
         // (a decoder that gave up sets the abort flag before it arrives
         // without waiting: stop, so the drain below covers every copy in flight)
-        if (issued[j] >= SWG && (!mbar_wait(&empty_w[j][q.s], q.ph ^ 1u, ctl, b.err) || aborted(ctl))) break;
+        if (i >= SW && (!mbar_wait(&empty_w[s], uint32_t(i / SW - 1) & 1u, ctl, b.err) || aborted(ctl))) break;
         const StreamOne &g = b.g[c.gi];
-        const int nb = 2 * c.p + j;
-        uint64_t *bar = &full_w[j][q.s];
+        const uint8_t *unit = unit_block(g, c);
         if (u != b.withhold_unit) {
-            if (nb >= g.NB) {
-                mbar_arrive(bar);
-            } else {
-                const int pf = pair_first(b, c);
-                if (c.kg == 0 || u - 2 < u0) {
-                    // first unit of this tile in the CTA: prefetch the
-                    // escapes of the tile's groups up to the CTA's last one
-                    const int last = min(u1 - 1, pf + 2 * g.KG - 1);
-                    const int lu = (last & 1) == j ? last : last - 1;
-                    prefetch_tile_escapes(g, nb, c.kg, ((lu - pf) >> 1) + 1);
-                }
-                mbar_expect_tx(bar, uint32_t(kUnitBytes));
-                bulk_copy(wbase + uint32_t(j * SWG + q.s) * stride,
-                          g.units + size_t(uint32_t(nb) * uint32_t(g.KG) + uint32_t(c.kg)) * kUnitBytes,
-                          uint32_t(kUnitBytes), bar, pol);
-            }
+            if (u == u0 || c.kg == 0) prefetch_piece_escapes(g, c, unit, u, u1);
+            uint64_t *bar = &full_w[2 * s + (i & 1)];
+            mbar_expect_tx(bar, uint32_t(kUnitBytes));
+            bulk_copy(wbase + uint32_t(s) * stride, unit, uint32_t(kUnitBytes), bar, pol);
         }
-        ++issued[j];
-        q.template next<SWG>();
+        s_next(b, c);
+        ++issued;
     }
-    if (aborted(ctl)) {  // let the copies in flight land
-        for (int j = 0; j < 2; ++j) {
-            Ring q = r[j];
-            for (int k = 0; k < SWG && k < issued[j]; ++k) {
-                if (--q.s < 0) {
-                    q.s = SWG - 1;
-                    q.ph ^= 1u;
-                }
-                mbar_drain(&full_w[j][q.s], q.ph, ctl->limit_ns);
-            }
-        }
-    }
+    if (aborted(ctl))  // let the copies in flight land
+        for (int j = issued - 1; j >= 0 && j >= issued - SW; --j)
+            mbar_drain(&full_w[2 * (j % SW) + (j & 1)], group_parity<SW>(j), ctl->limit_ns);
 }
 
-// Token producer (lane 0 of its warp): the token box of each of the CTA's
-// steps into the next token slot, once both issuers' UMMAs that read the
-// slot's previous step have completed.  x may be written by the previous
-// kernel of the stream.
+// Token producer (lane 0 of its warp): the two 64-k boxes of unit i's tokens
+// into token slot i % SX, once the UMMAs that read the slot's previous unit
+// have completed.  x may be written by the previous kernel of the stream.
 template <int SX>
 __device__ __forceinline__ void tc_x_producer(const StreamBatch &b, uint32_t xbase, int mp, uint64_t *full_x,
                                               uint64_t *empty_x, WaitCtl *ctl, int u0, int u1) {
     pdl_wait();
     const uint32_t kx = uint32_t(mp) * 256u;
-    const int nsteps = ((u1 - 1) >> 1) - (u0 >> 1) + 1;
-    PCur c = p_at(b, u0);
-    Ring q{0, 0u};
+    SCur c = s_at(b, u0);
     int issued = 0;
-    for (int t = 0; t < nsteps; ++t, p_next_step(b, c)) {
-        if (t >= SX && (!mbar_wait(&empty_x[q.s], q.ph ^ 1u, ctl, b.err) || aborted(ctl))) break;
+    for (int u = u0; u < u1; ++u) {
+        const int i = u - u0, s = i % SX;
+        if (i >= SX && (!mbar_wait(&empty_x[s], uint32_t(i / SX - 1) & 1u, ctl, b.err) || aborted(ctl))) break;
         const StreamOne &g = b.g[c.gi];
-        const uint32_t dst = xbase + uint32_t(q.s) * kx;
-        uint64_t *bar = &full_x[q.s];
+        const uint32_t dst = xbase + uint32_t(s) * kx;
+        uint64_t *bar = &full_x[2 * s + (i & 1)];
         mbar_expect_tx(bar, kx);
         tma_2d_keep(dst, &g.tx, 128 * c.kg, 0, bar);
         tma_2d_keep(dst + uint32_t(mp) * 128u, &g.tx, 128 * c.kg + 64, 0, bar);
+        s_next(b, c);
         ++issued;
-        q.template next<SX>();
     }
     if (aborted(ctl))
-        for (int k = 0; k < SX && k < issued; ++k) {
-            if (--q.s < 0) {
-                q.s = SX - 1;
-                q.ph ^= 1u;
-            }
-            mbar_drain(&full_x[q.s], q.ph, ctl->limit_ns);
-        }
-}
-
-// Stream-K fix-up of tile nb = 2 p + j of a pair that starts at unit pf,
-// run by the kGT threads of decoder group j (named barrier kBarGroup + j).
-// Each piece of the tile adds its unit count to counters[nb]; the group
-// that completes the count sums the pieces' partial slots in CTA order (the
-// same bits on every call), writes y and resets the counter.  CTA c keeps
-// the piece of the pair that contains its first unit in slots 0 + j and
-// its other (last) pair piece in slots 2 + j.
-template <bool FUSED>
-__device__ __forceinline__ void tc_fixup(const StreamBatch &b, const StreamOne &g, int pf, int nb, int j,
-                                         int count, int *s_last, int gtid, unsigned long long *s_best) {
-    __threadfence();
-    named_sync_id(kBarGroup + j, kGT);
-    if (gtid == 0) {
-        const uint32_t old = atomicAdd(&g.counters[nb], uint32_t(count));
-        *s_last = (int(old) + count == g.KG);
-    }
-    named_sync_id(kBarGroup + j, kGT);
-    if (*s_last) {
-        __threadfence();
-        const int G = int(gridDim.x), per = b.U / G, rem = b.U % G;
-        const int KG = g.KG;
-        const int c_first = sk_cta_of(pf + j, per, rem), c_last = sk_cta_of(pf + 2 * (KG - 1) + j, per, rem);
-        const int M = b.M;
-        const size_t slot_floats = size_t(M) * kTileN;
-        for (int o = gtid; o < M * (kTileN / 4); o += kGT) {
-            const int m = o / (kTileN / 4), c4 = o % (kTileN / 4);
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            bool started = false;
-            for (int c = c_first; c <= c_last; ++c) {
-                const int beg = sk_unit_begin(c, per, rem), end = sk_unit_begin(c + 1, per, rem);
-                if (tile_units_in(pf, KG, j, beg, end) == 0) continue;
-                const int slot = (beg >= pf ? 0 : 2) + j;
-                const float4 v = __ldcg(reinterpret_cast<const float4 *>(
-                    b.partial + (size_t(c) * 4 + slot) * slot_floats + size_t(m) * kTileN) + c4);
-                if (!started) {
-                    acc = v;
-                    started = true;
-                } else {
-                    acc.x += v.x;
-                    acc.y += v.y;
-                    acc.z += v.z;
-                    acc.w += v.w;
-                }
-            }
-            const int n0 = nb * kTileN + 4 * c4;
-            const float r[4] = {acc.x, acc.y, acc.z, acc.w};
-            unsigned long long best = 0ull;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                if (n0 + e >= g.N) continue;
-                if (!FUSED || g.y) store_out(g.y, b.y_dtype, g.N, m, n0 + e, r[e]);
-                if (FUSED) {
-                    const unsigned long long k = pack_key(r[e], uint32_t(n0 + e));
-                    best = k > best ? k : best;
-                }
-            }
-            if (FUSED && best != 0ull) atomicMax(&s_best[m], best);
-        }
-        if (gtid == 0) g.counters[nb] = 0u;
-    }
-    named_sync_id(kBarGroup + j, kGT);  // s_last is reused by the next piece
+        for (int j = issued - 1; j >= 0 && j >= issued - SX; --j)
+            mbar_drain(&full_x[2 * (j % SX) + (j & 1)], group_parity<SX>(j), ctl->limit_ns);
 }
 
 // FUSED: the lm_head + greedy verify epilogue (as in kernels_stream.cu):
@@ -407,15 +228,15 @@ __device__ __forceinline__ void tc_fixup(const StreamBatch &b, const StreamOne &
 template <int MP, bool FUSED>
 __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ StreamBatch b) {
     using C = TCfg<MP>;
-    constexpr int SWG = C::SWG, SX = C::SX, NA = C::NA;
+    constexpr int SW = C::SW, SX = C::SX;
     extern __shared__ unsigned char smem_dyn[];
-    __shared__ __align__(8) uint64_t full_w[2][SWG], empty_w[2][SWG], full_x[SX], empty_x[SX];
-    __shared__ __align__(8) uint64_t a_full[2][NA], a_empty[2][NA], acc_full[2], acc_empty[2], fin;
+    __shared__ __align__(8) uint64_t full_w[2 * SW], empty_w[SW], full_x[2 * SX], empty_x[SX], a_full[2 * SX];
+    __shared__ __align__(8) uint64_t acc_full, acc_empty, fin;
     __shared__ uint32_t s_tmem;
     __shared__ WaitCtl s_ctl;
-    __shared__ int s_last[2];
+    __shared__ int s_last;
     __shared__ unsigned long long s_best[FUSED ? MP : 1];
-    const uint32_t xbase = (smem_addr(smem_dyn) + 1023u) & ~1023u;  // token ring, then the weight rings
+    const uint32_t xbase = (smem_addr(smem_dyn) + 1023u) & ~1023u;  // token ring, then the weight ring
     const uint32_t wbase = xbase + uint32_t(C::kXRing);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int u0, u1;
@@ -426,22 +247,13 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
         u1 = u0 + per + (c < rem ? 1 : 0);
     }
     if (threadIdx.x == 0) {
-        for (int j = 0; j < 2; ++j) {
-            for (int s = 0; s < SWG; ++s) {
-                mbar_init(&full_w[j][s], 1);       // the producer's (expect_tx) arrival
-                mbar_init(&empty_w[j][s], kDW / 2);  // the group's warps
-            }
-            for (int a = 0; a < NA; ++a) {
-                mbar_init(&a_full[j][a], kDW / 2);  // the group's warps
-                mbar_init(&a_empty[j][a], 1);       // the issuer's commit
-            }
-            mbar_init(&acc_full[j], 1);
-            mbar_init(&acc_empty[j], kDW / 2);
-        }
-        for (int s = 0; s < SX; ++s) {
-            mbar_init(&full_x[s], 1);
-            mbar_init(&empty_x[s], 2);  // one commit per issuer and step
-        }
+        for (int s = 0; s < 2 * SW; ++s) mbar_init(&full_w[s], 1);  // the producer's expect_tx arrival (+ bytes)
+        for (int s = 0; s < 2 * SX; ++s) mbar_init(&full_x[s], 1);
+        for (int s = 0; s < SW; ++s) mbar_init(&empty_w[s], kDW / 2);  // the decoder group of the unit
+        for (int s = 0; s < SX; ++s) mbar_init(&empty_x[s], 1);         // the unit's UMMA commit
+        for (int s = 0; s < 2 * SX; ++s) mbar_init(&a_full[s], kDW / 2);  // per decoder group, as full_x
+        mbar_init(&acc_full, 2);  // both issuers' commits after a piece's last unit
+        mbar_init(&acc_empty, kDW);
         mbar_init(&fin, 2);
         wait_ctl_init(&s_ctl, b);
         mbar_fence_init();
@@ -461,7 +273,7 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
     if (threadIdx.x == 0) pdl_launch();
 
     if (warp == kWProdWarp) {
-        if (lane == 0 && u0 < u1) tc_weight_producer<SWG>(b, wbase, C::kW, full_w, empty_w, &s_ctl, u0, u1);
+        if (lane == 0 && u0 < u1) tc_weight_producer<SW>(b, wbase, C::kW, full_w, empty_w, &s_ctl, u0, u1);
         return;
     }
     if (warp == kXProdWarp) {
@@ -470,36 +282,32 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
     }
     pdl_wait();  // nothing below touches global memory the previous kernel may write before this
 
-    if (warp >= kMmaWarp) {
+    if (warp == kMmaWarp || warp == kMmaWarp1) {
         // ----------------------------------------------------------- UMMA issuers
-        const int j = warp - kMmaWarp;  // units of parity j, accumulator D_j
-        if (lane == 0 && u0 < u1) {
+        const int t = warp - kMmaWarp;  // units of parity t, accumulator t
+        if (lane == 0) {
             const uint32_t idesc = idesc_bf16<MP>();
-            const uint32_t dt = tmem + uint32_t(j * MP);
-            const int nsteps = ((u1 - 1) >> 1) - (u0 >> 1) + 1;
-            PCur c = p_at(b, u0 & ~1);
-            Ring xq{0, 0u}, aq{0, 0u};
-            int pieces = 0;
-            bool fresh = true;
-            for (int t = 0; t < nsteps; ++t, p_next_step(b, c)) {
-                const int u = ((u0 >> 1) + t) * 2 + j;
-                // every issuer waits for every step's tokens, so each phase
-                // of a slot's empty barrier gets exactly the step's two commits
-                mbar_wait(&full_x[xq.s], xq.ph, &s_ctl, b.err);
-                if (u >= u0 && u < u1) {
-                    const StreamOne &g = b.g[c.gi];
-                    const bool first = c.kg == 0 || u - 2 < u0;
-                    const bool last = c.kg == g.KG - 1 || u + 2 >= u1;
-                    if (first) {
-                        // the epilogue of the previous piece has read D_j
-                        if (pieces > 0) mbar_wait(&acc_empty[j], uint32_t(pieces - 1) & 1u, &s_ctl, b.err);
-                        fresh = true;
-                    }
-                    mbar_wait(&a_full[j][aq.s], aq.ph, &s_ctl, b.err);
-                    tc_fence_after();
-                    if (2 * c.p + j < g.NB) {
-                        const uint64_t d0 = desc_sw128(xbase + uint32_t(xq.s) * uint32_t(C::kX));
-                        const uint32_t ta = tmem + C::kA + 64u * uint32_t(j * NA + aq.s);
+            const uint32_t dt = tmem + uint32_t(t * MP);
+            SCur c = s_at(b, u0);
+            int i = 0, piece = 0;
+            for (int u = u0; u < u1;) {
+                const StreamOne &g = b.g[c.gi];
+                const int first = g.ubase + c.nb * g.KG;
+                const int ub = min(u1, first + g.KG);
+                // the epilogue of the previous piece has read the accumulators
+                if (piece > 0) mbar_wait(&acc_empty, uint32_t(piece - 1) & 1u, &s_ctl, b.err);
+                tc_fence_after();
+                bool fresh = true;  // this issuer's next UMMA starts its sum of the piece
+                for (; u < ub; ++u, ++i) {
+                    if ((i & 1) == t) {
+                        const int sx = i % SX;
+                        // The decoders that signal a_full waited for this
+                        // slot's full barrier first (tokens landed), so the
+                        // UMMAs may read it once a_full is observed.
+                        mbar_wait(&a_full[2 * sx + t], group_parity<SX>(i), &s_ctl, b.err);
+                        tc_fence_after();
+                        const uint64_t d0 = desc_sw128(xbase + uint32_t(sx) * uint32_t(C::kX));
+                        const uint32_t ta = tmem + C::kA + 64u * uint32_t(sx);
 #pragma unroll
                         for (int ks = 0; ks < 8; ++ks) {
                             // x box ks / 4 (k half), 16 k = 32 bytes per step inside the swizzle atom
@@ -507,28 +315,20 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
                             umma_ts(dt, ta + 8u * uint32_t(ks), dx, idesc, (fresh && ks == 0) ? 0u : 1u);
                         }
                         fresh = false;
+                        umma_commit(&empty_x[sx]);  // frees the token slot and its A buffer
                     }
-                    umma_commit(&a_empty[j][aq.s]);  // frees the A buffer
-                    aq.template next<NA>();
-                    if (last) {
-                        umma_commit(&acc_full[j]);
-                        ++pieces;
-                    }
+                    if (u == ub - 1) umma_commit(&acc_full);
                 }
-                umma_commit(&empty_x[xq.s]);  // this issuer is done with the slot
-                xq.template next<SX>();
+                ++piece;
+                s_next_tile(b, c);
             }
             // every UMMA issued has completed before the memory is freed
             umma_commit(&fin);
             mbar_drain(&fin, 0u, s_ctl.limit_ns);
-        } else if (lane == 0) {
-            umma_commit(&fin);
-            mbar_drain(&fin, 0u, s_ctl.limit_ns);
+            if (piece > 0) mbar_wait(&acc_empty, uint32_t(piece - 1) & 1u, &s_ctl, b.err);
         }
         __syncwarp();
         if (warp == kMmaWarp) {
-            // the decoders have read the accumulators back
-            named_sync_id(kBarEnd, kDT + 32);
             tc_fence_after();
             asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
                          : "memory");
@@ -537,125 +337,124 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
     }
 
     // ---------------------------------------------------------------- decoders
-    const int j = warp >> 3;               // tile of the pair = unit parity
-    const int gtid = threadIdx.x - j * kGT;
     const int r = 32 * (warp & 3) + lane;  // tile row = tensor-memory lane
-    const int h = (warp & 7) >> 2;         // k half of the group; token half of the epilogue
+    const int grp = warp >> 3;             // units of this parity
+    const int h = (warp & 7) >> 2;         // k half of the group
+    const int qt = warp >> 2;              // token quarter of the epilogue
     const uint32_t lane_off = uint32_t(32 * (warp & 3)) << 16;
     // plane row r, logical 16-byte chunks 2h and 2h + 1 (the format stores
-    // chunk q of row r at q ^ ((r >> 1) & 3): a warp's 32 rows read 8
+    // chunk j of row r at j ^ ((r >> 1) & 3): a warp's 32 rows read 8
     // different bank groups per quarter-warp)
     const uint32_t sw = uint32_t((r >> 1) & 3);
     const uint32_t p0 = uint32_t(r * 64) + ((uint32_t(2 * h) ^ sw) << 4);
     const uint32_t p1 = uint32_t(r * 64) + ((uint32_t(2 * h + 1) ^ sw) << 4);
-    const uint32_t wst0 = wbase + uint32_t(j * SWG) * uint32_t(C::kW);
-    const uint32_t a0col = tmem + lane_off + C::kA + 64u * uint32_t(j * NA) + 32u * uint32_t(h);
     const int M = b.M;
-    Ring wq{0, 0u}, aq{0, 0u};
-    int uses = 0, pieces = 0;
-    int ua = -1;  // first unit of the current piece
-    const int ufirst = (u0 & 1) == j ? u0 : u0 + 1;
-    PCur c = p_at(b, ufirst < u1 ? ufirst : u0);
-    for (int u = ufirst; u < u1; u += 2, p_next_step(b, c)) {
+    SCur c = s_at(b, u0);
+    int i = 0, piece = 0;
+    for (int u = u0; u < u1;) {
         const StreamOne &g = b.g[c.gi];
-        const int nb = 2 * c.p + j;
-        const bool real = nb < g.NB;
-        if (c.kg == 0 || ua < 0) ua = u;
-        mbar_wait(&full_w[j][wq.s], wq.ph, &s_ctl, b.err);
-        uint32_t w[32];
-        if (real) {
-            const uint32_t st = wst0 + uint32_t(wq.s) * uint32_t(C::kW);
-            const uint4 h0 = lds128(st + p0), h1 = lds128(st + p1);
-            const uint4 l0 = lds128(st + kPlaneBlock + p0), l1 = lds128(st + kPlaneBlock + p1);
-            const uint4 e0 = lds128(st + 2 * kPlaneBlock + p0), e1 = lds128(st + 2 * kPlaneBlock + p1);
-            const uint2 mw = make_uint2(lds32(st + kMetaAt + 4u * uint32_t(r)),
-                                        lds32(st + kMetaAt + 4u * uint32_t(r) + 4u));
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty_w[j][wq.s]);  // planes and meta read
-            uint32_t(&wlo)[16] = *reinterpret_cast<uint32_t(*)[16]>(&w[0]);
-            uint32_t(&whi)[16] = *reinterpret_cast<uint32_t(*)[16]>(&w[16]);
-            const uint32_t b4 = base4(mw.x);
-            rebuild32(h0, l0, e0, b4, wlo);
-            rebuild32(h1, l1, e1, b4, whi);
-            if (nb * kTileN + r < g.N && (mw.x >> 8) != (mw.y >> 8)) {
-                patch_escapes(wlo, mw.x, mw.y, uint32_t(64 * h), g.esc, g.n_esc, b.err);
-                patch_escapes(whi, mw.x, mw.y, uint32_t(64 * h + 32), g.esc, g.n_esc, b.err);
+        const int nb = c.nb, first = g.ubase + nb * g.KG;
+        const int ua = u, ub = min(u1, first + g.KG);
+        const int n = nb * kTileN + r;
+        const bool valid = n < g.N;
+        for (; u < ub; ++u, ++i) {
+            if ((i & 1) == grp) {
+                const int s = i % SW, sx = i % SX;
+                mbar_wait(&full_w[2 * s + grp], group_parity<SW>(i), &s_ctl, b.err);
+                const uint32_t st = wbase + uint32_t(s) * uint32_t(C::kW);
+                const uint4 h0 = lds128(st + p0), h1 = lds128(st + p1);
+                const uint4 l0 = lds128(st + kPlaneBlock + p0), l1 = lds128(st + kPlaneBlock + p1);
+                const uint4 e0 = lds128(st + 2 * kPlaneBlock + p0), e1 = lds128(st + 2 * kPlaneBlock + p1);
+                const uint2 mw = make_uint2(lds32(st + kMetaAt + 4u * uint32_t(r)),
+                                            lds32(st + kMetaAt + 4u * uint32_t(r) + 4u));
+                // the column's first escape entry (if any) is read while the
+                // rebuild runs
+                const EscPending ep = esc_begin(valid, mw.x, mw.y, g.esc, g.n_esc, b.err);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty_w[s]);  // planes and meta read
+                uint32_t w[32];
+                uint32_t(&wlo)[16] = *reinterpret_cast<uint32_t(*)[16]>(&w[0]);
+                uint32_t(&whi)[16] = *reinterpret_cast<uint32_t(*)[16]>(&w[16]);
+                const uint32_t b4 = base4(mw.x);
+                rebuild32(h0, l0, e0, b4, wlo);
+                rebuild32(h1, l1, e1, b4, whi);
+                esc_apply(ep, wlo, uint32_t(64 * h), g.esc);
+                esc_apply(ep, whi, uint32_t(64 * h + 32), g.esc);
+                // the unit's tokens have landed, and with them the UMMAs that
+                // read this slot's A buffer last have completed
+                mbar_wait(&full_x[2 * sx + grp], group_parity<SX>(i), &s_ctl, b.err);
+                tc_fence_after();
+                tmem_st32(tmem + lane_off + C::kA + 64u * uint32_t(sx) + 32u * uint32_t(h), w);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&a_full[2 * sx + grp]);
             }
-        } else {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty_w[j][wq.s]);
         }
-        wq.template next<SWG>();
-        // the UMMAs that read this A buffer last have completed
-        if (uses >= NA) mbar_wait(&a_empty[j][aq.s], aq.ph ^ 1u, &s_ctl, b.err);
+
+        // ---- epilogue: accumulator row r, tokens [h MP/4, (h + 1) MP/4):
+        // D_0 + D_1, each only if its issuer had a unit in this piece
+        mbar_wait(&acc_full, uint32_t(piece) & 1u, &s_ctl, b.err);
         tc_fence_after();
-        if (real) tmem_st32(a0col + 64u * uint32_t(aq.s), w);
+        const int cnt = ub - ua, ia = i - cnt;
+        const bool has0 = cnt >= 2 || (ia & 1) == 0, has1 = cnt >= 2 || (ia & 1) == 1;
+        constexpr int kHalf = MP / 4;
+        float v[kHalf];
+        // up to 8 tokens of each accumulator per round trip to tensor memory
+        constexpr int kQ = kHalf >= 8 ? 8 : kHalf;
+#pragma unroll
+        for (int q0 = 0; q0 < kHalf; q0 += kQ) {
+            uint32_t r0[kQ] = {}, r1[kQ] = {};
+#pragma unroll
+            for (int q = 0; q < kQ; q += 4) {
+                uint32_t(&a)[4] = *reinterpret_cast<uint32_t(*)[4]>(&r0[q]);
+                uint32_t(&bb)[4] = *reinterpret_cast<uint32_t(*)[4]>(&r1[q]);
+                if (has0) tmem_ld4(tmem + lane_off + uint32_t(qt * kHalf + q0 + q), a);
+                if (has1) tmem_ld4(tmem + lane_off + uint32_t(MP + qt * kHalf + q0 + q), bb);
+            }
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < kQ; ++e)
+                v[q0 + e] = has0 && has1 ? __uint_as_float(r0[e]) + __uint_as_float(r1[e])
+                                         : __uint_as_float(has0 ? r0[e] : r1[e]);
+        }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&a_full[j][aq.s]);
-        aq.template next<NA>();
-        ++uses;
-
-        if (!(c.kg == g.KG - 1 || u + 2 >= u1)) continue;
-
-        // ---- epilogue of the piece: accumulator D_j, row r, tokens
-        // [h MP / 2, (h + 1) MP / 2), read 8 at a time.  The decoders start
-        // the next piece only after it, so the accumulator is released at
-        // its end.
-        mbar_wait(&acc_full[j], uint32_t(pieces) & 1u, &s_ctl, b.err);
-        ++pieces;
-        tc_fence_after();
-        if (real) {
-            constexpr int kHalf = MP / 2;
-            const int pf = pair_first(b, c);
-            const int cnt = (u - ua) / 2 + 1;
-            const int n = nb * kTileN + r;
-            const bool valid = n < g.N;
-            const bool whole = cnt == g.KG;
-            // the pair holds the CTA's first unit: slots 0 + j, else 2 + j
-            const int slot = (pf <= u0 ? 0 : 2) + j;
-            float *P = b.partial + (size_t(blockIdx.x) * 4 + slot) * size_t(M) * kTileN;
-#pragma unroll 1
-            for (int q = 0; q < kHalf / 8; ++q) {
-                uint32_t t8[8];
-                tmem_ld8(tmem + lane_off + uint32_t(j * MP + h * kHalf + 8 * q), t8);
-                tmem_ld_wait();
-                const int m0 = h * kHalf + 8 * q;
-                if (m0 >= M) break;
+        if (lane == 0) mbar_arrive(&acc_empty);
+        if (ua == first && ub == first + g.KG) {
+            if (valid && (!FUSED || g.y)) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float v = __uint_as_float(t8[e]);
-                    const int m = m0 + e;
-                    if (!whole) {
-                        if (m < M) P[m * kTileN + r] = v;
-                        continue;
-                    }
-                    if (valid && m < M && (!FUSED || g.y)) store_out(g.y, b.y_dtype, g.N, m, n, v);
-                    if (FUSED) {
-                        // per token: the warp's 32 rows -> one key, then the CTA maximum
-                        unsigned long long best = valid ? pack_key(v, uint32_t(n)) : 0ull;
-#pragma unroll
-                        for (int off = 16; off >= 1; off >>= 1) {
-                            const unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, best, off);
-                            best = o > best ? o : best;
-                        }
-                        if (lane == 0 && m < M && best != 0ull) atomicMax(&s_best[m], best);
-                    }
+                for (int e = 0; e < kHalf; ++e) {
+                    const int m = qt * kHalf + e;
+                    if (m < M) store_out(g.y, b.y_dtype, g.N, m, n, v[e]);
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[j]);
-            if (!whole) tc_fixup<FUSED>(b, g, pf, nb, j, cnt, &s_last[j], gtid, s_best);
+            if (FUSED) {
+                // per token: the warp's 32 rows -> one key, then the CTA maximum
+#pragma unroll
+                for (int e = 0; e < kHalf; ++e) {
+                    unsigned long long best = valid ? pack_key(v[e], uint32_t(n)) : 0ull;
+#pragma unroll
+                    for (int off = 16; off >= 1; off >>= 1) {
+                        const unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, best, off);
+                        best = o > best ? o : best;
+                    }
+                    const int m = qt * kHalf + e;
+                    if (lane == 0 && m < M && best != 0ull) atomicMax(&s_best[m], best);
+                }
+            }
         } else {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[j]);
+            const int slot = ua == u0 ? 0 : 1;
+            float *P = b.partial + (size_t(blockIdx.x) * 2 + slot) * size_t(M) * kTileN;
+#pragma unroll
+            for (int e = 0; e < kHalf; ++e) {
+                const int m = qt * kHalf + e;
+                if (m < M) P[m * kTileN + r] = v[e];
+            }
+            stream_fixup<FUSED>(b, g, first, nb, ub - ua, &s_last, threadIdx.x, kDT, s_best);
         }
-        ua = -1;
+        ++piece;
+        s_next_tile(b, c);
     }
-    tc_fence_before();
-    named_arrive_id(kBarEnd, kDT + 32);  // accumulators read: the owner may free the tensor memory
 
     if (FUSED) {
         // publish this CTA's per-token best; the last CTA to arrive folds
@@ -665,9 +464,9 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
         for (int m = tid; m < M; m += kDT) b.row_best[size_t(blockIdx.x) * M + m] = s_best[m];
         __threadfence();
         named_sync(kDT);
-        if (tid == 0) s_last[0] = (atomicAdd(b.done, 1u) == gridDim.x - 1);
+        if (tid == 0) s_last = (atomicAdd(b.done, 1u) == gridDim.x - 1);
         named_sync(kDT);
-        if (s_last[0]) {
+        if (s_last) {
             __threadfence();
             verify_from_keys(b.row_best, int64_t(gridDim.x), M, b.vR, b.vT, b.draft, b.accept_len, b.next_tok,
                              b.gbuf, tid, kDT);

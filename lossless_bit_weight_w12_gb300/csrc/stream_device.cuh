@@ -101,35 +101,53 @@ __device__ __forceinline__ void stream_fixup(const StreamBatch &b, const StreamO
         const int c_first = sk_cta_of(first, per, rem), c_last = sk_cta_of(first + g.KG - 1, per, rem);
         const int M = b.M;
         const size_t slot_floats = size_t(M) * kTileN;
-        for (int o = tid; o < M * (kTileN / 4); o += nthreads) {
-            const int m = o / (kTileN / 4), c4 = o % (kTileN / 4);
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int total = M * (kTileN / 4);
+        // four outputs per thread and round trip, summed in CTA order (the
+        // same bits on every call)
+        for (int o0 = tid; o0 < total; o0 += 4 * nthreads) {
+            float4 acc[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int c = c_first; c <= c_last; ++c) {
                 const int slot = sk_unit_begin(c, per, rem) >= first ? 0 : 1;
-                const float4 v = __ldcg(reinterpret_cast<const float4 *>(
-                    b.partial + (size_t(c) * 2 + slot) * slot_floats + size_t(m) * kTileN) + c4);
-                if (c == c_first) {
-                    acc = v;
-                } else {
-                    acc.x += v.x;
-                    acc.y += v.y;
-                    acc.z += v.z;
-                    acc.w += v.w;
-                }
-            }
-            const int n0 = nb * kTileN + 4 * c4;
-            const float r[4] = {acc.x, acc.y, acc.z, acc.w};
-            unsigned long long best = 0ull;
+                const float4 *P = reinterpret_cast<const float4 *>(b.partial + (size_t(c) * 2 + slot) * slot_floats);
+                float4 v[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                if (n0 + e >= g.N) continue;
-                if (!FUSED || g.y) store_out(g.y, b.y_dtype, g.N, m, n0 + e, r[e]);
-                if (FUSED) {
-                    const unsigned long long k = pack_key(r[e], uint32_t(n0 + e));
-                    best = k > best ? k : best;
+                for (int k = 0; k < 4; ++k) {
+                    const int o = o0 + k * nthreads;
+                    v[k] = o < total ? __ldcg(P + o) : make_float4(0.f, 0.f, 0.f, 0.f);  // [m][c4] = o
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    if (c == c_first) {
+                        acc[k] = v[k];
+                    } else {
+                        acc[k].x += v[k].x;
+                        acc[k].y += v[k].y;
+                        acc[k].z += v[k].z;
+                        acc[k].w += v[k].w;
+                    }
                 }
             }
-            if (FUSED && best != 0ull) atomicMax(&s_best[m], best);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int o = o0 + k * nthreads;
+                if (o >= total) break;
+                const int m = o / (kTileN / 4), c4 = o % (kTileN / 4);
+                const int n0 = nb * kTileN + 4 * c4;
+                const float r[4] = {acc[k].x, acc[k].y, acc[k].z, acc[k].w};
+                unsigned long long best = 0ull;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (n0 + e >= g.N) continue;
+                    if (!FUSED || g.y) store_out(g.y, b.y_dtype, g.N, m, n0 + e, r[e]);
+                    if (FUSED) {
+                        const unsigned long long key = pack_key(r[e], uint32_t(n0 + e));
+                        best = key > best ? key : best;
+                    }
+                }
+                if (FUSED && best != 0ull) atomicMax(&s_best[m], best);
+            }
         }
         if (tid == 0) g.counters[nb] = 0u;
     }

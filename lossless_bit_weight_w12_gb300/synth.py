@@ -67,10 +67,14 @@ def weights(rng: np.random.Generator, K: int, N: int, std: float = 0.02,
             p_special: float = 1e-4) -> np.ndarray:
     """[N, K] bf16 weight following the recipe in the module docstring."""
     size = K * N
-    f = rng.standard_normal(size, dtype=np.float32)
-    f *= np.float32(std)
-    w = bf16_rne(f)
-    del f
+    # The normal draws are taken in chunks (the same sequence as one draw of
+    # `size`) and rounded while they are in cache.
+    w = np.empty(size, dtype=np.uint16)
+    chunk = 1 << 20
+    for c0 in range(0, size, chunk):
+        f = rng.standard_normal(min(chunk, size - c0), dtype=np.float32)
+        f *= np.float32(std)
+        w[c0:c0 + f.size] = bf16_rne(f)
     if size:
         n_out = int(rng.binomial(size, p_outlier))
         at = rng.integers(0, size, n_out)

@@ -2,28 +2,22 @@
 
 The kernel's correctness rests on mbarrier phase parity: a wait names a
 phase only by its parity, so no waiter may fall two phases behind a
-barrier.  This model runs the kernel's six roles -- weight producer, token
-producer, two UMMA issuers, two decoder groups (a group's 8 warp arrivals
-are one arrival here) -- against barriers with the hardware's parity
-semantics (try_wait.parity(P) is true iff the current phase's parity differs
-from P), with copies landing and UMMAs completing after random delays under
-random scheduling.  Units are in the kernel's pair order: a pair of tiles
-covers 2 KG units (k-group kg of tile j is unit 2 kg + j of the pair), an odd
-tile count is padded by a phantom tile (its units copy and multiply
-nothing), and a CTA's range [u0, u1) may start and end anywhere.  For every
-combination of ring sizes the kernel builds (weight stages per group SWG,
-token slots SX, A buffers per group NA) it asserts:
+barrier.  This model runs the kernel's five roles -- weight producer, token
+producer, UMMA thread, two decoder groups (a group's 8 warp arrivals are
+one arrival here) -- against barriers with the hardware's parity semantics
+(try_wait.parity(P) is true iff the current phase's parity differs from P),
+with fills landing and UMMAs completing after random delays under random
+scheduling.  It asserts, for every pair of ring sizes the kernel builds
+(weight stages SW, token slots SX):
   - every role finishes (no deadlock);
-  - a decoder reads a landed copy of its own unit, never a stale or
-    in-flight one, and a weight stage is refilled only after its group read it;
-  - UMMAs read their step's tokens and their unit's A buffer, both unchanged
-    until they complete: the token producer never refills a slot and the
-    decoders never overwrite an A buffer under them;
-  - an accumulator is read only after its piece's UMMAs completed and is not
-    reset before its decoder group read it.
-A negative control gives the token slots' empty barrier one arrival (only
-one issuer's commit) instead of two; the model must catch the refill under
-the other issuer's UMMAs.
+  - a decoder reads a landed fill of its own unit, never a stale or
+    in-flight one;
+  - UMMAs read the unit's tokens and A buffer, unchanged until they
+    complete, and the decoders never overwrite an A buffer under them;
+  - the accumulator is read only after its piece's UMMAs completed and is
+    not reset before both decoder groups read it.
+A negative control runs the earlier scheme (one full barrier per slot and a
+group waiting on the other group's fills), which the model must catch.
 """
 import random
 
@@ -58,161 +52,151 @@ class Bar:
         return (self.phase & 1) != parity
 
 
-def run(SWG, SX, NA, u0, u1, KG, NB, seed, empty_x_count=2):
-    """One CTA over units [u0, u1) of a product with KG groups and NB real
-    tiles (pair order, phantom tile if NB is odd)."""
+def gp(i, S, per_group):
+    if not per_group:
+        return (i // S) & 1
+    k = i // S
+    return ((k >> 1) if (S & 1) else k) & 1
+
+
+def run(SW, SX, n_units, KG, u0_off, seed, per_group=True, skip_wait=False, issuers=1):
     rnd = random.Random(seed)
-    NBP = NB + (NB & 1)
-    assert 0 <= u0 < u1 <= KG * NBP
-
-    def tile(u):
-        return 2 * (u // (2 * KG)) + (u & 1)
-
-    def kg_of(u):
-        return (u % (2 * KG)) >> 1
-
-    def phantom(u):
-        return tile(u) >= NB
-
-    def first_of_piece(u):
-        return kg_of(u) == 0 or u - 2 < u0
-
-    def last_of_piece(u):
-        return kg_of(u) == KG - 1 or u + 2 >= u1
-
-    full_w = [[Bar(1) for _ in range(SWG)] for _ in range(2)]
-    empty_w = [[Bar(1) for _ in range(SWG)] for _ in range(2)]
-    full_x = [Bar(1) for _ in range(SX)]
-    empty_x = [Bar(empty_x_count) for _ in range(SX)]
-    a_full = [[Bar(1) for _ in range(NA)] for _ in range(2)]
-    a_empty = [[Bar(1) for _ in range(NA)] for _ in range(2)]
-    acc_full = [Bar(1), Bar(1)]
-    acc_empty = [Bar(1), Bar(1)]
-    wstage = [[None] * SWG for _ in range(2)]  # ('fly', u) / ('ok', u) / ('read', u)
-    xslot = [None] * SX                          # ('fly', step) / ('ok', step)
-    xbusy = [0] * SX                             # UMMAs in flight reading the slot
-    abuf = [[None] * NA for _ in range(2)]
-    abusy = [[0] * NA for _ in range(2)]
-    pending = [{}, {}]                           # per issuer: piece -> UMMAs in flight
-    events = []
+    U = n_units
+    # pieces: tiles of KG units, CTA range starts at offset u0_off inside a tile
+    piece_of = [(u0_off + i) // KG for i in range(U)]
+    last_of_piece = [i == U - 1 or piece_of[i + 1] != piece_of[i] for i in range(U)]
+    first_of_piece = [i == 0 or piece_of[i - 1] != piece_of[i] for i in range(U)]
+    nfull = 2 if per_group else 1
+    full_w = [Bar(1) for _ in range(nfull * SW)]
+    full_x = [Bar(1) for _ in range(nfull * SX)]
+    empty_w = [Bar(1) for _ in range(SW)]
+    empty_x = [Bar(1) for _ in range(SX)]
+    a_full = [Bar(1) for _ in range((2 if issuers == 2 else 1) * SX)]
+    acc_full, acc_empty = Bar(issuers), Bar(2)
+    wstage = [None] * SW  # content: ('fly', i) or ('ok', i)
+    xslot = [None] * SX
+    abuf = [None] * SX
+    abuf_busy = [0] * SX  # in-flight UMMAs reading it
+    events = []  # (time, seq, fn)
     now = [0]
     seq = [0]
-    last_done = [0, 0]
+    piece_pending = {}
+    epi_done = set()
 
-    def sched_at(t, fn):
+    def sched(delay, fn):
         seq[0] += 1
-        events.append((t, seq[0], fn))
+        events.append((now[0] + delay, seq[0], fn))
 
-    s0, s1 = u0 >> 1, (u1 - 1) >> 1
-    nsteps = s1 - s0 + 1
+    def fbar(arr, S, i):
+        return arr[(2 * (i % S) + (i & 1)) if per_group else (i % S)]
 
     def WP():
-        issued = [0, 0]
-        for u in range(u0, u1):
-            j = u & 1
-            k = issued[j]
-            s = k % SWG
-            if k >= SWG:
-                yield (empty_w[j][s], ((k // SWG) - 1) & 1)
-            assert wstage[j][s] is None or wstage[j][s][0] == 'read', ('WP overwrite', u, wstage[j][s])
-            b = full_w[j][s]
-            if phantom(u):
-                wstage[j][s] = ('ok', u)
-                b.arrive()
-            else:
-                b.expect_tx(1)
-                wstage[j][s] = ('fly', u)
+        for i in range(U):
+            s = i % SW
+            if i >= SW:
+                yield (empty_w[s], ((i // SW) - 1) & 1)
+            assert wstage[s] is None or wstage[s][0] == 'read', ('WP overwrite', i, wstage[s])
+            b = fbar(full_w, SW, i)
+            b.expect_tx(1)
+            wstage[s] = ('fly', i)
 
-                def land(j=j, s=s, u=u, b=b):
-                    wstage[j][s] = ('ok', u)
-                    b.complete_tx(1)
-                sched_at(now[0] + rnd.randint(1, 40), land)
-            issued[j] += 1
+            def land(s=s, i=i, b=b):
+                wstage[s] = ('ok', i)
+                b.complete_tx(1)
+            sched(rnd.randint(1, 40), land)
 
     def XP():
-        for t in range(nsteps):
-            s = t % SX
-            if t >= SX:
-                yield (empty_x[s], ((t // SX) - 1) & 1)
-            assert xbusy[s] == 0, ('token slot refilled under a UMMA', t)
-            full_x[s].expect_tx(1)
-            xslot[s] = ('fly', s0 + t)
+        for i in range(U):
+            s = i % SX
+            if i >= SX:
+                yield (empty_x[s], ((i // SX) - 1) & 1)
+            assert abuf_busy[s] == 0
+            b = fbar(full_x, SX, i)
+            b.expect_tx(1)
+            xslot[s] = ('fly', i)
 
-            def land(s=s, st=s0 + t):
-                xslot[s] = ('ok', st)
-                full_x[s].complete_tx(1)
-            sched_at(now[0] + rnd.randint(1, 25), land)
+            def land(s=s, i=i, b=b):
+                xslot[s] = ('ok', i)
+                b.complete_tx(1)
+            sched(rnd.randint(1, 25), land)
 
-    def commit(j, fn):
-        # a commit arrives once every UMMA this issuer issued before it completed
-        sched_at(max(now[0], last_done[j]) + 1, fn)
+    def abar(i):
+        return a_full[2 * (i % SX) + (i & 1)] if issuers == 2 else a_full[i % SX]
 
-    def MMA(j):
-        pieces = 0
-        uses = 0
-        for t in range(nsteps):
-            st = s0 + t
-            u = 2 * st + j
-            xs = t % SX
-            yield (full_x[xs], (t // SX) & 1)
-            if u0 <= u < u1:
-                if first_of_piece(u) and pieces > 0:
-                    yield (acc_empty[j], (pieces - 1) & 1)
-                a = uses % NA
-                yield (a_full[j][a], (uses // NA) & 1)
-                assert xslot[xs] == ('ok', st), ('MMA tokens', u, xslot[xs])
-                assert abuf[j][a] == u, ('MMA A', u, abuf[j][a])
-                if not phantom(u):
-                    xbusy[xs] += 1
-                    abusy[j][a] += 1
-                    pending[j][pieces] = pending[j].get(pieces, 0) + 1
+    def apar(i):
+        return gp(i, SX, True) if issuers == 2 else (i // SX) & 1
 
-                    def done(xs=xs, a=a, st=st, u=u, p=pieces):
-                        assert xslot[xs] == ('ok', st) and abuf[j][a] == u, ('UMMA operands changed', u)
-                        xbusy[xs] -= 1
-                        abusy[j][a] -= 1
-                        pending[j][p] -= 1
-                    t_done = max(now[0] + rnd.randint(1, 30), last_done[j] + 1)
-                    last_done[j] = t_done
-                    sched_at(t_done, done)
-                commit(j, lambda j=j, a=a: a_empty[j][a].arrive())
-                uses += 1
-                if last_of_piece(u):
-                    commit(j, lambda j=j: acc_full[j].arrive())
-                    pieces += 1
-            commit(j, lambda xs=xs: empty_x[xs].arrive())
+    last_done = [0, 0]  # per issuer: its UMMAs complete in issue order
 
-    def DEC(j):
-        ws = 0
-        wph = 0
-        uses = 0
-        pieces = 0
-        u = u0 if (u0 & 1) == j else u0 + 1
-        while u < u1:
-            yield (full_w[j][ws], wph)
-            assert wstage[j][ws] == ('ok', u), ('DEC read', j, u, wstage[j][ws])
-            wstage[j][ws] = ('read', u)
-            empty_w[j][ws].arrive()
-            ws += 1
-            if ws == SWG:
-                ws, wph = 0, wph ^ 1
-            yield ('delay', rnd.randint(1, 30))
-            a = uses % NA
-            if uses >= NA:
-                yield (a_empty[j][a], ((uses // NA) - 1) & 1)
-            assert abusy[j][a] == 0, ('A overwrite under UMMA', u)
-            abuf[j][a] = u
-            a_full[j][a].arrive()
-            uses += 1
-            if last_of_piece(u):
-                yield (acc_full[j], pieces & 1)
-                assert pending[j].get(pieces, 0) == 0, ('accumulator read early', j, pieces)
-                yield ('delay', rnd.randint(1, 20))
-                acc_empty[j].arrive()
-                pieces += 1
-            u += 2
+    def MMA(t):
+        """UMMA issuer t: every unit (issuers == 1) or the units of parity t."""
+        piece = -1
+        for i in range(U):
+            if first_of_piece[i]:
+                piece += 1
+                if piece > 0:
+                    yield (acc_empty, (piece - 1) & 1)
+                assert (piece - 1) in epi_done or piece == 0
+            mine = issuers == 1 or (i & 1) == t
+            if mine:
+                sx = i % SX
+                yield (abar(i), apar(i))
+                assert xslot[sx] == ('ok', i), ('MMA x', i, xslot[sx])
+                assert abuf[sx] == i, ('MMA A', i, abuf[sx])
+                abuf_busy[sx] += 1
+                piece_pending[piece] = piece_pending.get(piece, 0) + 1
 
-    actors = {'WP': WP(), 'XP': XP(), 'D0': DEC(0), 'D1': DEC(1), 'M0': MMA(0), 'M1': MMA(1)}
+                def done(sx=sx, i=i, p=piece):
+                    assert xslot[sx] == ('ok', i) and abuf[sx] == i, ('UMMA operands changed', i)
+                    abuf_busy[sx] -= 1
+                    piece_pending[p] -= 1
+                    empty_x[sx].arrive()
+                # one issuer's UMMAs complete in issue order; the two
+                # issuers' interleave in any order
+                t_done = max(now[0] + rnd.randint(1, 30), last_done[t] + 1)
+                last_done[t] = t_done
+                seq[0] += 1
+                events.append((t_done, seq[0], done))
+            if last_of_piece[i]:
+                # the commit arrives once this issuer's UMMAs so far completed
+                t_done = max(now[0], last_done[t]) + 1
+                seq[0] += 1
+                events.append((t_done, seq[0], lambda: acc_full.arrive()))
+
+    def DEC(grp):
+        piece = 0
+        for i in range(U):
+            if (i & 1) == grp:
+                s, sx = i % SW, i % SX
+                yield (fbar(full_w, SW, i), gp(i, SW, per_group))
+                assert wstage[s] == ('ok', i), ('DEC read', grp, i, wstage[s])
+                wstage[s] = ('read', i)
+                empty_w[s].arrive()
+                yield ('delay', rnd.randint(1, 30))
+                yield (fbar(full_x, SX, i), gp(i, SX, per_group))
+                assert abuf_busy[sx] == 0, ('A overwrite under UMMA', i)
+                assert xslot[sx] == ('ok', i), ('DEC x', i, xslot[sx])
+                abuf[sx] = i
+                abar(i).arrive()
+            elif skip_wait:
+                s, sx = i % SW, i % SX
+                if SW & 1:
+                    yield (full_w[s], (i // SW) & 1)
+                if SX & 1:
+                    yield (full_x[sx], (i // SX) & 1)
+            if last_of_piece[i]:
+                yield (acc_full, piece & 1)
+                assert piece_pending.get(piece, 0) == 0, ('acc read early', piece)
+                DEC.reads[piece] = DEC.reads.get(piece, 0) + 1
+                if DEC.reads[piece] == 2:
+                    epi_done.add(piece)
+                acc_empty.arrive()
+                piece += 1
+    DEC.reads = {}
+
+    actors = {'WP': WP(), 'XP': XP(), 'D0': DEC(0), 'D1': DEC(1)}
+    for t in range(issuers):
+        actors[f'MMA{t}'] = MMA(t)
     waiting = {k: None for k in actors}
     sleeping = {}
     done = set()
@@ -222,7 +206,7 @@ def run(SWG, SX, NA, u0, u1, KG, NB, seed, empty_x_count=2):
         if steps > 2_000_000:
             raise RuntimeError('livelock')
         runnable = []
-        for k in actors:
+        for k, g in actors.items():
             if k in done or k in sleeping:
                 continue
             w = waiting[k]
@@ -240,7 +224,9 @@ def run(SWG, SX, NA, u0, u1, KG, NB, seed, empty_x_count=2):
             except StopIteration:
                 done.add(k)
             continue
-        cand = [e[0] for e in events] + list(sleeping.values())
+        # advance time
+        wake = [t for t in sleeping.values()]
+        cand = [e[0] for e in events] + wake
         if not cand:
             blocked = {k: (waiting[k][1], waiting[k][0].phase) for k in actors if k not in done}
             raise RuntimeError(f'deadlock: {blocked}')
@@ -255,45 +241,39 @@ def run(SWG, SX, NA, u0, u1, KG, NB, seed, empty_x_count=2):
     return True
 
 
-# ring sizes of tc_kernel<MP> (SWG, SX, NA) for MP = 16, 32, 64, 128, and
-# smaller or odd neighbours
-CONFIGS = [(4, 4, 3), (4, 3, 3), (3, 4, 3), (3, 2, 2), (2, 2, 2), (2, 3, 2), (3, 1, 2), (2, 5, 4)]
+# ring sizes of tc_kernel<MP>: (SW, SX) for MP = 16, 32, 64, 128, and
+# neighbours (odd and even rings, tiny rings)
+CONFIGS = [(8, 4), (7, 4), (6, 4), (5, 3), (3, 3), (4, 2), (2, 2), (5, 4), (7, 3)]
 
 
 def _cases(seeds):
-    for SWG, SX, NA in CONFIGS:
+    for SW, SX in CONFIGS:
         for seed in range(seeds):
-            rnd = random.Random(1000 * SWG + 100 * SX + 10 * NA + seed)
-            KG = rnd.choice([1, 2, 3, 5, 8, 40])
-            NB = rnd.choice([1, 2, 3, 4, 5, 7])
-            U = KG * (NB + (NB & 1))
-            # ranges long enough to turn every ring over several times, and
-            # a few short ones
-            n = min(U, rnd.randint(1, 8)) if rnd.random() < 0.2 else rnd.randint(min(U, 16), min(U, 120))
-            u0 = rnd.randint(0, U - n)
-            u1 = u0 + n
-            yield SWG, SX, NA, u0, u1, KG, NB, seed
+            rnd = random.Random(seed)
+            n = rnd.randint(1, 60)
+            KG = rnd.choice([1, 2, 3, 5, 40])
+            yield SW, SX, n, KG, rnd.randint(0, KG - 1), seed
 
 
-def test_ring_protocol_pair_order():
-    for case in _cases(40):
-        assert run(*case), case
+def test_ring_protocol_per_group_barriers():
+    for SW, SX, n, KG, off, seed in _cases(40):
+        assert run(SW, SX, n, KG, off, seed, per_group=True, skip_wait=False), (SW, SX, seed)
 
 
-def test_ring_protocol_whole_product_from_unit_zero():
-    """A CTA that holds a whole product (every pair, both tiles)."""
-    for SWG, SX, NA in CONFIGS:
-        for NB in (1, 2, 3, 6):
-            for seed in range(4):
-                KG = 3
-                assert run(SWG, SX, NA, 0, KG * (NB + (NB & 1)), KG, NB, seed)
+def test_ring_protocol_two_issuers():
+    """Two UMMA issuers (even and odd units, one accumulator each), a_full
+    per decoder group and slot, acc_full with two arrivals."""
+    for SW, SX, n, KG, off, seed in _cases(40):
+        assert run(SW, SX, n, KG, off, seed, per_group=True, skip_wait=False, issuers=2), (SW, SX, seed)
 
 
-def test_model_catches_a_single_commit_token_slot():
+def test_model_catches_the_skip_wait_deadlock():
     failures = 0
-    for case in _cases(12):
+    for SW, SX, n, KG, off, seed in _cases(10):
+        if (SW & 1) == 0 and (SX & 1) == 0:
+            continue
         try:
-            run(*case, empty_x_count=1)
+            run(SW, SX, n, KG, off, seed, per_group=False, skip_wait=True)
         except (AssertionError, RuntimeError):
             failures += 1
     assert failures > 0
