@@ -551,7 +551,7 @@ def run_w12(args):
     # ---- steady state: the same step 10 000 times (25 replays of a graph of
     # 400 steps, each replay between two events) with the SM clock sampled
     # throughout, beyond the short timed region above
-    long_steps, long_reps = 400, 25
+    long_steps, long_reps = 400, max(1, args.steady_steps // 400)
     glong = GraphSteps(torch, lambda mark: batch(), long_steps)
     glong.run(barrier)
     clk_long = ClockSampler(torch.cuda.current_device(), interval_ms=100)
@@ -986,6 +986,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-verify", dest="verify", action="store_false")
     ap.add_argument("--no-stack", dest="stack", action="store_false",
                     help="skip the measured 64-layer stack (config 4)")
+    ap.add_argument("--steady-steps", type=int, default=10000,
+                    help="steps of the steady-state measurement (graphs of 400 steps)")
     ap.add_argument("--kernel-only", default=None, help="time one layer GEMM by name, or \"layer\" for the batched layer (for ncu)")
     ap.add_argument("--m", type=int, default=1, help="tokens for --kernel-only")
     ap.add_argument("--path", type=int, default=0,
