@@ -295,6 +295,34 @@ def test_gemm_batched_full_layer(dev, w12mod, oracle):
                 check_gemm(ys[i][:, ns], yo, so, what=f"batched {name} M={M} path={path} (oracle)")
 
 
+@pytest.mark.parametrize("M", [1, 4, 16, 33, 64, 128])
+def test_gemm_early_weights_option(dev, w12mod, oracle, M):
+    """W12_OPT_EARLY_WEIGHTS (the weight stream starts under the previous
+    kernel's tail; the launch configuration the bench times) gives the same
+    bits as the default launch on every path, single and batched, on blobs
+    uploaded before the calls."""
+    import torch
+    shapes = [(1024, 130), (2048, 257), (384, 33)]
+    rng = synth.streams(4200 + M, 2 * len(shapes))
+    items, refs = [], []
+    for i, (K, N) in enumerate(shapes):
+        w = synth.weights(rng[2 * i], K, N)
+        x = synth.activations(rng[2 * i + 1], M, K)
+        d, blob = w12mod.encode(w, w12mod.LAYOUT_NK)
+        items.append((d, w12mod.upload(blob, dev), x))
+        refs.append(oracle.gemm(*oracle.encode(w, oracle.LAYOUT_NK), x))
+    torch.cuda.synchronize()
+    for path in [0] + _paths(M):
+        ys_default = _batched(w12mod, dev, items, M, path=path)
+        ys_early = _batched(w12mod, dev, items, M, path=path | w12mod.OPT_EARLY_WEIGHTS)
+        for (K, N), a, e, (y_ref, s_ref) in zip(shapes, ys_default, ys_early, refs):
+            assert np.array_equal(a, e), f"early weights changed the result K={K} N={N} M={M} path={path}"
+            check_gemm(e, y_ref, s_ref, what=f"early weights K={K} N={N} M={M} path={path}")
+        for (d, b, x), (y_ref, s_ref) in zip(items, refs):
+            y = _run(w12mod, dev, d, b, x, path | w12mod.OPT_EARLY_WEIGHTS)
+            check_gemm(y, y_ref, s_ref, what=f"early weights single M={M} path={path}")
+
+
 def test_gemm_batched_argument_errors(dev, w12mod):
     import torch
     w = np.full((16, 256), 0x3F80, dtype=np.uint16)
