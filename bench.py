@@ -795,27 +795,34 @@ def run_w12(args):
 
 
 def bench_lmhead(w12, torch, dev, args, barrier):
-    """Fused lm_head (5120 -> 151936) + greedy verify, R = 1, T = 16."""
+    """Fused lm_head (5120 -> 151936) + greedy verify, T = 16 and R = 1, 2, 4,
+    8 draft blocks (R*T = 16 .. 128 rows: the batched verify)."""
     K, N = synth.LM_HEAD_SHAPE[1], synth.LM_HEAD_SHAPE[2]
-    R, T = 1, 16
+    T = 16
     rng = synth.streams(4, 3)
     w = synth.weights(rng[0], K, N)
     d, blob = w12.encode(w, w12.LAYOUT_NK)
     blob_d = w12.upload(blob, dev)
-    hidden = torch.from_numpy(synth.activations(rng[1], R * T, K).view(np.int16)).to(dev)
-    draft = torch.from_numpy(rng[2].integers(0, N, (R, T - 1)).astype(np.int32)).to(dev)
-    acc = torch.empty(R, dtype=torch.int32, device=dev)
-    nxt = torch.empty(R, dtype=torch.int32, device=dev)
-    ws = w12.workspace(w12.verify_lmhead_workspace_size(d, R, T), dev)
-
-    def step(mark=None):
-        w12.verify_greedy_lmhead(hidden, d, blob_d, R, T, draft, acc, nxt, ws)
-    n = max(5, args.steps)
-    gl = GraphSteps(torch, step, n)
-    gl.run(barrier)
-    t = gl.run(barrier)
     b = synth.weight_bytes_w12(K, N)
-    return {"us": 1e6 * t / n, "gbs": b * n / t / 1e9, "R": R, "T": T, "N": N, "K": K}
+    out = {}
+    for R in (1, 2, 4, 8):
+        hidden = torch.from_numpy(synth.activations(rng[1], R * T, K).view(np.int16)).to(dev)
+        draft = torch.from_numpy(rng[2].integers(0, N, (R, T - 1)).astype(np.int32)).to(dev)
+        acc = torch.empty(R, dtype=torch.int32, device=dev)
+        nxt = torch.empty(R, dtype=torch.int32, device=dev)
+        ws = w12.workspace(w12.verify_lmhead_workspace_size(d, R, T), dev)
+
+        def step(mark=None):
+            w12.verify_greedy_lmhead(hidden, d, blob_d, R, T, draft, acc, nxt, ws)
+        n = max(5, args.steps)
+        gl = GraphSteps(torch, step, n)
+        gl.run(barrier)
+        t = gl.run(barrier)
+        assert w12.get_device_error(ws) == 0
+        out[str(R * T)] = {"us": 1e6 * t / n, "gbs": b * n / t / 1e9, "R": R, "T": T}
+    res = dict(out["16"])
+    res.update({"N": N, "K": K, "by_rows": out})
+    return res
 
 
 def _stack_weight(task):
