@@ -120,12 +120,12 @@ int plan_batch(const w12_desc *d, int count, int64_t M, int path, BatchPlan *bp)
         if (!gemv_fits_32bit(&d[i])) return W12_ERR_SHAPE;
     }
     // Measured on the 27B-class layer (GB300, us per layer, GEMV / mma.sync
-    // / tcgen05, early weight stream): M = 1: 79.9 / 79.3 / 86.8,
-    // 4: 120.1 / 79.9 / 86.8, 16: - / 84.9 / 87.9, 32: - / 94.2 / 90.3,
-    // 64: - / 156 / 98.5, 128: - / 229 / 111.4.  At M = 1 the weight stream
+    // / tcgen05, early weight stream): M = 1: 79.6 / 79.2 / 83.4,
+    // 4: 121.9 / 79.8 / 83.6, 16: - / 85.0 / 84.8, 32: - / 94.3 / 87.3,
+    // 64: - / 151 / 93.5, 128: - / 231 / 107.1.  At M = 1 the weight stream
     // is the whole cost and the warp-shuffle GEMV does it on the CUDA cores
-    // (within 1 % of mma.sync); mma.sync serves the small blocks and tcgen05
-    // takes over above 16 tokens.
+    // (within 1 % of mma.sync); mma.sync serves the small blocks (level with
+    // tcgen05 at 16) and tcgen05 takes over above 16 tokens.
     if (path == W12_PATH_AUTO) path = M == 1 ? W12_PATH_GEMV : M <= 16 ? W12_PATH_MMA : W12_PATH_TC;
     if (path == W12_PATH_GEMV && M > 4) return W12_ERR_SHAPE;
     if (path != W12_PATH_GEMV && path != W12_PATH_MMA && path != W12_PATH_TC) return W12_ERR_ARG;

@@ -298,27 +298,28 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
                 if (piece > 0) mbar_wait(&acc_empty, uint32_t(piece - 1) & 1u, &s_ctl, b.err);
                 tc_fence_after();
                 bool fresh = true;  // this issuer's next UMMA starts its sum of the piece
-                for (; u < ub; ++u, ++i) {
-                    if ((i & 1) == t) {
-                        const int sx = i % SX;
-                        // The decoders that signal a_full waited for this
-                        // slot's full barrier first (tokens landed), so the
-                        // UMMAs may read it once a_full is observed.
-                        mbar_wait(&a_full[2 * sx + t], group_parity<SX>(i), &s_ctl, b.err);
-                        tc_fence_after();
-                        const uint64_t d0 = desc_sw128(xbase + uint32_t(sx) * uint32_t(C::kX));
-                        const uint32_t ta = tmem + C::kA + 64u * uint32_t(sx);
+                const int iend = i + (ub - u);
+                for (int iu = i + ((i & 1) != t); iu < iend; iu += 2) {  // this issuer's units
+                    const int sx = iu % SX;
+                    // The decoders that signal a_full waited for this
+                    // slot's full barrier first (tokens landed), so the
+                    // UMMAs may read it once a_full is observed.
+                    mbar_wait(&a_full[2 * sx + t], group_parity<SX>(iu), &s_ctl, b.err);
+                    tc_fence_after();
+                    const uint64_t d0 = desc_sw128(xbase + uint32_t(sx) * uint32_t(C::kX));
+                    const uint32_t ta = tmem + C::kA + 64u * uint32_t(sx);
 #pragma unroll
-                        for (int ks = 0; ks < 8; ++ks) {
-                            // x box ks / 4 (k half), 16 k = 32 bytes per step inside the swizzle atom
-                            const uint64_t dx = d0 + uint64_t(((ks >> 2) * MP * 128 + 32 * (ks & 3)) >> 4);
-                            umma_ts(dt, ta + 8u * uint32_t(ks), dx, idesc, (fresh && ks == 0) ? 0u : 1u);
-                        }
-                        fresh = false;
-                        umma_commit(&empty_x[sx]);  // frees the token slot and its A buffer
+                    for (int ks = 0; ks < 8; ++ks) {
+                        // x box ks / 4 (k half), 16 k = 32 bytes per step inside the swizzle atom
+                        const uint64_t dx = d0 + uint64_t(((ks >> 2) * MP * 128 + 32 * (ks & 3)) >> 4);
+                        umma_ts(dt, ta + 8u * uint32_t(ks), dx, idesc, (fresh && ks == 0) ? 0u : 1u);
                     }
-                    if (u == ub - 1) umma_commit(&acc_full);
+                    fresh = false;
+                    umma_commit(&empty_x[sx]);  // frees the token slot and its A buffer
                 }
+                umma_commit(&acc_full);
+                u = ub;
+                i = iend;
                 ++piece;
                 s_next_tile(b, c);
             }
@@ -357,39 +358,40 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
         const int ua = u, ub = min(u1, first + g.KG);
         const int n = nb * kTileN + r;
         const bool valid = n < g.N;
-        for (; u < ub; ++u, ++i) {
-            if ((i & 1) == grp) {
-                const int s = i % SW, sx = i % SX;
-                mbar_wait(&full_w[2 * s + grp], group_parity<SW>(i), &s_ctl, b.err);
-                const uint32_t st = wbase + uint32_t(s) * uint32_t(C::kW);
-                const uint4 h0 = lds128(st + p0), h1 = lds128(st + p1);
-                const uint4 l0 = lds128(st + kPlaneBlock + p0), l1 = lds128(st + kPlaneBlock + p1);
-                const uint4 e0 = lds128(st + 2 * kPlaneBlock + p0), e1 = lds128(st + 2 * kPlaneBlock + p1);
-                const uint2 mw = make_uint2(lds32(st + kMetaAt + 4u * uint32_t(r)),
-                                            lds32(st + kMetaAt + 4u * uint32_t(r) + 4u));
-                // the column's first escape entry (if any) is read while the
-                // rebuild runs
-                const EscPending ep = esc_begin(valid, mw.x, mw.y, g.esc, g.n_esc, b.err);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty_w[s]);  // planes and meta read
-                uint32_t w[32];
-                uint32_t(&wlo)[16] = *reinterpret_cast<uint32_t(*)[16]>(&w[0]);
-                uint32_t(&whi)[16] = *reinterpret_cast<uint32_t(*)[16]>(&w[16]);
-                const uint32_t b4 = base4(mw.x);
-                rebuild32(h0, l0, e0, b4, wlo);
-                rebuild32(h1, l1, e1, b4, whi);
-                esc_apply(ep, wlo, uint32_t(64 * h), g.esc);
-                esc_apply(ep, whi, uint32_t(64 * h + 32), g.esc);
-                // the unit's tokens have landed, and with them the UMMAs that
-                // read this slot's A buffer last have completed
-                mbar_wait(&full_x[2 * sx + grp], group_parity<SX>(i), &s_ctl, b.err);
-                tc_fence_after();
-                tmem_st32(tmem + lane_off + C::kA + 64u * uint32_t(sx) + 32u * uint32_t(h), w);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&a_full[2 * sx + grp]);
-            }
+        const int iend = i + (ub - u);
+        for (int iu = i + ((i & 1) != grp); iu < iend; iu += 2) {  // this group's units of the piece
+            const int s = iu % SW, sx = iu % SX;
+            mbar_wait(&full_w[2 * s + grp], group_parity<SW>(iu), &s_ctl, b.err);
+            const uint32_t st = wbase + uint32_t(s) * uint32_t(C::kW);
+            const uint4 h0 = lds128(st + p0), h1 = lds128(st + p1);
+            const uint4 l0 = lds128(st + kPlaneBlock + p0), l1 = lds128(st + kPlaneBlock + p1);
+            const uint4 e0 = lds128(st + 2 * kPlaneBlock + p0), e1 = lds128(st + 2 * kPlaneBlock + p1);
+            const uint2 mw = make_uint2(lds32(st + kMetaAt + 4u * uint32_t(r)),
+                                        lds32(st + kMetaAt + 4u * uint32_t(r) + 4u));
+            // the column's first escape entry (if any) is read while the
+            // rebuild runs
+            const EscPending ep = esc_begin(valid, mw.x, mw.y, g.esc, g.n_esc, b.err);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty_w[s]);  // planes and meta read
+            uint32_t w[32];
+            uint32_t(&wlo)[16] = *reinterpret_cast<uint32_t(*)[16]>(&w[0]);
+            uint32_t(&whi)[16] = *reinterpret_cast<uint32_t(*)[16]>(&w[16]);
+            const uint32_t b4 = base4(mw.x);
+            rebuild32(h0, l0, e0, b4, wlo);
+            rebuild32(h1, l1, e1, b4, whi);
+            esc_apply(ep, wlo, uint32_t(64 * h), g.esc);
+            esc_apply(ep, whi, uint32_t(64 * h + 32), g.esc);
+            // the unit's tokens have landed, and with them the UMMAs that
+            // read this slot's A buffer last have completed
+            mbar_wait(&full_x[2 * sx + grp], group_parity<SX>(iu), &s_ctl, b.err);
+            tc_fence_after();
+            tmem_st32(tmem + lane_off + C::kA + 64u * uint32_t(sx) + 32u * uint32_t(h), w);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&a_full[2 * sx + grp]);
         }
+        u = ub;
+        i = iend;
 
         // ---- epilogue: accumulator row r, tokens [h MP/4, (h + 1) MP/4):
         // D_0 + D_1, each only if its issuer had a unit in this piece
