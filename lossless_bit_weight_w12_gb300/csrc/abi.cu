@@ -97,8 +97,7 @@ struct BatchPlan {
     int64_t U = 0;
     size_t counters[kMaxBatch] = {}, partial[kMaxBatch] = {};
     int64_t steps[kMaxBatch] = {}, NB[kMaxBatch] = {}, ubase[kMaxBatch] = {};
-    size_t stream_partial = 0;  // [grid][slots][M][128] floats
-    int slots = 2;              // partial slots per CTA (a CTA's first and last tile pieces)
+    size_t stream_partial = 0;  // [grid][2][M][128] floats: a CTA's first and last tile pieces
     size_t total = 0;
 };
 
@@ -152,7 +151,6 @@ int plan_batch(const w12_desc *d, int count, int64_t M, int path, BatchPlan *bp)
         cpt = kMmaCols;
         uk = kGroup;
     }
-    bp->slots = 2;
     size_t off = kWsHeader;
     for (int i = 0; i < count; ++i) {
         bp->steps[i] = ceil_div(d[i].K, uk);
@@ -165,7 +163,7 @@ int plan_batch(const w12_desc *d, int count, int64_t M, int path, BatchPlan *bp)
     if (bp->U >= (int64_t(1) << 31)) return W12_ERR_SHAPE;
     bp->grid = int(std::min<int64_t>(int64_t(dv.sms) * occ, std::max<int64_t>(bp->U, 1)));
     bp->stream_partial = off;
-    off += round256(uint64_t(bp->grid) * uint64_t(bp->slots) * uint64_t(M) * uint64_t(cpt) * 4u);
+    off += round256(uint64_t(bp->grid) * 2u * uint64_t(M) * uint64_t(cpt) * 4u);
     bp->total = off;
     return W12_OK;
 }
@@ -262,7 +260,7 @@ int plan_fused(const w12_desc *d, int64_t M, FusedPlan *fp) {
     if (cached_occupancy(dv, key, 0, &occ) != W12_OK || occ < 1) return W12_ERR_CUDA;
     bp.grid = int(std::min<int64_t>(int64_t(dv.sms) * occ, bp.U));
     size_t off = bp.stream_partial;
-    off += round256(uint64_t(bp.grid) * uint64_t(bp.slots) * uint64_t(M) * uint64_t(kMmaCols) * 4u);
+    off += round256(uint64_t(bp.grid) * 2u * uint64_t(M) * uint64_t(kMmaCols) * 4u);
     fp->off_best = off;
     off += round256(uint64_t(bp.grid) * uint64_t(M) * 8u);
     fp->off_done = off;
