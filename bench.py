@@ -929,14 +929,19 @@ def bench_stack(w12, torch, dev, args, barrier):
     w12.verify_greedy_lmhead(hidden_d, d_lm, b_lm, R, T, draft_d, acc, nxt, ws_lm, logits_out_dev=logits)
     torch.cuda.synchronize()
     oracle.lib()
-    want = oracle.verify_greedy(logits.cpu().numpy(), R, T, draft)
+    lg = logits.cpu().numpy()
+    want = oracle.verify_greedy(lg, R, T, draft)
     assert acc_step == want[0].tolist() and nxt_step == want[1].tolist(), (acc_step, nxt_step, want)
+    # positions whose argmax on the kernel's fp32 logits differs from the
+    # float64 logits' (expected 0 outside near-ties)
+    flips = int((oracle.argmax(lg) != g64.reshape(-1)).sum())
     planted = int(np.argmax(draft[0] != g64[0, :T - 1])) if (draft[0] != g64[0, :T - 1]).any() else T - 1
     wbytes = 64 * _layer_bytes() + synth.weight_bytes_w12(K_lm, N_lm)
     res = {"us_per_step": 1e6 * t, "tokens_per_s": R * T / t, "gbs": wbytes / t / 1e9,
            "frac_of_peak": wbytes / t / 1e9 / _peaks()[0], "w12_weight_gb": wbytes / 1e9,
            "launches_per_step": 65, "build_s": t_build,
            "accept_len": acc_step, "next_token": nxt_step, "draft_prefix_of_fp64_argmax": planted,
+           "argmax_flips_vs_fp64": flips,
            "verify_matches_oracle_on_kernel_logits": True,
            "data": "seed-4 synth recipe (config 4 as stated): weights drawn in spawned host processes, "
                    "encoded on the device; drafts from the float64 lm_head argmax, geometric(0.7) prefix",
