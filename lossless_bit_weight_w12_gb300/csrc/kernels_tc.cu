@@ -36,8 +36,9 @@
 //    that only after they saw the unit's tokens land), and commits them to
 //    the token slot's empty barrier and, after a piece's last unit, to the
 //    accumulators' barrier.  The epilogue adds D_0 and D_1.
-// Tensor memory: the accumulators at columns 0 and MP, then one A buffer of
-// 64 columns per token slot; 512 columns allocated.  The slot's commit
+// Shared memory: the token ring (1024-byte aligned), the weight ring, then
+// the barriers.  Tensor memory: the accumulators at columns 0 and MP, then
+// one A buffer of 64 columns per token slot; 512 columns allocated.  The slot's commit
 // releases both; decoders that see the slot full again know that the UMMAs
 // which read its A buffer last have completed (the producer refilled the
 // slot only after that commit).  A K = 16 UMMA of M = 128 takes 45 cycles
@@ -70,15 +71,27 @@ constexpr int kMmaWarp1 = kDW + 3;       // UMMA issuer of the odd units
 constexpr int kTT = (kDW + 4) * 32;      // 640 threads
 constexpr uint32_t kTmemCols = 512;
 
-template <int MP>
+template <int MP, bool FUSED = false>
 struct TCfg {
     static constexpr int kX = MP * 256;                        // token slot: two boxes of MP rows x 128 bytes
-    static constexpr int SX = MP >= 128 ? 3 : 4;               // token slots (and A buffers)
+    // token slots (and A buffers): 4, but 3 for the fused lm_head at MP = 128
+    // (its per-token keys leave no room for a fourth 32 KB slot)
+    static constexpr int SX = MP >= 128 ? (FUSED ? 3 : 4) : 4;
     static constexpr int kXRing = SX * kX;                     // at the (1024-aligned) start of the ring
-    static constexpr int kW = (kUnitBytes + 127) / 128 * 128;  // weight stage stride
-    static constexpr int kFit = (227 * 1024 - 1024 - 2048 - kXRing) / kW;
+    static constexpr int kW = kUnitBytes;                      // weight stage stride (16-byte aligned)
+    // The barriers and scalars live after the rings, so the kernel has no
+    // static shared memory and its dynamic region starts at the CTA's
+    // shared base (1024-byte aligned: no alignment slack is reserved; the
+    // kernel checks it): (3 SW + 5 SX + 3) mbarriers, the tensor-memory
+    // address, the wait state, s_last, s_best.  kBarMax sizes them for the
+    // deepest weight ring (8 stages) to choose SW.
+    static constexpr int kBarMax = (3 * 8 + 5 * SX + 3) * 8 + 64 + (FUSED ? MP * 8 : 8);
+    static constexpr int kFit = (227 * 1024 - kBarMax - kXRing) / kW;
     static constexpr int SW = kFit > 8 ? 8 : kFit;             // weight stages, after the token ring
-    static constexpr size_t kDynSmem = size_t(kXRing) + size_t(SW) * kW + 1024;
+    static constexpr int kBarOff = kXRing + SW * kW;
+    static constexpr int kBar = (3 * SW + 5 * SX + 3) * 8 + 64 + (FUSED ? MP * 8 : 8);
+    static constexpr size_t kDynSmem = size_t(kBarOff) + size_t(kBar);
+    static_assert(kDynSmem <= 227 * 1024, "shared memory");
     // tensor-memory columns: accumulators [0, MP) and [MP, 2 MP), A buffer of
     // slot s at kA + 64 s
     static constexpr uint32_t kA = 2 * MP < 64 ? 64u : uint32_t(2 * MP);
@@ -227,16 +240,29 @@ __device__ __forceinline__ void tc_x_producer(const StreamBatch &b, uint32_t xba
 // last CTA to arrive runs the acceptance rule over every CTA's keys.
 template <int MP, bool FUSED>
 __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ StreamBatch b) {
-    using C = TCfg<MP>;
+    using C = TCfg<MP, FUSED>;
     constexpr int SW = C::SW, SX = C::SX;
-    extern __shared__ unsigned char smem_dyn[];
-    __shared__ __align__(8) uint64_t full_w[2 * SW], empty_w[SW], full_x[2 * SX], empty_x[SX], a_full[2 * SX];
-    __shared__ __align__(8) uint64_t acc_full, acc_empty, fin;
-    __shared__ uint32_t s_tmem;
-    __shared__ WaitCtl s_ctl;
-    __shared__ int s_last;
-    __shared__ unsigned long long s_best[FUSED ? MP : 1];
-    const uint32_t xbase = (smem_addr(smem_dyn) + 1023u) & ~1023u;  // token ring, then the weight ring
+    extern __shared__ __align__(1024) unsigned char smem_dyn[];
+    // the token ring needs a 1024-byte aligned start (128-byte swizzle of the
+    // boxes and the UMMA descriptors); a misaligned region is reported, not used
+    if (smem_addr(smem_dyn) & 1023u) {
+        if (threadIdx.x == 0) record_error(b.err, W12_ERR_DEVICE);
+        return;
+    }
+    unsigned char *bar_block = smem_dyn + C::kBarOff;
+    uint64_t *full_w = reinterpret_cast<uint64_t *>(bar_block);
+    uint64_t *empty_w = full_w + 2 * SW;
+    uint64_t *full_x = empty_w + SW;
+    uint64_t *empty_x = full_x + 2 * SX;
+    uint64_t *a_full = empty_x + SX;
+    uint64_t &acc_full = a_full[2 * SX];
+    uint64_t &acc_empty = a_full[2 * SX + 1];
+    uint64_t &fin = a_full[2 * SX + 2];
+    uint32_t &s_tmem = *reinterpret_cast<uint32_t *>(a_full + 2 * SX + 3);
+    WaitCtl &s_ctl = *reinterpret_cast<WaitCtl *>(a_full + 2 * SX + 4);
+    int &s_last = *reinterpret_cast<int *>(a_full + 2 * SX + 6);
+    unsigned long long *s_best = reinterpret_cast<unsigned long long *>(a_full + 2 * SX + 8);
+    const uint32_t xbase = smem_addr(smem_dyn);  // token ring, then the weight ring
     const uint32_t wbase = xbase + uint32_t(C::kXRing);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int u0, u1;
@@ -479,15 +505,15 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
 
 template <int MP, bool FUSED = false>
 int launch_tc_t(const StreamBatch &b, int grid, cudaStream_t s) {
-    return launch_pdl(tc_kernel<MP, FUSED>, grid, kTT, TCfg<MP>::kDynSmem, s, b);
+    return launch_pdl(tc_kernel<MP, FUSED>, grid, kTT, TCfg<MP, FUSED>::kDynSmem, s, b);
 }
 
 template <int MP, bool FUSED = false>
 int occ_tc_t(int *blocks) {
     if (cudaFuncSetAttribute(tc_kernel<MP, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(TCfg<MP>::kDynSmem)) != cudaSuccess)
+                             int(TCfg<MP, FUSED>::kDynSmem)) != cudaSuccess)
         return W12_ERR_CUDA;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, tc_kernel<MP, FUSED>, kTT, TCfg<MP>::kDynSmem) ==
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, tc_kernel<MP, FUSED>, kTT, TCfg<MP, FUSED>::kDynSmem) ==
                    cudaSuccess
                ? W12_OK
                : W12_ERR_CUDA;

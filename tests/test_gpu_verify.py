@@ -86,6 +86,7 @@ def test_verify_repeated_calls_reuse_workspace(dev, w12mod, oracle):
 
 
 @pytest.mark.parametrize("R,T,K,N", [(1, 16, 256, 5000), (2, 16, 1024, 3001), (1, 1, 128, 77),
+                                     (1, 8, 512, 3001), (2, 4, 384, 2000),
                                      (8, 16, 512, 2048), (4, 16, 384, 3000), (3, 13, 256, 2500)])
 def test_verify_lmhead_fused(dev, w12mod, oracle, R, T, K, N):
     """Fused lm_head + verify.  Drafts follow the oracle's fp64-logit argmax for

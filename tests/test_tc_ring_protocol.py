@@ -241,9 +241,9 @@ def run(SW, SX, n_units, KG, u0_off, seed, per_group=True, skip_wait=False, issu
     return True
 
 
-# ring sizes of tc_kernel<MP>: (SW, SX) for MP = 16, 32, 64, 128, and
-# neighbours (odd and even rings, tiny rings)
-CONFIGS = [(8, 4), (7, 4), (6, 4), (5, 3), (3, 3), (4, 2), (2, 2), (5, 4), (7, 3)]
+# ring sizes of tc_kernel<MP>: (SW, SX) for MP = 16, 32, 64, 128 (plain:
+# 4 / 4, fused: 5 / 3), and neighbours (odd and even rings, tiny rings)
+CONFIGS = [(8, 4), (7, 4), (6, 4), (4, 4), (5, 3), (3, 3), (4, 2), (2, 2), (5, 4), (7, 3)]
 
 
 def _cases(seeds):
