@@ -405,11 +405,13 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
             const uint32_t b4 = base4(mw.x);
             rebuild32(h0, l0, e0, b4, wlo);
             rebuild32(h1, l1, e1, b4, whi);
+            // the unit's tokens have landed, and with them the UMMAs that
+            // read this slot's A buffer last have completed; the escape
+            // entries are applied after that wait, which gives their loads
+            // more time
+            mbar_wait(&full_x[2 * sx + grp], group_parity<SX>(iu), &s_ctl, b.err);
             esc_apply(ep, wlo, uint32_t(64 * h), g.esc);
             esc_apply(ep, whi, uint32_t(64 * h + 32), g.esc);
-            // the unit's tokens have landed, and with them the UMMAs that
-            // read this slot's A buffer last have completed
-            mbar_wait(&full_x[2 * sx + grp], group_parity<SX>(iu), &s_ctl, b.err);
             tc_fence_after();
             tmem_st32(tmem + lane_off + C::kA + 64u * uint32_t(sx) + 32u * uint32_t(h), w);
             tc_fence_before();
