@@ -77,8 +77,8 @@ extern "C" {
 /* GEMM paths (w12_gemm_ex, w12_gemm_batched_ex).  All three stream the
  * weights' unit blocks with bulk copies (TMA) through a shared-memory ring,
  * stream-K over the whole GPU; they differ in the contraction.
- * W12_PATH_AUTO takes the GEMV at M = 1, mma.sync for M <= 8 and tcgen05
- * above (the fastest on GB300 at each M). */
+ * W12_PATH_AUTO takes the GEMV at M = 1 and tcgen05 above (the fastest on
+ * GB300 from 2 tokens on). */
 #define W12_PATH_AUTO 0
 #define W12_PATH_GEMV 1 /* CUDA-core bf16 FMA GEMV with warp-shuffle reduction, M <= 4   */
 #define W12_PATH_MMA 2  /* mma.sync tiles, M <= 128                                     */

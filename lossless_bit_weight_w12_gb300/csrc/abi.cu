@@ -119,13 +119,14 @@ int plan_batch(const w12_desc *d, int count, int64_t M, int path, BatchPlan *bp)
         if (!gemv_fits_32bit(&d[i])) return W12_ERR_SHAPE;
     }
     // Measured on the 27B-class layer (GB300, us per layer, GEMV / mma.sync
-    // / tcgen05, early weight stream): M = 1: 79.0 / 79.1 / 80.8,
-    // 4: 120.2 / 80.2 / 81.2, 8: - / 80.9 / 81.5, 16: - / 83.9 / 82.3,
-    // 32: - / 94.9 / 84.6, 64: - / 148 / 90.7, 128: - / 230 / 103.6.  At
-    // M = 1 the weight stream is the whole cost and the warp-shuffle GEMV does
-    // it on the CUDA cores; mma.sync serves up to 8 tokens (one 8-token
-    // fragment column) and tcgen05 takes over above.
-    if (path == W12_PATH_AUTO) path = M == 1 ? W12_PATH_GEMV : M <= 8 ? W12_PATH_MMA : W12_PATH_TC;
+    // / tcgen05, early weight stream): M = 1: 78.9 / 79.0 / 77.7,
+    // 4: 120.6 / 79.8 / 78.6, 8: - / 80.5 / 79.3, 16: - / 83.8 / 79.8,
+    // 32: - / 95.6 / 81.2, 64: - / 151 / 86.0, 128: - / 231 / 100.0.  At
+    // M = 1 the product is no dense contraction: the warp-shuffle GEMV
+    // streams the weights on the CUDA cores (1.5 % behind tcgen05 on a
+    // 16-token tile of which 15 rows would be padding); from 2 tokens on
+    // tcgen05 is the fastest.
+    if (path == W12_PATH_AUTO) path = M == 1 ? W12_PATH_GEMV : W12_PATH_TC;
     if (path == W12_PATH_GEMV && M > 4) return W12_ERR_SHAPE;
     if (path != W12_PATH_GEMV && path != W12_PATH_MMA && path != W12_PATH_TC) return W12_ERR_ARG;
     Device dv;
@@ -251,7 +252,7 @@ struct FusedPlan {
 
 int plan_fused(const w12_desc *d, int64_t M, FusedPlan *fp) {
     BatchPlan &bp = fp->bp;
-    int st = plan_batch(d, 1, M, M <= 8 ? W12_PATH_MMA : W12_PATH_TC, &bp);
+    int st = plan_batch(d, 1, M, M == 1 ? W12_PATH_MMA : W12_PATH_TC, &bp);
     if (st != W12_OK) return st;
     Device dv;
     if (query_device(&dv) != W12_OK) return W12_ERR_CUDA;

@@ -16,7 +16,8 @@
 // right moves every field of both halves into its bf16 place, the two signs
 // crossing over.  The base is at most 240, so b + code (<= 255) never carries
 // between bytes.  An escape (code 15) leaves a wrong exponent that
-// esc_apply() (or patch_escapes()) replaces.
+// patch_escapes() replaces (in the tcgen05 decoders: the column's first
+// entry in tensor memory, esc_apply_rest() the others).
 #pragma once
 
 #include <cstdint>
@@ -134,11 +135,11 @@ __device__ __forceinline__ void patch_escapes(uint32_t out[16], uint32_t m0, uin
 // while the rebuild runs: esc_begin() is called as soon as a column's meta
 // words m0 = meta[c], m1 = meta[c + 1] are in registers; it checks the
 // column's entry range (a corrupt range records W12_ERR_DEVICE and is not
-// followed) and starts the load of its first entry.  esc_apply() then
-// patches every entry whose pos falls in the 32 weights [pos0, pos0 + 32)
-// held in out[16] (pair r/2 of word r/8 ...), the first from the register,
-// any further ones (two or more escapes in one column of a group) loaded
-// then.
+// followed) and starts the load of its first entry, which the caller
+// patches once the rebuild is done; esc_apply_rest() patches every further
+// entry (two or more escapes in one column of a group) whose pos falls in
+// the 32 weights [pos0, pos0 + 32) held in out[16] (pair r/2 of word r/8
+// ...), loading each.
 struct EscPending {
     uint32_t lo, hi, e0;
 };
@@ -180,10 +181,10 @@ __device__ __forceinline__ void esc_patch_one(uint32_t out[16], uint32_t pos0, u
 
 // Patch the 32 weights of out (positions [pos0, pos0 + 32)) from a pending
 // escape range.
-__device__ __forceinline__ void esc_apply(const EscPending &e, uint32_t out[16], uint32_t pos0,
-                                          const uint16_t *esc) {
-    if (e.lo == e.hi) return;
-    esc_patch_one(out, pos0, e.e0);
+// The entries after a column's first one (the first is patched by the
+// caller).
+__device__ __forceinline__ void esc_apply_rest(const EscPending &e, uint32_t out[16], uint32_t pos0,
+                                               const uint16_t *esc) {
     for (uint32_t i = e.lo + 1; i < e.hi; ++i) esc_patch_one(out, pos0, ldg_u16(esc + i));
 }
 

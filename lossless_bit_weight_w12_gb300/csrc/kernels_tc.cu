@@ -136,7 +136,8 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// Store 32 consecutive 32-bit columns of this thread's lane.
+// Store 32 consecutive 32-bit columns of this thread's lane (the caller
+// waits: tcgen05.wait::st).
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
@@ -146,8 +147,21 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
         "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
         "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
         : "memory");
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
+
+// One 32-bit column of this thread's lane: load (tmem_ld_wait() before the
+// register is used) and store (tcgen05.wait::st before a later load).
+__device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
+    uint32_t r;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+    return r;
+}
+
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Load 4 consecutive 32-bit columns of this thread's lane (tmem_ld_wait()
 // before the registers are used).
@@ -158,6 +172,33 @@ __device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t (&r)[4]) {
 }
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// The first escape entry of each lane's column, when it falls in the lane's
+// 64 weights (already stored, word i at column ta + i: the weights at
+// k = pos0 + 2i, pos0 + 2i + 1), patched in tensor memory: the lanes that
+// have one are taken in turn, warp-wide; each turn loads the column that
+// holds the escaped weight (the same column in every lane), replaces the
+// weight's exponent in the owner lane and stores the column back.  Tensor
+// memory does the indexing, so no register select over the 32 words.
+__device__ __forceinline__ void patch_first_escapes_tmem(const EscPending &ep, uint32_t ta, uint32_t pos0,
+                                                         int lane) {
+    const uint32_t j = (ep.e0 & 0x7Fu) - pos0;
+    uint32_t todo = __ballot_sync(0xFFFFFFFFu, ep.lo != ep.hi && j < 64u);
+    tmem_st_wait();  // the tile's words are in place before any column is read back
+    if (!todo) return;
+    const uint32_t sh = (j & 1u) * 16u;
+    const uint32_t keep = ~(0x7F80u << sh), put = (ep.e0 & 0x7F80u) << sh;
+    do {
+        const int src = __ffs(todo) - 1;
+        todo &= todo - 1u;
+        const uint32_t q = __shfl_sync(0xFFFFFFFFu, j >> 1, src);
+        uint32_t x = tmem_ld1(ta + q);
+        tmem_ld_wait();
+        if (lane == src) x = (x & keep) | put;
+        tmem_st1(ta + q, x);
+        tmem_st_wait();  // a later turn may read the same column
+    } while (todo);
+}
 
 // Both rings signal a landed fill on a barrier of the decoder group that
 // owns the unit (full[2 s + (i & 1)] for unit i in slot s = i % S), so each
@@ -410,10 +451,14 @@ __global__ void __launch_bounds__(kTT, 1) tc_kernel(const __grid_constant__ Stre
             // entries are applied after that wait, which gives their loads
             // more time
             mbar_wait(&full_x[2 * sx + grp], group_parity<SX>(iu), &s_ctl, b.err);
-            esc_apply(ep, wlo, uint32_t(64 * h), g.esc);
-            esc_apply(ep, whi, uint32_t(64 * h + 32), g.esc);
+            if (__any_sync(0xFFFFFFFFu, ep.hi - ep.lo > 1u)) {  // a column's further entries (rare)
+                esc_apply_rest(ep, wlo, uint32_t(64 * h), g.esc);
+                esc_apply_rest(ep, whi, uint32_t(64 * h + 32), g.esc);
+            }
             tc_fence_after();
-            tmem_st32(tmem + lane_off + C::kA + 64u * uint32_t(sx) + 32u * uint32_t(h), w);
+            const uint32_t ta = tmem + lane_off + C::kA + 64u * uint32_t(sx) + 32u * uint32_t(h);
+            tmem_st32(ta, w);
+            patch_first_escapes_tmem(ep, ta, uint32_t(64 * h), lane);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&a_full[2 * sx + grp]);

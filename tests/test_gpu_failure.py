@@ -103,7 +103,7 @@ def test_gemm_corrupt_escape_range_is_contained(dev, w12mod, oracle, path, M):
     check_gemm(y.cpu().numpy().astype(np.float64), y_ref, s_ref, what=f"after corrupt path={path}")
 
 
-@pytest.mark.parametrize("R,T", [(1, 8), (4, 16)])  # mma.sync and tcgen05 fused kernels
+@pytest.mark.parametrize("R,T", [(1, 1), (4, 16)])  # mma.sync and tcgen05 fused kernels
 def test_lmhead_verify_corrupt_escape_range_is_contained(dev, w12mod, oracle, R, T):
     import torch
     K, N = 1024, 1000
