@@ -20,9 +20,10 @@
 //    r = 32 (w % 4) + l (tensor-memory lane r) and half h = (w % 8) / 4 of
 //    the group's 128 k.  Per unit it rebuilds its 64 weights in registers
 //    ("reconstructing bit by bit in GEMM registers", SpecPilot summary,
-//    airadar.tv English edition, "Reasons" bullet 2), patches escapes, and
-//    stores them with tcgen05.st into the A buffer of the unit's token slot
-//    (64 columns, column j holding the bf16 pair k = 2j, 2j + 1).  At the
+//    airadar.tv English edition, "Reasons" bullet 2), stores them with
+//    tcgen05.st into the A buffer of the unit's token slot (64 columns,
+//    column j holding the bf16 pair k = 2j, 2j + 1) and patches the
+//    escaped ones there, one column per escaping lane, warp-wide.  At the
 //    end of a tile piece all 16 warps read the accumulator back (tcgen05.ld;
 //    warp w takes a quarter w / 4 of the tokens) and write y or the
 //    stream-K partial slot, then run the fix-up.
