@@ -796,6 +796,17 @@ def run_w12(args):
         torch.distributed.destroy_process_group()
 
 
+def accept_rule(g, draft):
+    """The greedy acceptance rule on per-position target tokens g [R, T]
+    and drafts [R, T - 1]: accept_len = the first position whose draft
+    differs from g (T - 1 if none), next = g at that position."""
+    g = np.asarray(g)
+    R, T = g.shape
+    miss = np.asarray(draft).reshape(R, T - 1) != g[:, :T - 1]
+    acc = np.where(miss.any(axis=1), miss.argmax(axis=1), T - 1) if T > 1 else np.zeros(R, dtype=np.int64)
+    return acc, g[np.arange(R), acc]
+
+
 def bench_codec(w12, torch, dev, layer, gi, d, blob_dev, w_dev, barrier):
     """The other steps of the path, each against the measured copy bandwidth:
     the decode of gate_up's blob back to bf16 (1.5 B read + 2 B written per
@@ -988,9 +999,7 @@ def bench_stack(w12, torch, dev, args, barrier):
     w12.verify_greedy_lmhead(hidden_d, d_lm, b_lm, R, T, draft_d, acc, nxt, ws_lm, logits_out_dev=logits)
     torch.cuda.synchronize()
     g32 = np.argmax(logits.cpu().numpy(), axis=1).reshape(R, T)
-    miss = draft != g32[:, :T - 1]
-    want_acc = np.where(miss.any(axis=1), miss.argmax(axis=1), T - 1)
-    want_next = g32[np.arange(R), want_acc]
+    want_acc, want_next = accept_rule(g32, draft)
     assert acc_step == want_acc.tolist() and nxt_step == want_next.tolist(), (acc_step, nxt_step)
     # positions whose argmax on the kernel's fp32 logits differs from the
     # float64 logits' (expected 0 outside near-ties)
